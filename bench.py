@@ -1,0 +1,355 @@
+"""Throughput of the M²RNN forward recurrence on GB300: tokens·heads per second.
+
+One step = one full forward pass (gate, rank-1 write, H W contraction, tanh,
+gate lerp, readout, writeback) over the whole workload, inputs resident in HBM.
+Default workload: the 16K-context training shape B=8, T=16384, N=16, K=V=64,
+bf16 operands / fp32 state.  Inputs (0.81 GB of q, k, v, a) are larger than the
+129 MB L2, so no flush is needed between timed steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+Under torchrun (N > 1) every rank runs its own replica of the workload (the
+(batch, head) pairs are independent; there is no exchange step), and the value
+is the units of all ranks divided by the slowest rank's time.
+`--impl reference` times the fp64 CPU oracle on a bounded sample instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "M²RNN fwd tokens·heads/s at K=V=64,T=16K; % of MMA/HBM roofline"
+UNIT = "tokens·heads/s"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default=None)
+    ap.add_argument("--variant", type=int, default=0)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="target CPU time of the oracle sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            return json.load(fh), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------------- clocks sampler
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "power_w_max": max(power), "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------- CPU oracle sample
+def oracle_sample(wl, seconds: float, T_s: int | None = None):
+    """Times the fp64 oracle on a bounded sample of the workload.
+
+    The sample is every (batch, head) pair of the workload over its first T_s
+    time steps; without a given T_s it is grown until one run takes about
+    `seconds` of wall time.  Returns (units per second, sample description,
+    cores used = process CPU time / wall time, T_s).
+    """
+    from matrix_state_nonlinear_gb300.inputs import make_inputs, to_f64_numpy
+    from oracle import m2rnn_forward
+
+    fixed = T_s is not None
+    T_s = T_s or 8
+    while True:
+        inp = make_inputs(wl.with_(T=T_s), "cpu", 0)
+        arrs = {k: to_f64_numpy(v) for k, v in inp.items()}
+        c0 = time.process_time()
+        t0 = time.perf_counter()
+        m2rnn_forward(arrs["q"], arrs["k"], arrs["v"], arrs["a"], arrs["alpha"], arrs["beta"],
+                      arrs["W"], arrs["w_r"], arrs["H0"])
+        wall = time.perf_counter() - t0
+        cpu = time.process_time() - c0
+        if fixed or wall >= seconds or T_s >= wl.T:
+            break
+        grow = max(2.0, min(8.0, 1.1 * seconds / max(wall, 1e-3)))
+        T_s = min(wl.T, int(T_s * grow))
+    units = wl.B * wl.N * T_s
+    cores = max(1, round(cpu / wall)) if wall > 0 else 1
+    desc = (f"all {wl.B * wl.N} (batch, head) pairs of {wl.name} over the first {T_s} of "
+            f"{wl.T} steps (fp64 NumPy oracle, {units} token-heads, {wall:.1f} s wall)")
+    return units / wall, desc, cores, T_s
+
+
+def reference_arm(args, wl):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    per = max(2.0, min(args.cpu_seconds, 120.0 / max(1, args.steps + args.warmup)))
+    vals = []
+    _, desc, cores, T_s = oracle_sample(wl, per)          # sizes the sample (untimed)
+    for i in range(args.warmup + args.steps):
+        v, desc, cores, _ = oracle_sample(wl, per, T_s)
+        if i >= args.warmup:
+            vals.append(v)
+    value = statistics.median(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": None,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(wl),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def input_bytes(wl):
+    e = 2 if wl.dtype == "bf16" else 4
+    return wl.units * e * (2 * wl.K + wl.V + 1)
+
+
+def workload_config(wl):
+    big = input_bytes(wl) > L2_BYTES
+    return {"workload": wl.name, "B": wl.B, "T": wl.T, "N": wl.N, "K": wl.K, "V": wl.V,
+            "operands": wl.dtype, "state": "f32",
+            "l2": ("inputs larger than L2 (no flush between steps)" if big else
+                   "L2 flushed (256 MB write) between steps, outside the timed launches"),
+            "parallelism": "replicas (one independent workload per GPU)"}
+
+
+# ---------------------------------------------------------------- GPU arm
+def main():
+    args = parse()
+    from matrix_state_nonlinear_gb300.inputs import HEADLINE, WORKLOADS
+    wl = WORKLOADS[args.workload or HEADLINE]
+    if args.impl == "reference":
+        return reference_arm(args, wl)
+
+    import torch
+    import torch.distributed as dist
+
+    import __graft_entry__
+    import matrix_state_nonlinear_gb300 as pkg
+    from matrix_state_nonlinear_gb300.inputs import make_inputs
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0 or world == 1:
+        __graft_entry__.build()
+    if world > 1:
+        dist.barrier()
+    pkg.load_library()
+
+    inp = make_inputs(wl, dev, seed=rank)
+    B, T, N, K, V = wl.B, wl.T, wl.N, wl.K, wl.V
+    y = torch.empty((B, T, N, V), dtype=torch.float32, device=dev)
+    HT = torch.empty((B, N, K, V), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = None if input_bytes(wl) > L2_BYTES else torch.empty(64 << 20, dtype=torch.float32,
+                                                                  device=dev)
+
+    def step():
+        pkg.m2rnn_forward(inp, y=y, H_T=HT, variant=args.variant, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    if pkg.stream_status(stream) != 0:
+        raise RuntimeError("device status not OK after warm-up")
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    if flush is None:
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        total_ms = ev0.elapsed_time(ev1)
+    else:                                   # small inputs: flush L2 between timed launches
+        evs = []
+        for _ in range(args.steps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            step()
+            e1.record(stream)
+            evs.append((e0, e1))
+        torch.cuda.synchronize(dev)
+        total_ms = sum(a.elapsed_time(b) for a, b in evs)
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    if pkg.stream_status(stream) != 0:
+        raise RuntimeError("device status not OK after the timed steps")
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * wl.units / (ms_per_step / 1e3)
+
+    # ---- end to end: pinned host inputs -> device -> kernel -> y, H_T back to pinned host
+    e2e = None
+    if not args.no_e2e:
+        host = {k: (None if v is None else v.cpu().pin_memory()) for k, v in inp.items()}
+        dinp = {k: (None if v is None else torch.empty_like(v)) for k, v in inp.items()}
+        y_h = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
+        HT_h = torch.empty(HT.shape, dtype=HT.dtype, pin_memory=True)
+        h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
+        d2h = y_h.numel() * 4 + HT_h.numel() * 4
+
+        def e2e_step():
+            for k, v in host.items():
+                if v is not None:
+                    dinp[k].copy_(v, non_blocking=True)
+            pkg.m2rnn_forward(dinp, y=y, H_T=HT, variant=args.variant, stream=stream)
+            y_h.copy_(y, non_blocking=True)
+            HT_h.copy_(HT, non_blocking=True)
+
+        e_steps = max(3, min(args.steps, 10))
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            dist.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e_ms = e0.elapsed_time(e1) / e_steps
+        if world > 1:
+            t = torch.tensor([e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": world * wl.units / (e_ms / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms,
+               "steps": e_steps}
+
+    # ---- roofline of the forward kernel (one launch per step)
+    peaks, peak_src = load_peaks()
+    flops = 2.0 * K * V * V * wl.units
+    hbm_bytes = (wl.units * (2 * (2 * K + V + 1) + 4 * V) + N * V * V * 2
+                 + (2 if wl.h0 != "zero" else 1) * B * N * K * V * 4)
+    launch_s = ms_per_step / 1e3
+    tflops = flops / launch_s / 1e12
+    peak_t = float(peaks["bf16_tflops"])
+    roof = {"bound": "tensor", "achieved": tflops, "peak": peak_t, "unit": "TFLOP/s",
+            "frac": tflops / peak_t, "traffic": None,
+            "peak_source": f"{peak_src} bf16 dense burst (kernel timed alone)",
+            "kernel": pkg.variant_name(pkg.pick_variant(B, T, N, K, V) if args.variant == 0
+                                       else args.variant),
+            "algorithmic_flops_per_launch": flops, "algorithmic_bytes_per_launch": hbm_bytes,
+            "hbm_frac": hbm_bytes / launch_s / 1e9 / float(peaks["hbm_gbs"]),
+            "t_mma_roofline_ms": flops / (peak_t * 1e12) * 1e3,
+            "t_hbm_roofline_ms": hbm_bytes / (float(peaks["hbm_gbs"]) * 1e9) * 1e3}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        v, desc, cores, _ = oracle_sample(wl, args.cpu_seconds)
+        cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16" if wl.dtype == "bf16" else "f32", "data": "synthetic",
+                "config": workload_config(wl), "clocks": clk, "e2e": e2e,
+                "gpu_launches": args.steps, "roofline": roof, "cpu_baseline": cpu}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

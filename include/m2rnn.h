@@ -1,0 +1,122 @@
+/*
+ * m2rnn.h — C ABI of the GB300 (sm_103a) M²RNN forward-recurrence library.
+ *
+ * What it computes.  The forward pass of the M²RNN matrix-state nonlinear
+ * recurrence, as stated in the M²RNN study notes ("M²RNN: 矩阵状态非线性 RNN
+ * 的容量、表达力与系统代价", notes on arXiv:2603.14360v2):
+ *   Sec. 2.2, Eq. (13)/(17):  f_t = exp(-alpha_n * softplus(a_t + beta_n))
+ *   Sec. 2.1, Eq. (10):       Z_t = tanh(H_{t-1} W_n + k_t v_t^T)
+ *             Eq. (11):       H_t = f_t H_{t-1} + (1 - f_t) Z_t
+ *             Eq. (12):       y_t = H_t^T q_t + w_r ⊙ v_t
+ * for every (batch b, head n) independently (Sec. 2.6: each (b, n) pair is an
+ * independent work unit), starting from H_0 (zero when not given).
+ *
+ * Layout.  Every tensor is dense and row-major (innermost index last):
+ *   q, k   [B, T, N, K]     keys/queries, one row per (b, t, n)
+ *   v      [B, T, N, V]
+ *   a      [B, T, N]        gate logits a_{t,n} = (W_f x_t)_n
+ *   alpha  [N], beta [N]    gate parameters (float32); alpha_n >= 0 keeps f in [0, 1]
+ *   W      [N, V, V]        per-head transition, right-multiplied:
+ *                           (H W)_{ij} = sum_l H_{il} W_{lj}
+ *   w_r    [N, V]           value residual weight (float32)
+ *   H0     [B, N, K, V]     initial state (float32), or NULL for zeros
+ *   y      [B, T, N, V]     readout (float32), written
+ *   H_T    [B, N, K, V]     final state (float32), written unless NULL
+ *
+ * Ownership and threading.  The caller owns every buffer: device pointers
+ * (cudaMalloc'd or torch-owned) valid until the work on `stream` completes.
+ * The library allocates no device memory per call, keeps no per-call state, and
+ * only enqueues work on `stream` (a cudaStream_t passed as void*; NULL is the
+ * legacy default stream); it returns before the GPU finishes.  Calls from
+ * several host threads are safe.  H0 == H_T (in place) is allowed: the state is
+ * read once at the start and written once at the end by the same thread block.
+ * No other output may alias an input.
+ *
+ * Errors.  Arguments are validated on the host before anything is enqueued;
+ * a failed check returns an error and launches nothing.  A bounded device-side
+ * wait that gives up is recorded in a per-device status word and reported by
+ * m2rnn_stream_status().  The kernels never trap.
+ */
+#ifndef M2RNN_H
+#define M2RNN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum m2rnn_status {
+  M2RNN_OK = 0,
+  M2RNN_ERR_INVALID_ARG = 1,   /* null required pointer, B/N/K/V < 1, T < 0, misaligned pointer */
+  M2RNN_ERR_UNSUPPORTED = 2,   /* shape outside what the selected path supports */
+  M2RNN_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed */
+  M2RNN_ERR_TIMEOUT = 4        /* a bounded device wait gave up (from m2rnn_stream_status) */
+} m2rnn_status;
+
+/*
+ * fp32-operand path.  Every tensor is float32.  Supports 1 <= K, V <= 128 and
+ * any B, N >= 1, T >= 0.  tanh, exp and log1p are the accurate CUDA math
+ * functions; the contraction H W is an fp32 dot product.
+ * T == 0 writes H_T = H0 (or zeros) and no y.
+ * Returns INVALID_ARG for a null alpha/beta/W/w_r pointer, a null q/k/v/a/y
+ * pointer when T > 0 (the empty tensors of T == 0 may be NULL), B, N, K, V < 1
+ * or T < 0; UNSUPPORTED for K or V > 128; CUDA if the launch fails.
+ */
+m2rnn_status m2rnn_forward_f32(const float* q, const float* k, const float* v, const float* a,
+                               const float* alpha, const float* beta, const float* W,
+                               const float* w_r, const float* H0, float* y, float* H_T,
+                               int B, int T, int N, int K, int V, void* stream);
+
+/*
+ * bf16-operand / fp32-state path.  q, k, v, a and W are bfloat16 (passed as
+ * their uint16_t bit patterns); alpha, beta, w_r, H0, y and H_T are float32.
+ * The state H is carried in fp32 and rounded to bf16 only as the tensor-core
+ * operand of each step's H W; the rank-1 term, tanh, gate lerp and readout are
+ * fp32.  Supports K a multiple of 16 with 16 <= K <= 128 and V in
+ * {16, 32, 64, 128}.  q, k, v, W, y, H0 and H_T must be 16-byte aligned
+ * (INVALID_ARG otherwise).  Same argument rules and errors as m2rnn_forward_f32,
+ * plus UNSUPPORTED for any other K or V.
+ */
+m2rnn_status m2rnn_forward_bf16(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                const uint16_t* a, const float* alpha, const float* beta,
+                                const uint16_t* W, const float* w_r, const float* H0, float* y,
+                                float* H_T, int B, int T, int N, int K, int V, void* stream);
+
+/*
+ * As m2rnn_forward_bf16, with an explicit kernel variant (for testing each
+ * variant's parity and for measurement).  variant 0 = automatic choice (what
+ * m2rnn_forward_bf16 uses); other values are listed by m2rnn_variant_name().
+ * Returns UNSUPPORTED if the variant cannot run this shape.
+ */
+m2rnn_status m2rnn_forward_bf16_variant(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                        const uint16_t* a, const float* alpha, const float* beta,
+                                        const uint16_t* W, const float* w_r, const float* H0,
+                                        float* y, float* H_T, int B, int T, int N, int K, int V,
+                                        int variant, void* stream);
+
+/* Name of a bf16 kernel variant (NULL for an unknown id).  Id 0 is "auto". */
+const char* m2rnn_variant_name(int variant);
+
+/* The variant m2rnn_forward_bf16 would pick for this shape on the current
+ * device (>0), or 0 if no variant supports it. */
+int m2rnn_pick_variant(int B, int T, int N, int K, int V);
+
+/*
+ * Synchronises `stream`, then returns and clears the current device's status
+ * word: M2RNN_ERR_TIMEOUT if a kernel's bounded wait gave up since the last
+ * call, M2RNN_ERR_CUDA if the synchronisation itself failed, else M2RNN_OK.
+ */
+m2rnn_status m2rnn_stream_status(void* stream);
+
+/* Static, human-readable name of a status code. */
+const char* m2rnn_status_string(m2rnn_status s);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int m2rnn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* M2RNN_H */

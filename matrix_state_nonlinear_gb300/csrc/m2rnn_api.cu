@@ -1,0 +1,177 @@
+// m2rnn_api.cu — host layer behind include/m2rnn.h: argument validation, variant
+// choice, the per-device status word, and the launches.  All arithmetic of the
+// recurrence runs in the kernels of the other translation units.
+#include <mutex>
+
+#include "../../include/m2rnn.h"
+#include "m2rnn_internal.h"
+
+namespace m2rnn {
+
+// One status word per device (every device that loads the module holds its copy).
+__device__ int g_status_word = 0;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+int* status_address(int dev) {
+  static int* addr[kMaxDevices] = {};
+  static std::mutex mu;
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+    addr[dev] = static_cast<int*>(p);
+  }
+  return addr[dev];
+}
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+bool aligned(const void* p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
+
+enum Variant : int { kAuto = 0, kMmaRowWarp = 1, kNumVariants = 2 };
+
+m2rnn_status common_checks(const void* q, const void* k, const void* v, const void* a,
+                           const float* alpha, const float* beta, const void* W, const float* w_r,
+                           const float* y, int B, int T, int N, int K, int V) {
+  if (!alpha || !beta || !W || !w_r) return M2RNN_ERR_INVALID_ARG;
+  if (T > 0 && (!q || !k || !v || !a || !y)) return M2RNN_ERR_INVALID_ARG;
+  if (B < 1 || N < 1 || K < 1 || V < 1 || T < 0) return M2RNN_ERR_INVALID_ARG;
+  if ((long long)B * N > 0x7fffffffLL) return M2RNN_ERR_UNSUPPORTED;
+  return M2RNN_OK;
+}
+
+// T == 0: the final state is the initial state.
+m2rnn_status empty_sequence(const float* H0, float* H_T, int B, int N, int K, int V,
+                            cudaStream_t s) {
+  if (!H_T) return M2RNN_OK;
+  const size_t bytes = sizeof(float) * (size_t)B * N * K * V;
+  cudaError_t err = cudaSuccess;
+  if (!H0)
+    err = cudaMemsetAsync(H_T, 0, bytes, s);
+  else if (H0 != H_T)
+    err = cudaMemcpyAsync(H_T, H0, bytes, cudaMemcpyDeviceToDevice, s);
+  return err == cudaSuccess ? M2RNN_OK : M2RNN_ERR_CUDA;
+}
+
+int pick(int K, int V) { return mma_rowwarp_supports(K, V) ? kMmaRowWarp : 0; }
+
+}  // namespace
+}  // namespace m2rnn
+
+using namespace m2rnn;
+
+extern "C" {
+
+const char* m2rnn_status_string(m2rnn_status s) {
+  switch (s) {
+    case M2RNN_OK: return "ok";
+    case M2RNN_ERR_INVALID_ARG: return "invalid argument";
+    case M2RNN_ERR_UNSUPPORTED: return "unsupported shape or variant";
+    case M2RNN_ERR_CUDA: return "CUDA error";
+    case M2RNN_ERR_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+int m2rnn_version(void) { return 100; }
+
+const char* m2rnn_variant_name(int variant) {
+  switch (variant) {
+    case kAuto: return "auto";
+    case kMmaRowWarp: return "mma_sync_rowwarp";
+  }
+  return nullptr;
+}
+
+int m2rnn_pick_variant(int B, int T, int N, int K, int V) {
+  (void)B;
+  (void)T;
+  (void)N;
+  return pick(K, V);
+}
+
+m2rnn_status m2rnn_forward_f32(const float* q, const float* k, const float* v, const float* a,
+                               const float* alpha, const float* beta, const float* W,
+                               const float* w_r, const float* H0, float* y, float* H_T, int B,
+                               int T, int N, int K, int V, void* stream) {
+  m2rnn_status st = common_checks(q, k, v, a, alpha, beta, W, w_r, y, B, T, N, K, V);
+  if (st != M2RNN_OK) return st;
+  if (K > 128 || V > 128) return M2RNN_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (T == 0) return empty_sequence(H0, H_T, B, N, K, V, s);
+  Problem p{q, k, v, a, alpha, beta, W, w_r, H0, y, H_T, B, T, N, K, V, 0, nullptr};
+  return launch_fwd_f32(p, s) == cudaSuccess ? M2RNN_OK : M2RNN_ERR_CUDA;
+}
+
+m2rnn_status m2rnn_forward_bf16_variant(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                        const uint16_t* a, const float* alpha, const float* beta,
+                                        const uint16_t* W, const float* w_r, const float* H0,
+                                        float* y, float* H_T, int B, int T, int N, int K, int V,
+                                        int variant, void* stream) {
+  m2rnn_status st = common_checks(q, k, v, a, alpha, beta, W, w_r, y, B, T, N, K, V);
+  if (st != M2RNN_OK) return st;
+  const int debug = variant >> 8;
+  int base = variant & 0xff;
+  if (base < 0 || base >= kNumVariants) return M2RNN_ERR_INVALID_ARG;
+  if (base == kAuto) base = pick(K, V);
+  if (base == 0) return M2RNN_ERR_UNSUPPORTED;
+  if (base == kMmaRowWarp && !mma_rowwarp_supports(K, V)) return M2RNN_ERR_UNSUPPORTED;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(W, 16) ||
+      !aligned(y, 16) || !aligned(H0, 16) || !aligned(H_T, 16) || !aligned(a, 2))
+    return M2RNN_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (T == 0) return empty_sequence(H0, H_T, B, N, K, V, s);
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return M2RNN_ERR_CUDA;
+  int* status = status_address(dev);
+  EncodeTiledFn enc = encode_fn();
+  if (!status || !enc) return M2RNN_ERR_CUDA;
+  Problem p{q, k, v, a, alpha, beta, W, w_r, H0, y, H_T, B, T, N, K, V, debug, status};
+  cudaError_t err = cudaErrorInvalidValue;
+  switch (base) {
+    case kMmaRowWarp: err = launch_fwd_bf16_mma_rowwarp(p, enc, s); break;
+  }
+  return err == cudaSuccess ? M2RNN_OK : M2RNN_ERR_CUDA;
+}
+
+m2rnn_status m2rnn_forward_bf16(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                const uint16_t* a, const float* alpha, const float* beta,
+                                const uint16_t* W, const float* w_r, const float* H0, float* y,
+                                float* H_T, int B, int T, int N, int K, int V, void* stream) {
+  return m2rnn_forward_bf16_variant(q, k, v, a, alpha, beta, W, w_r, H0, y, H_T, B, T, N, K, V,
+                                    kAuto, stream);
+}
+
+m2rnn_status m2rnn_stream_status(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return M2RNN_ERR_CUDA;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return M2RNN_ERR_CUDA;
+  int* addr = status_address(dev);
+  if (!addr) return M2RNN_ERR_CUDA;
+  int word = 0;
+  const int zero = 0;
+  if (cudaMemcpy(&word, addr, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemcpy(addr, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+    return M2RNN_ERR_CUDA;
+  return word == kStatusTimeout ? M2RNN_ERR_TIMEOUT : M2RNN_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,51 @@
+// m2rnn_internal.h — shared between the host API layer and the kernel launchers.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace m2rnn {
+
+// Device status word values (written by kernels, read by m2rnn_stream_status).
+enum : int { kStatusOk = 0, kStatusTimeout = 4 };
+
+// Test hook carried in bits 8.. of the variant id: the kernel's first wait is on
+// a barrier that nothing arrives at, with a short limit, so the timeout path runs.
+enum : int { kDebugForceTimeout = 1 };
+
+// Bounded waits give up after this many SM cycles (about one second at 2 GHz).
+constexpr long long kWaitLimitCycles = 2000000000LL;
+// Limit used by the forced-timeout test hook (about 0.5 ms).
+constexpr long long kDebugWaitLimitCycles = 1000000LL;
+
+struct Problem {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* a;
+  const float* alpha;
+  const float* beta;
+  const void* W;
+  const float* w_r;
+  const float* H0;
+  float* y;
+  float* H_T;
+  int B, T, N, K, V;
+  int debug;        // kDebug* bits (tests only)
+  int* status;      // device address of this device's status word
+};
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// fp32 SIMT path (any 1 <= K, V <= 128).
+cudaError_t launch_fwd_f32(const Problem& p, cudaStream_t stream);
+
+// bf16 warp-MMA path: K % 16 == 0, K <= 128, V in {16, 32, 64, 128}.
+bool mma_rowwarp_supports(int K, int V);
+cudaError_t launch_fwd_bf16_mma_rowwarp(const Problem& p, EncodeTiledFn enc, cudaStream_t stream);
+
+}  // namespace m2rnn

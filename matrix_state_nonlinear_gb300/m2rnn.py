@@ -1,0 +1,174 @@
+"""Thin Python binding of the C ABI in include/m2rnn.h (argument marshalling only).
+
+Every step of the recurrence runs in the CUDA kernels of libm2rnn.so; this
+module checks tensor dtypes, devices and contiguity, passes raw device pointers
+and the current CUDA stream, and turns status codes into exceptions.  There is
+no CPU fallback: if the library is missing, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libm2rnn.so")
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = 0, 1, 2, 3, 4
+
+# Exported symbols of include/m2rnn.h, with (restype, argtypes).
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+SYMBOLS = {
+    "m2rnn_forward_f32": (_I, [_P] * 11 + [_I] * 5 + [_P]),
+    "m2rnn_forward_bf16": (_I, [_P] * 11 + [_I] * 5 + [_P]),
+    "m2rnn_forward_bf16_variant": (_I, [_P] * 11 + [_I] * 6 + [_P]),
+    "m2rnn_variant_name": (ctypes.c_char_p, [_I]),
+    "m2rnn_pick_variant": (_I, [_I] * 5),
+    "m2rnn_stream_status": (_I, [_P]),
+    "m2rnn_status_string": (ctypes.c_char_p, [_I]),
+    "m2rnn_version": (_I, []),
+}
+
+_lib = None
+
+
+class M2RNNError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status) if _lib else status} (status {status})")
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Loads libm2rnn.so once; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"libm2rnn.so not found at {path}; build it first "
+                           "(python -c 'import __graft_entry__ as g; g.build()')")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SYMBOLS.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load_library().m2rnn_status_string(int(status)).decode()
+
+
+def version() -> int:
+    return load_library().m2rnn_version()
+
+
+def variant_name(variant: int) -> str | None:
+    s = load_library().m2rnn_variant_name(int(variant))
+    return None if s is None else s.decode()
+
+
+def pick_variant(B: int, T: int, N: int, K: int, V: int) -> int:
+    return load_library().m2rnn_pick_variant(B, T, N, K, V)
+
+
+def _stream_ptr(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def stream_status(stream=None) -> int:
+    """Synchronises the stream; returns (and clears) the device status (OK or ERR_TIMEOUT)."""
+    return load_library().m2rnn_stream_status(ctypes.c_void_p(_stream_ptr(stream)))
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _check(t, name, dtype, shape, dev):
+    if t is None:
+        return
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
+    if t.device != dev:
+        raise ValueError(f"{name}: expected device {dev}, got {t.device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+
+
+def _marshal(q, k, v, a, alpha, beta, W, w_r, H0, y, H_T, opdtype):
+    if q.device.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    B, T, N, K = q.shape
+    V = v.shape[-1]
+    dev = q.device
+    for t, name, dt, shp in [(q, "q", opdtype, (B, T, N, K)), (k, "k", opdtype, (B, T, N, K)),
+                             (v, "v", opdtype, (B, T, N, V)), (a, "a", opdtype, (B, T, N)),
+                             (alpha, "alpha", torch.float32, (N,)),
+                             (beta, "beta", torch.float32, (N,)),
+                             (W, "W", opdtype, (N, V, V)), (w_r, "w_r", torch.float32, (N, V)),
+                             (H0, "H0", torch.float32, (B, N, K, V))]:
+        _check(t, name, dt, shp, dev)
+    if y is None:
+        y = torch.empty((B, T, N, V), dtype=torch.float32, device=dev)
+    _check(y, "y", torch.float32, (B, T, N, V), dev)
+    if H_T is not None:
+        _check(H_T, "H_T", torch.float32, (B, N, K, V), dev)
+    ptrs = [_ptr(x) for x in (q, k, v, a, alpha, beta, W, w_r, H0, y, H_T)]
+    return ptrs, (B, T, N, K, V), y
+
+
+def m2rnn_forward_f32(q, k, v, a, alpha, beta, W, w_r, H0=None, y=None, H_T=None, stream=None):
+    """fp32-operand forward (all tensors float32).  Returns (y, H_T)."""
+    lib = load_library()
+    ptrs, dims, y = _marshal(q, k, v, a, alpha, beta, W, w_r, H0, y, H_T, torch.float32)
+    st = lib.m2rnn_forward_f32(*ptrs, *dims, ctypes.c_void_p(_stream_ptr(stream)))
+    if st != OK:
+        raise M2RNNError(st, "m2rnn_forward_f32")
+    return y, H_T
+
+
+def m2rnn_forward_bf16_variant(q, k, v, a, alpha, beta, W, w_r, H0=None, y=None, H_T=None,
+                               variant=0, stream=None):
+    """bf16-operand / fp32-state forward with an explicit kernel variant (0 = auto)."""
+    lib = load_library()
+    ptrs, dims, y = _marshal(q, k, v, a, alpha, beta, W, w_r, H0, y, H_T, torch.bfloat16)
+    st = lib.m2rnn_forward_bf16_variant(*ptrs, *dims, int(variant),
+                                        ctypes.c_void_p(_stream_ptr(stream)))
+    if st != OK:
+        raise M2RNNError(st, "m2rnn_forward_bf16_variant")
+    return y, H_T
+
+
+def m2rnn_forward_bf16(q, k, v, a, alpha, beta, W, w_r, H0=None, y=None, H_T=None, stream=None):
+    """bf16-operand / fp32-state forward (q, k, v, a, W bfloat16; the rest float32)."""
+    lib = load_library()
+    ptrs, dims, y = _marshal(q, k, v, a, alpha, beta, W, w_r, H0, y, H_T, torch.bfloat16)
+    st = lib.m2rnn_forward_bf16(*ptrs, *dims, ctypes.c_void_p(_stream_ptr(stream)))
+    if st != OK:
+        raise M2RNNError(st, "m2rnn_forward_bf16")
+    return y, H_T
+
+
+def m2rnn_forward(inputs: dict, y=None, H_T=None, variant=0, stream=None):
+    """Forward pass on a dict keyed like the input generator's output.
+
+    Dispatches on the operand dtype of q: float32 -> the fp32 path, bfloat16 ->
+    the tensor-core path.  Allocates y and H_T (torch memory) when not given.
+    """
+    q = inputs["q"]
+    B, T, N, K = q.shape
+    V = inputs["v"].shape[-1]
+    if H_T is None:
+        H_T = torch.empty((B, N, K, V), dtype=torch.float32, device=q.device)
+    args = [inputs[x] for x in ("q", "k", "v", "a", "alpha", "beta", "W", "w_r")]
+    if q.dtype == torch.float32:
+        return m2rnn_forward_f32(*args, inputs.get("H0"), y, H_T, stream=stream)
+    return m2rnn_forward_bf16_variant(*args, inputs.get("H0"), y, H_T, variant=variant,
+                                      stream=stream)

@@ -1,0 +1,123 @@
+"""The C-ABI library builds, loads, and exports every function include/m2rnn.h declares.
+
+These run without a GPU: only calls that return before touching the device are
+made (status strings, version, variant table, and argument checks that reject a
+call before anything is enqueued).
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import __graft_entry__
+from matrix_state_nonlinear_gb300 import m2rnn as binding
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "m2rnn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    __graft_entry__.build()
+    return binding.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(m2rnn_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for must in ("m2rnn_forward_f32", "m2rnn_forward_bf16", "m2rnn_stream_status",
+                 "m2rnn_status_string"):
+        assert must in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert names, "no declarations parsed"
+    for name in names:
+        assert hasattr(lib, name), f"{name} declared in m2rnn.h but not exported"
+        assert name in binding.SYMBOLS, f"{name} has no binding"
+
+
+def test_status_strings_and_version(lib):
+    assert binding.status_string(0) == "ok"
+    assert "invalid" in binding.status_string(1)
+    assert "timed out" in binding.status_string(4)
+    assert binding.version() >= 100
+    assert binding.variant_name(0) == "auto"
+    assert binding.variant_name(999) is None
+
+
+def test_pick_variant_host_logic(lib):
+    assert binding.pick_variant(8, 16384, 16, 64, 64) > 0
+    assert binding.pick_variant(1, 64, 2, 8, 8) == 0       # K = 8: only the fp32 path
+    assert binding.pick_variant(1, 64, 2, 64, 48) == 0     # V not supported by the MMA paths
+
+
+NULL = None
+
+
+def call_f32(lib, ptrs, dims):
+    return lib.m2rnn_forward_f32(*ptrs, *dims, None)
+
+
+def call_bf16(lib, ptrs, dims, variant=0):
+    return lib.m2rnn_forward_bf16_variant(*ptrs, *dims, variant, None)
+
+
+def fake_ptrs(n=11, base=1 << 20):
+    # distinct, 256-byte aligned, never dereferenced (rejected before any launch)
+    return [base + 256 * i for i in range(n)]
+
+
+@pytest.mark.parametrize("which", range(8))
+def test_null_required_pointer_is_invalid_arg(lib, which):
+    p = fake_ptrs()
+    p[which] = None                          # q k v a alpha beta W w_r
+    assert call_f32(lib, p, (1, 4, 1, 8, 8)) == binding.ERR_INVALID_ARG
+    assert call_bf16(lib, p, (1, 4, 1, 16, 16)) == binding.ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("dims", [(0, 4, 1, 8, 8), (1, -1, 1, 8, 8), (1, 4, 0, 8, 8),
+                                  (1, 4, 1, 0, 8), (1, 4, 1, 8, 0)])
+def test_bad_sizes_are_invalid_arg(lib, dims):
+    assert call_f32(lib, fake_ptrs(), dims) == binding.ERR_INVALID_ARG
+
+
+def test_null_y_with_steps_is_invalid_arg(lib):
+    p = fake_ptrs()
+    p[9] = None
+    assert call_f32(lib, p, (1, 4, 1, 8, 8)) == binding.ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("dims", [(1, 4, 1, 129, 8), (1, 4, 1, 8, 129)])
+def test_f32_too_large_is_unsupported(lib, dims):
+    assert call_f32(lib, fake_ptrs(), dims) == binding.ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("dims", [(1, 4, 1, 8, 16), (1, 4, 1, 24, 16), (1, 4, 1, 16, 48),
+                                  (1, 4, 1, 144, 64), (1, 4, 1, 64, 256)])
+def test_bf16_unsupported_shapes(lib, dims):
+    assert call_bf16(lib, fake_ptrs(), dims) == binding.ERR_UNSUPPORTED
+
+
+def test_bf16_misaligned_is_invalid_arg(lib):
+    p = fake_ptrs()
+    p[0] += 8                                 # q not 16-byte aligned
+    assert call_bf16(lib, p, (1, 4, 1, 16, 16)) == binding.ERR_INVALID_ARG
+
+
+def test_unknown_variant_is_invalid_arg(lib):
+    assert call_bf16(lib, fake_ptrs(), (1, 4, 1, 16, 16), variant=77) == binding.ERR_INVALID_ARG
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+    from matrix_state_nonlinear_gb300.inputs import WORKLOADS, make_inputs
+    inp = make_inputs(WORKLOADS["tiny_f32_b1_t64_n2_k8_v8"], "cpu")
+    with pytest.raises(ValueError):
+        binding.m2rnn_forward(inp)
