@@ -102,6 +102,9 @@ const char* m2rnn_variant_name(int variant);
  * device (>0), or 0 if no variant supports it. */
 int m2rnn_pick_variant(int B, int T, int N, int K, int V);
 
+/* 1 if bf16 kernel variant `variant` (> 0) can run this shape, else 0. */
+int m2rnn_variant_supports(int variant, int B, int T, int N, int K, int V);
+
 /*
  * Synchronises `stream`, then returns and clears the current device's status
  * word: M2RNN_ERR_TIMEOUT if a kernel's bounded wait gave up since the last

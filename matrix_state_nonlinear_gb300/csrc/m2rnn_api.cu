@@ -44,7 +44,7 @@ EncodeTiledFn encode_fn() {
 
 bool aligned(const void* p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
 
-enum Variant : int { kAuto = 0, kMmaRowWarp = 1, kNumVariants = 2 };
+enum Variant : int { kAuto = 0, kMmaRowWarp = 1, kMmaPipe = 2, kNumVariants = 3 };
 
 m2rnn_status common_checks(const void* q, const void* k, const void* v, const void* a,
                            const float* alpha, const float* beta, const void* W, const float* w_r,
@@ -69,7 +69,19 @@ m2rnn_status empty_sequence(const float* H0, float* H_T, int B, int N, int K, in
   return err == cudaSuccess ? M2RNN_OK : M2RNN_ERR_CUDA;
 }
 
-int pick(int K, int V) { return mma_rowwarp_supports(K, V) ? kMmaRowWarp : 0; }
+int pick(int K, int V) {
+  if (mma_pipe_supports(K, V)) return kMmaPipe;
+  if (mma_rowwarp_supports(K, V)) return kMmaRowWarp;
+  return 0;
+}
+
+bool supports(int variant, int K, int V) {
+  switch (variant) {
+    case kMmaRowWarp: return mma_rowwarp_supports(K, V);
+    case kMmaPipe: return mma_pipe_supports(K, V);
+  }
+  return false;
+}
 
 }  // namespace
 }  // namespace m2rnn
@@ -95,6 +107,7 @@ const char* m2rnn_variant_name(int variant) {
   switch (variant) {
     case kAuto: return "auto";
     case kMmaRowWarp: return "mma_sync_rowwarp";
+    case kMmaPipe: return "mma_sync_pipelined";
   }
   return nullptr;
 }
@@ -104,6 +117,13 @@ int m2rnn_pick_variant(int B, int T, int N, int K, int V) {
   (void)T;
   (void)N;
   return pick(K, V);
+}
+
+int m2rnn_variant_supports(int variant, int B, int T, int N, int K, int V) {
+  (void)B;
+  (void)T;
+  (void)N;
+  return supports(variant, K, V) ? 1 : 0;
 }
 
 m2rnn_status m2rnn_forward_f32(const float* q, const float* k, const float* v, const float* a,
@@ -131,7 +151,7 @@ m2rnn_status m2rnn_forward_bf16_variant(const uint16_t* q, const uint16_t* k, co
   if (base < 0 || base >= kNumVariants) return M2RNN_ERR_INVALID_ARG;
   if (base == kAuto) base = pick(K, V);
   if (base == 0) return M2RNN_ERR_UNSUPPORTED;
-  if (base == kMmaRowWarp && !mma_rowwarp_supports(K, V)) return M2RNN_ERR_UNSUPPORTED;
+  if (!supports(base, K, V)) return M2RNN_ERR_UNSUPPORTED;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(W, 16) ||
       !aligned(y, 16) || !aligned(H0, 16) || !aligned(H_T, 16) || !aligned(a, 2))
     return M2RNN_ERR_INVALID_ARG;
@@ -147,6 +167,7 @@ m2rnn_status m2rnn_forward_bf16_variant(const uint16_t* q, const uint16_t* k, co
   cudaError_t err = cudaErrorInvalidValue;
   switch (base) {
     case kMmaRowWarp: err = launch_fwd_bf16_mma_rowwarp(p, enc, s); break;
+    case kMmaPipe: err = launch_fwd_bf16_mma_pipe(p, enc, s); break;
   }
   return err == cudaSuccess ? M2RNN_OK : M2RNN_ERR_CUDA;
 }

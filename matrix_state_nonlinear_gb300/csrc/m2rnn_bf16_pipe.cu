@@ -1,0 +1,505 @@
+// m2rnn_bf16_pipe.cu — software-pipelined bf16-operand / fp32-state forward recurrence
+// on the warp-level tensor-core MMA, for K <= 64 and V in {16, 32, 64} (W held in
+// registers).
+//
+// Same recurrence and mapping as the row-warp kernel (M²RNN study notes, Sec. 2.1
+// Eq. (10)-(12), Sec. 2.2 Eq. (13)/(17); one thread block per (batch, head) pair,
+// warp w owns rows 16w .. 16w+15 of H in registers), with two changes that let the
+// MUFU tanh and the tensor-core MMA of one warp run at the same time:
+//
+//  * Step wavefront.  The bf16 A fragment of k-tile j of H_t is packed from the
+//    accumulators of n-tiles 2j and 2j+1 alone, so the MMA of step t+1 for k-tile
+//    j can start as soon as those two n-tiles of step t have been through
+//    tanh and the gate lerp.  Each step therefore runs, for j = 0 .. V/16-1:
+//      tanh + lerp of n-tiles 2j, 2j+1 (step t)  ->  pack A_j  ->  MMA(step t+1, k-tile j)
+//    and the MMAs of k-tile j overlap the tanh of k-tile j+1.  Two accumulator
+//    sets alternate: P_t being consumed, P_{t+1} being built (initialised with the
+//    rank-1 term k_{t+1} v_{t+1}^T).
+//
+//  * Producer warp.  An extra warp issues the TMA loads of q, k, v chunks,
+//    computes the gates (f, 1 - f) of a chunk before its load is armed, and sums
+//    the per-warp readout partials (+ w_r ⊙ v) into y after the compute warps
+//    finish a chunk.  Compute warps and the producer meet only through
+//    mbarriers (full: inputs and gates ready; done: a chunk's partials written),
+//    never through a block-wide barrier inside the time loop.
+//
+// fp32 elementwise math uses the packed f32x2 instructions (two lanes of work per
+// issue slot); tanh is the MUFU tanh.approx.f32.
+#include <cuda_bf16.h>
+
+#include "m2rnn_internal.h"
+#include "ptx_util.cuh"
+
+namespace m2rnn {
+namespace {
+
+__device__ __forceinline__ uint64_t f2u(float2 v) { return *reinterpret_cast<uint64_t*>(&v); }
+__device__ __forceinline__ float2 u2f(uint64_t v) { return *reinterpret_cast<float2*>(&v); }
+
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {  // a * b + c
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(f2u(a)), "l"(f2u(b)), "l"(f2u(c)));
+  return u2f(d);
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2u(a)), "l"(f2u(b)));
+  return u2f(d);
+}
+__device__ __forceinline__ float2 bf16x2_to_float2(uint32_t u) {
+  return make_float2(bf16_lo(u), bf16_hi(u));
+}
+
+__device__ __forceinline__ void mma2(float2 (&d)[2], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0].x), "+f"(d[0].y), "+f"(d[1].x), "+f"(d[1].y)
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Bounded wait that also gives up early once another warp has raised `abort`.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, long long limit,
+                                              volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (clock64() - t0 > limit) return false;
+  }
+}
+
+struct PipeLayout {
+  int qs, ks, vs, stage_bytes;  // TMA destinations, two stages `stage_bytes` apart
+  int fg;                       // float2 [2][Tc]          (f, 1 - f) per step
+  int ypart;                    // float  [2][nw][Tc][V]   per-warp readout partials
+  int wr;                       // float  [V]
+  int bar;                      // uint64 full[2], done[2], never-armed[1]; int abort
+  int total;
+};
+
+__host__ __device__ inline int al128(int x) { return (x + 127) & ~127; }
+
+__host__ __device__ inline PipeLayout pipe_layout(int K, int V, int Tc) {
+  PipeLayout L;
+  const int nw = K / 16;
+  L.qs = 0;
+  L.ks = al128(Tc * K * 2);
+  L.vs = L.ks + al128(Tc * K * 2);
+  L.stage_bytes = L.vs + al128(Tc * V * 2);
+  int o = 2 * L.stage_bytes;
+  L.fg = o;
+  o += al128(2 * Tc * 8);
+  L.ypart = o;
+  o += al128(2 * nw * Tc * V * 4);
+  L.wr = o;
+  o += al128(V * 4);
+  L.bar = o;
+  o += 128;
+  L.total = o;
+  return L;
+}
+
+__device__ __forceinline__ float2 gate_fg(float a, float al, float be) {
+  const float x = a + be;
+  const float sp = fmaxf(x, 0.f) + log1pf(expf(-fabsf(x)));  // softplus, Eq. (17)
+  const float e = -al * sp;
+  return make_float2(expf(e), -expm1f(e));                     // (f, 1 - f)
+}
+
+template <int VT>
+__global__ void __launch_bounds__(160, 1)
+    fwd_bf16_mma_pipe(const __grid_constant__ CUtensorMap tm_q,
+                      const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v, const uint16_t* __restrict__ a,
+                      const float* __restrict__ alpha, const float* __restrict__ beta,
+                      const uint16_t* __restrict__ W, const float* __restrict__ w_r,
+                      const float* H0, float* __restrict__ y, float* H_T, int T, int N, int K,
+                      int Tc, int debug, int* status) {
+  constexpr int V = 16 * VT;
+  constexpr int NT = 2 * VT;  // n-tiles of 8 columns
+  constexpr int M = 4 * VT;   // readout partial sums per thread
+
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int nw = K / 16;  // compute warps; warp nw is the producer
+  const PipeLayout L = pipe_layout(K, V, Tc);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int pair = blockIdx.x, b = pair / N, n = pair - (pair / N) * N;
+  const int nchunks = (T + Tc - 1) / Tc;
+  const size_t row_base = (size_t)b * T;  // (b, t) row index base
+
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bar);
+  uint64_t* done = full + 2;
+  uint64_t* never = full + 4;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(full + 5);
+  float2* fgs = reinterpret_cast<float2*>(smem + L.fg);
+  float* ypart = reinterpret_cast<float*>(smem + L.ypart);
+  float* wrs = reinterpret_cast<float*>(smem + L.wr);
+  const long long limit = kWaitLimitCycles;
+
+  if (tid == 0) {
+    // Every lane of the producer (full) and of each compute warp (done) arrives, so
+    // each thread's own shared-memory writes are released by its own arrive.
+    mbar_init(&full[0], 32);
+    mbar_init(&full[1], 32);
+    mbar_init(&done[0], 32 * nw);
+    mbar_init(&done[1], 32 * nw);
+    mbar_init(never, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  for (int j = tid; j < V; j += blockDim.x) wrs[j] = w_r[(size_t)n * V + j];
+  __syncthreads();
+
+  // ======================================================= producer warp
+  if (warp == nw) {
+    const float al = alpha[n], be = beta[n];
+    const uint32_t stage_tx = (uint32_t)(2 * K + V) * (uint32_t)Tc * 2u;
+    if (lane == 0) {
+      prefetch_tensormap(&tm_q);
+      prefetch_tensormap(&tm_k);
+      prefetch_tensormap(&tm_v);
+    }
+    // Gates of chunk cc into fg[cc & 1], then arm full[cc & 1] and start the TMA.
+    auto arm = [&](int cc) {
+      const int st = cc & 1;
+      for (int s = lane; s < Tc; s += 32) {
+        const int t = cc * Tc + s;
+        const float av = t < T ? bf16_bits_to_float(a[(row_base + t) * N + n]) : 0.f;
+        fgs[st * Tc + s] = gate_fg(av, al, be);
+      }
+      __syncwarp();
+      if (lane != 0) {
+        mbar_arrive(&full[st]);
+      } else {
+        uint8_t* base = smem + st * L.stage_bytes;
+        mbar_arrive_expect_tx(&full[st], stage_tx);
+        tma_load_4d(base + L.qs, &tm_q, &full[st], 0, n, cc * Tc, b);
+        tma_load_4d(base + L.ks, &tm_k, &full[st], 0, n, cc * Tc, b);
+        tma_load_4d(base + L.vs, &tm_v, &full[st], 0, n, cc * Tc, b);
+      }
+    };
+    int issued = 0;
+    for (; issued < 2 && issued < nchunks; ++issued) arm(issued);
+
+    for (int cc = 0; cc < nchunks; ++cc) {
+      const int st = cc & 1;
+      if (!wait_or_abort(&done[st], (uint32_t)(cc >> 1) & 1u, limit, abort_flag)) {
+        if (lane == 0) {
+          *abort_flag = 1;
+          atomicExch(status, kStatusTimeout);
+          // Let TMA copies still in flight land before the block's shared memory goes away.
+          for (int ci = cc; ci < issued; ++ci)
+            mbar_wait_bounded(&full[ci & 1], (uint32_t)(ci >> 1) & 1u, kDebugWaitLimitCycles);
+        }
+        return;
+      }
+      // y_t = sum of the per-warp partials + w_r ⊙ v_t, float4 per lane.
+      const int t0 = cc * Tc;
+      const int steps = min(Tc, T - t0);
+      const uint16_t* vs = reinterpret_cast<const uint16_t*>(smem + st * L.stage_bytes + L.vs);
+      const float* yp = ypart + (size_t)st * nw * Tc * V;
+      constexpr int V4 = V / 4;
+      for (int idx = lane; idx < steps * V4; idx += 32) {
+        const int s = idx / V4, j = (idx - s * V4) * 4;
+        const uint2 vv = *reinterpret_cast<const uint2*>(vs + s * V + j);
+        const float4 w4 = *reinterpret_cast<const float4*>(wrs + j);
+        float4 o = make_float4(w4.x * bf16_lo(vv.x), w4.y * bf16_hi(vv.x), w4.z * bf16_lo(vv.y),
+                               w4.w * bf16_hi(vv.y));
+        for (int w = 0; w < nw; ++w) {
+          const float4 u = *reinterpret_cast<const float4*>(yp + ((size_t)w * Tc + s) * V + j);
+          o.x += u.x;
+          o.y += u.y;
+          o.z += u.z;
+          o.w += u.w;
+        }
+        *reinterpret_cast<float4*>(y + ((row_base + t0 + s) * N + n) * V + j) = o;
+      }
+      __syncwarp();
+      if (issued < nchunks) arm(issued++);
+    }
+    return;
+  }
+
+  // ======================================================= compute warps
+  const int g = lane >> 2, c = lane & 3;
+  const int r0 = 16 * warp + g, r1 = r0 + 8;
+
+  // W as m16n8k16 B fragments (k index = row l of W, n index = column j).
+  const uint16_t* Wn = W + (size_t)n * V * V;
+  uint32_t wb[VT][NT][2];
+#pragma unroll
+  for (int kt = 0; kt < VT; ++kt)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int col = 8 * nt + g, r = 16 * kt + 2 * c;
+      wb[kt][nt][0] = (uint32_t)Wn[r * V + col] | ((uint32_t)Wn[(r + 1) * V + col] << 16);
+      wb[kt][nt][1] = (uint32_t)Wn[(r + 8) * V + col] | ((uint32_t)Wn[(r + 9) * V + col] << 16);
+    }
+
+  // H_0 (fp32) in the accumulator layout: h[nt][0] = row r0, h[nt][1] = row r1,
+  // columns 8 nt + 2c and 8 nt + 2c + 1.
+  float2 h[NT][2];
+  if (H0) {
+    const float* hp = H0 + (size_t)pair * K * V;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      h[nt][0] = *reinterpret_cast<const float2*>(hp + (size_t)r0 * V + 8 * nt + 2 * c);
+      h[nt][1] = *reinterpret_cast<const float2*>(hp + (size_t)r1 * V + 8 * nt + 2 * c);
+    }
+  } else {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) h[nt][0] = h[nt][1] = make_float2(0.f, 0.f);
+  }
+
+  bool ok = wait_or_abort(&full[0], 0u, limit, abort_flag);
+  if (debug & kDebugForceTimeout) ok = ok && mbar_wait_bounded(never, 0u, kDebugWaitLimitCycles);
+  if (!ok) {
+    *abort_flag = 1;
+    if (lane == 0) atomicExch(status, kStatusTimeout);
+    return;
+  }
+
+  // P_0 = k_0 v_0^T + H_0 W.
+  float2 acc[NT][2];
+  uint32_t af[VT][4];
+  {
+    const uint16_t* ks = reinterpret_cast<const uint16_t*>(smem + L.ks);
+    const uint16_t* vs = reinterpret_cast<const uint16_t*>(smem + L.vs);
+    const float2 k0 = make_float2(bf16_bits_to_float(ks[r0]), bf16_bits_to_float(ks[r0]));
+    const float2 k1 = make_float2(bf16_bits_to_float(ks[r1]), bf16_bits_to_float(ks[r1]));
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const float2 vv = bf16x2_to_float2(*reinterpret_cast<const uint32_t*>(vs + 8 * nt + 2 * c));
+      acc[nt][0] = mul2(k0, vv);
+      acc[nt][1] = mul2(k1, vv);
+    }
+#pragma unroll
+    for (int kt = 0; kt < VT; ++kt) {
+      af[kt][0] = pack_bf16x2(h[2 * kt][0].x, h[2 * kt][0].y);
+      af[kt][1] = pack_bf16x2(h[2 * kt][1].x, h[2 * kt][1].y);
+      af[kt][2] = pack_bf16x2(h[2 * kt + 1][0].x, h[2 * kt + 1][0].y);
+      af[kt][3] = pack_bf16x2(h[2 * kt + 1][1].x, h[2 * kt + 1][1].y);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) mma2(acc[nt], af[kt], wb[kt][nt][0], wb[kt][nt][1]);
+    }
+  }
+
+  // One time step.  On entry `cur` holds P_t (complete) and h holds H_{t-1}; on
+  // exit h holds H_t and `nxt` holds P_{t+1} (its last MMAs may still be in flight).
+  // Program order interleaves each MMA of step t+1 with one MUFU tanh of step t, so
+  // that in-order issue keeps the tensor pipe and the MUFU busy together.
+  float2 nxt[NT][2];
+  bool aborted = false;
+  auto step = [&](float2 (&cur)[NT][2], float2 (&nx)[NT][2], int cc, int s, int steps) {
+    const int st = cc & 1;
+    const uint8_t* sbase = smem + st * L.stage_bytes;
+    const uint8_t* nbase = sbase;
+    int sn = s + 1;
+    if (s == steps - 1) {  // step t+1 is the first of the next chunk
+      nbase = smem + (st ^ 1) * L.stage_bytes;
+      sn = 0;
+      if (cc + 1 < nchunks &&
+          !wait_or_abort(&full[st ^ 1], (uint32_t)((cc + 1) >> 1) & 1u, limit, abort_flag))
+        aborted = true;
+    }
+    const float2 fg = fgs[st * Tc + s];
+    const float2 ff = make_float2(fg.x, fg.x), gg = make_float2(fg.y, fg.y);
+
+    // Rank-1 k_{t+1} v_{t+1}^T initialises P_{t+1}.  (After the last step of the
+    // sequence this reads a stale stage; the result is never used.)
+    {
+      const uint16_t* ks = reinterpret_cast<const uint16_t*>(nbase + L.ks) + sn * K;
+      const uint16_t* vs = reinterpret_cast<const uint16_t*>(nbase + L.vs) + sn * V;
+      const float kv0 = bf16_bits_to_float(ks[r0]), kv1 = bf16_bits_to_float(ks[r1]);
+      const float2 k0 = make_float2(kv0, kv0), k1 = make_float2(kv1, kv1);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const float2 vv = bf16x2_to_float2(*reinterpret_cast<const uint32_t*>(vs + 8 * nt + 2 * c));
+        nx[nt][0] = mul2(k0, vv);
+        nx[nt][1] = mul2(k1, vv);
+      }
+    }
+    // k-tile 0 of H_t.
+    {
+      float z[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float2 pv = cur[e >> 2][(e >> 1) & 1];
+        z[e] = tanh_mufu((e & 1) ? pv.y : pv.x);
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        h[e >> 1][e & 1] = fma2(gg, make_float2(z[2 * e], z[2 * e + 1]), mul2(ff, h[e >> 1][e & 1]));
+      af[0][0] = pack_bf16x2(h[0][0].x, h[0][0].y);
+      af[0][1] = pack_bf16x2(h[0][1].x, h[0][1].y);
+      af[0][2] = pack_bf16x2(h[1][0].x, h[1][0].y);
+      af[0][3] = pack_bf16x2(h[1][1].x, h[1][1].y);
+    }
+    // Phases kt = 0 .. VT-1: MMAs of step t+1 on k-tile kt, interleaved with the
+    // tanh of k-tile kt+1 of step t.
+#pragma unroll
+    for (int kt = 0; kt < VT; ++kt) {
+      float z[8];
+      constexpr int E = NT > 8 ? NT : 8;
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        if (e < NT) mma2(nx[e], af[kt], wb[kt][e][0], wb[kt][e][1]);
+        if (kt + 1 < VT && e < 8) {
+          const float2 pv = cur[2 * (kt + 1) + (e >> 2)][(e >> 1) & 1];
+          z[e] = tanh_mufu((e & 1) ? pv.y : pv.x);
+        }
+      }
+      if (kt + 1 < VT) {
+        const int n0 = 2 * (kt + 1);
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          h[n0 + (e >> 1)][e & 1] =
+              fma2(gg, make_float2(z[2 * e], z[2 * e + 1]), mul2(ff, h[n0 + (e >> 1)][e & 1]));
+        af[kt + 1][0] = pack_bf16x2(h[n0][0].x, h[n0][0].y);
+        af[kt + 1][1] = pack_bf16x2(h[n0][1].x, h[n0][1].y);
+        af[kt + 1][2] = pack_bf16x2(h[n0 + 1][0].x, h[n0 + 1][0].y);
+        af[kt + 1][3] = pack_bf16x2(h[n0 + 1][1].x, h[n0 + 1][1].y);
+      }
+    }
+
+    // Readout of H_t (Eq. (12)): q-weighted sums of this thread's two rows.
+    const uint16_t* qs = reinterpret_cast<const uint16_t*>(sbase + L.qs) + s * K;
+    const float qv0 = bf16_bits_to_float(qs[r0]), qv1 = bf16_bits_to_float(qs[r1]);
+    const float2 q0 = make_float2(qv0, qv0), q1 = make_float2(qv1, qv1);
+    float p[M];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const float2 pp = fma2(q1, h[nt][1], mul2(q0, h[nt][0]));
+      p[2 * nt] = pp.x;
+      p[2 * nt + 1] = pp.y;
+    }
+    // Reduce-scatter over the 8 row groups (lane bits 4, 3, 2).
+#pragma unroll
+    for (int stg = 0; stg < 3; ++stg) {
+      const int mask = 16 >> stg;
+      const int half = M >> (stg + 1);
+      if (half >= 1) {
+        const bool up = (lane & mask) != 0;
+#pragma unroll
+        for (int i = 0; i < (half >= 1 ? half : 1); ++i) {
+          const float send = up ? p[i] : p[i + half];
+          const float keep = up ? p[i + half] : p[i];
+          p[i] = keep + __shfl_xor_sync(0xffffffffu, send, mask);
+        }
+      } else {
+        p[0] += __shfl_xor_sync(0xffffffffu, p[0], mask);
+      }
+    }
+    // Lane (g, c) holds value slots m0 .. m0 + cnt - 1; slot m is column
+    // 8 (m >> 1) + 2c + (m & 1).
+    float* yrow = ypart + (((size_t)st * nw + warp) * Tc + s) * V;
+    if constexpr (M >= 8) {
+      constexpr int cnt = M / 8;
+#pragma unroll
+      for (int i = 0; i < cnt; ++i) {
+        const int m = cnt * g + i;
+        yrow[8 * (m >> 1) + 2 * c + (m & 1)] = p[i];
+      }
+    } else {
+      if ((g & 1) == 0) {
+        const int m = g >> 1;
+        yrow[8 * (m >> 1) + 2 * c + (m & 1)] = p[0];
+      }
+    }
+  };
+
+  for (int cc = 0; cc < nchunks; ++cc) {
+    const int steps = min(Tc, T - cc * Tc);
+    int s = 0;
+    for (; s + 1 < steps; s += 2) {  // two steps per trip: the accumulator sets swap roles
+      step(acc, nxt, cc, s, steps);
+      step(nxt, acc, cc, s + 1, steps);
+      if (aborted) break;
+    }
+    if (s < steps && !aborted) {  // odd tail of the last chunk
+      step(acc, nxt, cc, s, steps);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        acc[nt][0] = nxt[nt][0];
+        acc[nt][1] = nxt[nt][1];
+      }
+    }
+    if (aborted) {
+      *abort_flag = 1;
+      if (lane == 0) atomicExch(status, kStatusTimeout);
+      return;
+    }
+    mbar_arrive(&done[cc & 1]);
+  }
+
+  if (H_T) {
+    float* hp = H_T + (size_t)pair * K * V;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      *reinterpret_cast<float2*>(hp + (size_t)r0 * V + 8 * nt + 2 * c) = h[nt][0];
+      *reinterpret_cast<float2*>(hp + (size_t)r1 * V + 8 * nt + 2 * c) = h[nt][1];
+    }
+  }
+}
+
+bool make_map_pipe(EncodeTiledFn enc, CUtensorMap* map, const void* base, int inner, int N, int T,
+                   int B, int Tc) {
+  const cuuint64_t dims[4] = {(cuuint64_t)inner, (cuuint64_t)N, (cuuint64_t)T, (cuuint64_t)B};
+  const cuuint64_t strides[3] = {(cuuint64_t)inner * 2, (cuuint64_t)inner * 2 * N,
+                                 (cuuint64_t)inner * 2 * N * T};
+  const cuuint32_t box[4] = {(cuuint32_t)inner, 1u, (cuuint32_t)Tc, 1u};
+  const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int VT>
+cudaError_t launch_pipe_vt(const Problem& p, EncodeTiledFn enc, cudaStream_t stream) {
+  const int V = 16 * VT;
+  int Tc = 64;
+  PipeLayout L = pipe_layout(p.K, V, Tc);
+  while (L.total > 227 * 1024 && Tc > 8) {
+    Tc /= 2;
+    L = pipe_layout(p.K, V, Tc);
+  }
+  CUtensorMap mq, mk, mv;
+  if (!make_map_pipe(enc, &mq, p.q, p.K, p.N, p.T, p.B, Tc) ||
+      !make_map_pipe(enc, &mk, p.k, p.K, p.N, p.T, p.B, Tc) ||
+      !make_map_pipe(enc, &mv, p.v, V, p.N, p.T, p.B, Tc))
+    return cudaErrorInvalidValue;
+  auto kern = fwd_bf16_mma_pipe<VT>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
+  if (err != cudaSuccess) return err;
+  const unsigned grid = (unsigned)p.B * (unsigned)p.N;
+  const int threads = 32 * (p.K / 16 + 1);
+  kern<<<grid, threads, L.total, stream>>>(mq, mk, mv, (const uint16_t*)p.a, p.alpha, p.beta,
+                                           (const uint16_t*)p.W, p.w_r, p.H0, p.y, p.H_T, p.T, p.N,
+                                           p.K, Tc, p.debug, p.status);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool mma_pipe_supports(int K, int V) {
+  // At most 4 compute warps + the producer (160 threads) keep the whole working
+  // set (H, two accumulator sets, A and W fragments) in registers without spills.
+  return K >= 16 && K <= 64 && K % 16 == 0 && (V == 16 || V == 32 || V == 64);
+}
+
+cudaError_t launch_fwd_bf16_mma_pipe(const Problem& p, EncodeTiledFn enc, cudaStream_t stream) {
+  switch (p.V) {
+    case 16: return launch_pipe_vt<1>(p, enc, stream);
+    case 32: return launch_pipe_vt<2>(p, enc, stream);
+    case 64: return launch_pipe_vt<4>(p, enc, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace m2rnn

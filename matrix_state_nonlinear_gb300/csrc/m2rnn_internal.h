@@ -48,4 +48,9 @@ cudaError_t launch_fwd_f32(const Problem& p, cudaStream_t stream);
 bool mma_rowwarp_supports(int K, int V);
 cudaError_t launch_fwd_bf16_mma_rowwarp(const Problem& p, EncodeTiledFn enc, cudaStream_t stream);
 
+// bf16 software-pipelined warp-MMA path with a producer warp: K % 16 == 0,
+// K <= 64, V in {16, 32, 64}.
+bool mma_pipe_supports(int K, int V);
+cudaError_t launch_fwd_bf16_mma_pipe(const Problem& p, EncodeTiledFn enc, cudaStream_t stream);
+
 }  // namespace m2rnn

@@ -26,6 +26,7 @@ SYMBOLS = {
     "m2rnn_forward_bf16_variant": (_I, [_P] * 11 + [_I] * 6 + [_P]),
     "m2rnn_variant_name": (ctypes.c_char_p, [_I]),
     "m2rnn_pick_variant": (_I, [_I] * 5),
+    "m2rnn_variant_supports": (_I, [_I] * 6),
     "m2rnn_stream_status": (_I, [_P]),
     "m2rnn_status_string": (ctypes.c_char_p, [_I]),
     "m2rnn_version": (_I, []),
@@ -72,6 +73,10 @@ def variant_name(variant: int) -> str | None:
 
 def pick_variant(B: int, T: int, N: int, K: int, V: int) -> int:
     return load_library().m2rnn_pick_variant(B, T, N, K, V)
+
+
+def variant_supports(variant: int, B: int, T: int, N: int, K: int, V: int) -> bool:
+    return bool(load_library().m2rnn_variant_supports(variant, B, T, N, K, V))
 
 
 def _stream_ptr(stream) -> int:

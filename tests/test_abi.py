@@ -52,6 +52,15 @@ def test_status_strings_and_version(lib):
     assert binding.variant_name(999) is None
 
 
+def test_variant_support_table(lib):
+    assert binding.variant_supports(1, 1, 8, 1, 128, 128)
+    assert binding.variant_supports(2, 1, 8, 1, 64, 64)
+    assert not binding.variant_supports(2, 1, 8, 1, 128, 64)   # pipelined: K <= 64
+    assert not binding.variant_supports(2, 1, 8, 1, 64, 128)   # pipelined: V <= 64
+    assert not binding.variant_supports(0, 1, 8, 1, 64, 64)    # 0 is "auto", not a kernel
+    assert binding.variant_name(2) is not None
+
+
 def test_pick_variant_host_logic(lib):
     assert binding.pick_variant(8, 16384, 16, 64, 64) > 0
     assert binding.pick_variant(1, 64, 2, 8, 8) == 0       # K = 8: only the fp32 path

@@ -103,15 +103,15 @@ BF16_SHAPES = [(1, 1, 1, 16, 16), (1, 2, 1, 16, 32), (3, 17, 1, 16, 64), (1, 63,
 
 
 def bf16_variants():
-    return [1]
+    return [1, 2]
 
 
 @pytest.mark.parametrize("B,T,N,K,V", BF16_SHAPES)
 @pytest.mark.parametrize("h0", ["zero", "uniform"])
 @pytest.mark.parametrize("variant", bf16_variants())
 def test_bf16_shapes(B, T, N, K, V, h0, variant):
-    if not binding.load_library().m2rnn_pick_variant(B, T, N, K, V):
-        pytest.skip("shape not supported")
+    if not binding.variant_supports(variant, B, T, N, K, V):
+        pytest.skip(f"variant {variant} does not support K={K}, V={V}")
     wl = Workload("bf16", B, T, N, K, V, h0=h0)
     check_full(wl, TOL_BF16, variant=variant, seed=B * 7 + T + K)
 
