@@ -299,15 +299,12 @@ __global__ void __launch_bounds__(160, 1)
   auto step = [&](float2 (&cur)[NT][2], float2 (&nx)[NT][2], int cc, int s, int steps) {
     const int st = cc & 1;
     const uint8_t* sbase = smem + st * L.stage_bytes;
-    const uint8_t* nbase = sbase;
-    int sn = s + 1;
-    if (s == steps - 1) {  // step t+1 is the first of the next chunk
-      nbase = smem + (st ^ 1) * L.stage_bytes;
-      sn = 0;
-      if (cc + 1 < nchunks &&
-          !wait_or_abort(&full[st ^ 1], (uint32_t)((cc + 1) >> 1) & 1u, limit, abort_flag))
-        aborted = true;
-    }
+    // Step t+1 is the first of the next chunk when s is the chunk's last step (its
+    // inputs were waited for before this step).  Selects, not branches, so that a
+    // step body stays one basic block the compiler can schedule as a whole.
+    const bool last = s == steps - 1;
+    const uint8_t* nbase = last ? smem + (st ^ 1) * L.stage_bytes : sbase;
+    const int sn = last ? 0 : s + 1;
     const float2 fg = fgs[st * Tc + s];
     const float2 ff = make_float2(fg.x, fg.x), gg = make_float2(fg.y, fg.y);
 
@@ -416,13 +413,22 @@ __global__ void __launch_bounds__(160, 1)
 
   for (int cc = 0; cc < nchunks; ++cc) {
     const int steps = min(Tc, T - cc * Tc);
+    // The chunk's last step reads k_{t+1}, v_{t+1} from the next chunk: wait for it
+    // before the two-step trip (or the odd tail) that contains that step.
+    auto wait_next = [&]() {
+      if (cc + 1 < nchunks &&
+          !wait_or_abort(&full[(cc + 1) & 1], (uint32_t)((cc + 1) >> 1) & 1u, limit, abort_flag))
+        aborted = true;
+    };
     int s = 0;
     for (; s + 1 < steps; s += 2) {  // two steps per trip: the accumulator sets swap roles
+      if (s + 2 >= steps) wait_next();
+      if (aborted) break;
       step(acc, nxt, cc, s, steps);
       step(nxt, acc, cc, s + 1, steps);
-      if (aborted) break;
     }
     if (s < steps && !aborted) {  // odd tail of the last chunk
+      wait_next();
       step(acc, nxt, cc, s, steps);
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
