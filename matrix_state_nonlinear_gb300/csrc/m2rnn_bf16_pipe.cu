@@ -16,6 +16,11 @@
 //    sets alternate: P_t being consumed, P_{t+1} being built (initialised with the
 //    rank-1 term k_{t+1} v_{t+1}^T).
 //
+//  * Deferred readout.  The q-weighted row sums of H_t are formed at the end of step
+//    t, but their shuffle reduce-scatter runs one stage per k-tile phase of step
+//    t+1, so the dependent shuffle chain overlaps that step's MUFU and MMA work
+//    instead of stalling the in-order issue of one warp.
+//
 //  * Producer warp.  An extra warp issues the TMA loads of q, k, v chunks,
 //    computes the gates (f, 1 - f) of a chunk before its load is armed, and sums
 //    the per-warp readout partials (+ w_r ⊙ v) into y after the compute warps
@@ -77,7 +82,8 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, lo
 struct PipeLayout {
   int qs, ks, vs, stage_bytes;  // TMA destinations, two stages `stage_bytes` apart
   int fg;                       // float2 [2][Tc]          (f, 1 - f) per step
-  int ypart;                    // float  [2][nw][Tc][V]   per-warp readout partials
+  int ypart;                    // float  [2][nw][Tc+1][V] per-warp readout partials (row Tc: scratch
+                                //                          target of the empty first pending readout)
   int wr;                       // float  [V]
   int bar;                      // uint64 full[2], done[2], never-armed[1]; int abort
   int total;
@@ -96,7 +102,7 @@ __host__ __device__ inline PipeLayout pipe_layout(int K, int V, int Tc) {
   L.fg = o;
   o += al128(2 * Tc * 8);
   L.ypart = o;
-  o += al128(2 * nw * Tc * V * 4);
+  o += al128(2 * nw * (Tc + 1) * V * 4);
   L.wr = o;
   o += al128(V * 4);
   L.bar = o;
@@ -203,7 +209,7 @@ __global__ void __launch_bounds__(160, 1)
       const int t0 = cc * Tc;
       const int steps = min(Tc, T - t0);
       const uint16_t* vs = reinterpret_cast<const uint16_t*>(smem + st * L.stage_bytes + L.vs);
-      const float* yp = ypart + (size_t)st * nw * Tc * V;
+      const float* yp = ypart + (size_t)st * nw * (Tc + 1) * V;
       constexpr int V4 = V / 4;
       for (int idx = lane; idx < steps * V4; idx += 32) {
         const int s = idx / V4, j = (idx - s * V4) * 4;
@@ -212,7 +218,7 @@ __global__ void __launch_bounds__(160, 1)
         float4 o = make_float4(w4.x * bf16_lo(vv.x), w4.y * bf16_hi(vv.x), w4.z * bf16_lo(vv.y),
                                w4.w * bf16_hi(vv.y));
         for (int w = 0; w < nw; ++w) {
-          const float4 u = *reinterpret_cast<const float4*>(yp + ((size_t)w * Tc + s) * V + j);
+          const float4 u = *reinterpret_cast<const float4*>(yp + ((size_t)w * (Tc + 1) + s) * V + j);
           o.x += u.x;
           o.y += u.y;
           o.z += u.z;
@@ -296,7 +302,43 @@ __global__ void __launch_bounds__(160, 1)
   // that in-order issue keeps the tensor pipe and the MUFU busy together.
   float2 nxt[NT][2];
   bool aborted = false;
-  auto step = [&](float2 (&cur)[NT][2], float2 (&nx)[NT][2], int cc, int s, int steps) {
+  // Reduce-scatter stage `stg` of a pending readout (lane bits 4, 3, 2), and its store.
+  auto red_stage = [&](float (&p)[M], int stg) {
+    const int mask = 16 >> stg;
+    const int half = M >> (stg + 1);
+    if (half >= 1) {
+      const bool up = (lane & mask) != 0;
+#pragma unroll
+      for (int i = 0; i < (half >= 1 ? half : 1); ++i) {
+        const float send = up ? p[i] : p[i + half];
+        const float keep = up ? p[i + half] : p[i];
+        p[i] = keep + __shfl_xor_sync(0xffffffffu, send, mask);
+      }
+    } else {
+      p[0] += __shfl_xor_sync(0xffffffffu, p[0], mask);
+    }
+  };
+  auto red_store = [&](float (&p)[M], float* yrow) {
+    if constexpr (M >= 8) {
+      constexpr int cnt = M / 8;
+#pragma unroll
+      for (int i = 0; i < cnt; ++i) {
+        const int m = cnt * g + i;
+        yrow[8 * (m >> 1) + 2 * c + (m & 1)] = p[i];
+      }
+    } else {
+      if ((g & 1) == 0) {
+        const int m = g >> 1;
+        yrow[8 * (m >> 1) + 2 * c + (m & 1)] = p[0];
+      }
+    }
+  };
+  auto yrow_of = [&](int cc, int s) {
+    return ypart + (((size_t)(cc & 1) * nw + warp) * (Tc + 1) + s) * V;
+  };
+  auto step = [&](float2 (&cur)[NT][2], float2 (&nx)[NT][2], int cc, int s, int steps,
+                  float (&pin)[M], float (&pout)[M]) {
+    float* pin_row = yrow_of(cc, s > 0 ? s - 1 : Tc);
     const int st = cc & 1;
     const uint8_t* sbase = smem + st * L.stage_bytes;
     // Step t+1 is the first of the next chunk when s is the chunk's last step (its
@@ -338,6 +380,7 @@ __global__ void __launch_bounds__(160, 1)
       af[0][2] = pack_bf16x2(h[1][0].x, h[1][0].y);
       af[0][3] = pack_bf16x2(h[1][1].x, h[1][1].y);
     }
+    red_stage(pin, 0);
     // Phases kt = 0 .. VT-1: MMAs of step t+1 on k-tile kt, interleaved with the
     // tanh of k-tile kt+1 of step t.
 #pragma unroll
@@ -363,6 +406,11 @@ __global__ void __launch_bounds__(160, 1)
         af[kt + 1][2] = pack_bf16x2(h[n0 + 1][0].x, h[n0 + 1][0].y);
         af[kt + 1][3] = pack_bf16x2(h[n0 + 1][1].x, h[n0 + 1][1].y);
       }
+      if (kt == 0) red_stage(pin, 1);
+      if (kt == (VT > 1 ? 1 : 0)) {
+        red_stage(pin, 2);
+        red_store(pin, pin_row);
+      }
     }
 
     // Readout of H_t (Eq. (12)): q-weighted sums of this thread's two rows.
@@ -376,41 +424,14 @@ __global__ void __launch_bounds__(160, 1)
       p[2 * nt] = pp.x;
       p[2 * nt + 1] = pp.y;
     }
-    // Reduce-scatter over the 8 row groups (lane bits 4, 3, 2).
+    // This step's partial sums are reduced during the next step (or at chunk end).
 #pragma unroll
-    for (int stg = 0; stg < 3; ++stg) {
-      const int mask = 16 >> stg;
-      const int half = M >> (stg + 1);
-      if (half >= 1) {
-        const bool up = (lane & mask) != 0;
-#pragma unroll
-        for (int i = 0; i < (half >= 1 ? half : 1); ++i) {
-          const float send = up ? p[i] : p[i + half];
-          const float keep = up ? p[i + half] : p[i];
-          p[i] = keep + __shfl_xor_sync(0xffffffffu, send, mask);
-        }
-      } else {
-        p[0] += __shfl_xor_sync(0xffffffffu, p[0], mask);
-      }
-    }
-    // Lane (g, c) holds value slots m0 .. m0 + cnt - 1; slot m is column
-    // 8 (m >> 1) + 2c + (m & 1).
-    float* yrow = ypart + (((size_t)st * nw + warp) * Tc + s) * V;
-    if constexpr (M >= 8) {
-      constexpr int cnt = M / 8;
-#pragma unroll
-      for (int i = 0; i < cnt; ++i) {
-        const int m = cnt * g + i;
-        yrow[8 * (m >> 1) + 2 * c + (m & 1)] = p[i];
-      }
-    } else {
-      if ((g & 1) == 0) {
-        const int m = g >> 1;
-        yrow[8 * (m >> 1) + 2 * c + (m & 1)] = p[0];
-      }
-    }
+    for (int i = 0; i < M; ++i) pout[i] = p[i];
   };
 
+  float pA[M], pB[M];
+#pragma unroll
+  for (int i = 0; i < M; ++i) pA[i] = pB[i] = 0.f;
   for (int cc = 0; cc < nchunks; ++cc) {
     const int steps = min(Tc, T - cc * Tc);
     // The chunk's last step reads k_{t+1}, v_{t+1} from the next chunk: wait for it
@@ -421,15 +442,17 @@ __global__ void __launch_bounds__(160, 1)
         aborted = true;
     };
     int s = 0;
+    bool tail = false;
     for (; s + 1 < steps; s += 2) {  // two steps per trip: the accumulator sets swap roles
       if (s + 2 >= steps) wait_next();
       if (aborted) break;
-      step(acc, nxt, cc, s, steps);
-      step(nxt, acc, cc, s + 1, steps);
+      step(acc, nxt, cc, s, steps, pA, pB);
+      step(nxt, acc, cc, s + 1, steps, pB, pA);
     }
     if (s < steps && !aborted) {  // odd tail of the last chunk
       wait_next();
-      step(acc, nxt, cc, s, steps);
+      step(acc, nxt, cc, s, steps, pA, pB);
+      tail = true;
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         acc[nt][0] = nxt[nt][0];
@@ -440,6 +463,14 @@ __global__ void __launch_bounds__(160, 1)
       *abort_flag = 1;
       if (lane == 0) atomicExch(status, kStatusTimeout);
       return;
+    }
+    {  // flush the chunk's last pending readout
+      float* row = yrow_of(cc, steps - 1);
+      if (tail) {
+        red_stage(pB, 0); red_stage(pB, 1); red_stage(pB, 2); red_store(pB, row);
+      } else {
+        red_stage(pA, 0); red_stage(pA, 1); red_stage(pA, 2); red_store(pA, row);
+      }
     }
     mbar_arrive(&done[cc & 1]);
   }
