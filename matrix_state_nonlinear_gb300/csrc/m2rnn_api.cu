@@ -44,7 +44,7 @@ EncodeTiledFn encode_fn() {
 
 bool aligned(const void* p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
 
-enum Variant : int { kAuto = 0, kMmaRowWarp = 1, kMmaPipe = 2, kNumVariants = 3 };
+enum Variant : int { kAuto = 0, kMmaRowWarp = 1, kMmaPipe = 2, kTc5 = 3, kNumVariants = 4 };
 
 m2rnn_status common_checks(const void* q, const void* k, const void* v, const void* a,
                            const float* alpha, const float* beta, const void* W, const float* w_r,
@@ -70,6 +70,7 @@ m2rnn_status empty_sequence(const float* H0, float* H_T, int B, int N, int K, in
 }
 
 int pick(int K, int V) {
+  if (tc5_supports(K, V)) return kTc5;
   if (mma_pipe_supports(K, V)) return kMmaPipe;
   if (mma_rowwarp_supports(K, V)) return kMmaRowWarp;
   return 0;
@@ -79,6 +80,7 @@ bool supports(int variant, int K, int V) {
   switch (variant) {
     case kMmaRowWarp: return mma_rowwarp_supports(K, V);
     case kMmaPipe: return mma_pipe_supports(K, V);
+    case kTc5: return tc5_supports(K, V);
   }
   return false;
 }
@@ -108,6 +110,7 @@ const char* m2rnn_variant_name(int variant) {
     case kAuto: return "auto";
     case kMmaRowWarp: return "mma_sync_rowwarp";
     case kMmaPipe: return "mma_sync_pipelined";
+    case kTc5: return "tcgen05_k128_v128";
   }
   return nullptr;
 }
@@ -168,6 +171,7 @@ m2rnn_status m2rnn_forward_bf16_variant(const uint16_t* q, const uint16_t* k, co
   switch (base) {
     case kMmaRowWarp: err = launch_fwd_bf16_mma_rowwarp(p, enc, s); break;
     case kMmaPipe: err = launch_fwd_bf16_mma_pipe(p, enc, s); break;
+    case kTc5: err = launch_fwd_bf16_tc5(p, enc, s); break;
   }
   return err == cudaSuccess ? M2RNN_OK : M2RNN_ERR_CUDA;
 }

@@ -38,47 +38,6 @@
 namespace m2rnn {
 namespace {
 
-__device__ __forceinline__ uint64_t f2u(float2 v) { return *reinterpret_cast<uint64_t*>(&v); }
-__device__ __forceinline__ float2 u2f(uint64_t v) { return *reinterpret_cast<float2*>(&v); }
-
-__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {  // a * b + c
-  uint64_t d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(f2u(a)), "l"(f2u(b)), "l"(f2u(c)));
-  return u2f(d);
-}
-__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
-  uint64_t d;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2u(a)), "l"(f2u(b)));
-  return u2f(d);
-}
-__device__ __forceinline__ float2 bf16x2_to_float2(uint32_t u) {
-  return make_float2(bf16_lo(u), bf16_hi(u));
-}
-
-__device__ __forceinline__ void mma2(float2 (&d)[2], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
-      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-      : "+f"(d[0].x), "+f"(d[0].y), "+f"(d[1].x), "+f"(d[1].y)
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-// Bounded wait that also gives up early once another warp has raised `abort`.
-__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, long long limit,
-                                              volatile int* abort) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const long long t0 = clock64();
-  while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (*abort) return false;
-    if (clock64() - t0 > limit) return false;
-  }
-}
-
 struct PipeLayout {
   int qs, ks, vs, stage_bytes;  // TMA destinations, two stages `stage_bytes` apart
   int fg;                       // float2 [2][Tc]          (f, 1 - f) per step
@@ -109,13 +68,6 @@ __host__ __device__ inline PipeLayout pipe_layout(int K, int V, int Tc) {
   o += 128;
   L.total = o;
   return L;
-}
-
-__device__ __forceinline__ float2 gate_fg(float a, float al, float be) {
-  const float x = a + be;
-  const float sp = fmaxf(x, 0.f) + log1pf(expf(-fabsf(x)));  // softplus, Eq. (17)
-  const float e = -al * sp;
-  return make_float2(expf(e), -expm1f(e));                     // (f, 1 - f)
 }
 
 template <int VT>

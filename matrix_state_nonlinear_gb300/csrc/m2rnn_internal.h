@@ -53,4 +53,9 @@ cudaError_t launch_fwd_bf16_mma_rowwarp(const Problem& p, EncodeTiledFn enc, cud
 bool mma_pipe_supports(int K, int V);
 cudaError_t launch_fwd_bf16_mma_pipe(const Problem& p, EncodeTiledFn enc, cudaStream_t stream);
 
+// bf16 path on the 5th-generation tensor cores (tcgen05, tensor-memory accumulators),
+// one pair per thread block, two blocks per SM: K = V = 128.
+bool tc5_supports(int K, int V);
+cudaError_t launch_fwd_bf16_tc5(const Problem& p, EncodeTiledFn enc, cudaStream_t stream);
+
 }  // namespace m2rnn

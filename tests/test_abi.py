@@ -58,6 +58,9 @@ def test_variant_support_table(lib):
     assert not binding.variant_supports(2, 1, 8, 1, 128, 64)   # pipelined: K <= 64
     assert not binding.variant_supports(2, 1, 8, 1, 64, 128)   # pipelined: V <= 64
     assert not binding.variant_supports(0, 1, 8, 1, 64, 64)    # 0 is "auto", not a kernel
+    assert binding.variant_supports(3, 1, 8, 1, 128, 128)      # tcgen05: K = V = 128 only
+    assert not binding.variant_supports(3, 1, 8, 1, 64, 128)
+    assert binding.pick_variant(16, 8192, 32, 128, 128) == 3
     assert binding.variant_name(2) is not None
 
 

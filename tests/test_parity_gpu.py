@@ -103,7 +103,7 @@ BF16_SHAPES = [(1, 1, 1, 16, 16), (1, 2, 1, 16, 32), (3, 17, 1, 16, 64), (1, 63,
 
 
 def bf16_variants():
-    return [1, 2]
+    return [1, 2, 3]
 
 
 @pytest.mark.parametrize("B,T,N,K,V", BF16_SHAPES)
