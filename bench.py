@@ -45,6 +45,8 @@ def parse():
                     help="target CPU time of the oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override B of the workload (smaller cases for profiling)")
     return ap.parse_args()
 
 
@@ -53,6 +55,44 @@ def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return rank, world, local
+
+
+KERNEL_SOURCES = {
+    "mma_sync_rowwarp": ["m2rnn_bf16_mma.cu"],
+    "mma_sync_pipelined": ["m2rnn_bf16_pipe.cu"],
+    "tcgen05_k128_v128": ["m2rnn_bf16_tc5.cu"],
+}
+
+
+def kernel_source_hash(variant_name):
+    """sha256 over the kernel's source file and the shared device helpers."""
+    import hashlib
+    csrc = os.path.join(ROOT, "matrix_state_nonlinear_gb300", "csrc")
+    hsh = hashlib.sha256()
+    for f in KERNEL_SOURCES.get(variant_name, []) + ["ptx_util.cuh"]:
+        with open(os.path.join(csrc, f), "rb") as fh:
+            hsh.update(fh.read())
+    return hsh.hexdigest()
+
+
+def measured_traffic(variant_name, wl):
+    """DRAM bytes per launch from the committed ncu capture, scaled to this workload.
+
+    profiles/traffic.json records, per kernel, dram__bytes_read.sum +
+    dram__bytes_write.sum of one captured launch, the units (token-heads) that launch
+    processed and the source hash of the kernel at capture time.  Traffic grows in
+    proportion to the units processed (every input row is read once and every output
+    row written once), so it is scaled by units.  Returns None when there is no capture
+    or the kernel has changed since it was taken.
+    """
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as fh:
+        rec = json.load(fh).get(variant_name)
+    if not rec or rec.get("source_sha256") != kernel_source_hash(variant_name):
+        return None
+    return rec["bytes_per_launch"] * wl.units / rec["units"]
 
 
 def load_peaks():
@@ -202,6 +242,8 @@ def main():
     args = parse()
     from matrix_state_nonlinear_gb300.inputs import HEADLINE, WORKLOADS
     wl = WORKLOADS[args.workload or HEADLINE]
+    if args.batch:
+        wl = wl.with_(B=args.batch, name=f"{wl.name}_b{args.batch}")
     if args.impl == "reference":
         return reference_arm(args, wl)
 
@@ -324,7 +366,7 @@ def main():
     tflops = flops / launch_s / 1e12
     peak_t = float(peaks["bf16_tflops"])
     roof = {"bound": "tensor", "achieved": tflops, "peak": peak_t, "unit": "TFLOP/s",
-            "frac": tflops / peak_t, "traffic": None,
+            "frac": tflops / peak_t,
             "peak_source": f"{peak_src} bf16 dense burst (kernel timed alone)",
             "kernel": pkg.variant_name(pkg.pick_variant(B, T, N, K, V) if args.variant == 0
                                        else args.variant),
@@ -332,6 +374,11 @@ def main():
             "hbm_frac": hbm_bytes / launch_s / 1e9 / float(peaks["hbm_gbs"]),
             "t_mma_roofline_ms": flops / (peak_t * 1e12) * 1e3,
             "t_hbm_roofline_ms": hbm_bytes / (float(peaks["hbm_gbs"]) * 1e9) * 1e3}
+    roof["traffic"] = measured_traffic(roof["kernel"], wl)
+    # The MUFU tanh floor: K*V tanh per token-head at 16 per clock per SM (measured rate).
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    mhz = clk.get("sm_mhz") or 1950.0
+    roof["t_mufu_tanh_floor_ms"] = K * V * wl.units / (16.0 * sms * mhz * 1e6) * 1e3
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
