@@ -95,6 +95,25 @@ m2rnn_status m2rnn_forward_bf16_variant(const uint16_t* q, const uint16_t* k, co
                                         float* y, float* H_T, int B, int T, int N, int K, int V,
                                         int variant, void* stream);
 
+/*
+ * Multi-value sharing (the notes' Sec. 2.4: one query/key set shared by all value
+ * heads, N_q = N_k = 1, while each head keeps its own v, f, W and state).  As
+ * m2rnn_forward_f32 / m2rnn_forward_bf16_variant, with q and k of shape
+ * [B, T, Nqk, K]: Nqk == N gives one query/key vector per head (the plain entry
+ * points), Nqk == 1 uses the same q_t, k_t for every head n.  Any other Nqk
+ * returns INVALID_ARG.  Input bytes per token-head drop to about 2 (V + 1) + 4K/N
+ * on the bf16 path when Nqk == 1.
+ */
+m2rnn_status m2rnn_forward_f32_qk(const float* q, const float* k, const float* v, const float* a,
+                                  const float* alpha, const float* beta, const float* W,
+                                  const float* w_r, const float* H0, float* y, float* H_T, int B,
+                                  int T, int N, int Nqk, int K, int V, void* stream);
+m2rnn_status m2rnn_forward_bf16_qk(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                   const uint16_t* a, const float* alpha, const float* beta,
+                                   const uint16_t* W, const float* w_r, const float* H0, float* y,
+                                   float* H_T, int B, int T, int N, int Nqk, int K, int V,
+                                   int variant, void* stream);
+
 /* Name of a bf16 kernel variant (NULL for an unknown id).  Id 0 is "auto". */
 const char* m2rnn_variant_name(int variant);
 

@@ -129,26 +129,36 @@ int m2rnn_variant_supports(int variant, int B, int T, int N, int K, int V) {
   return supports(variant, K, V) ? 1 : 0;
 }
 
+m2rnn_status m2rnn_forward_f32_qk(const float* q, const float* k, const float* v, const float* a,
+                                  const float* alpha, const float* beta, const float* W,
+                                  const float* w_r, const float* H0, float* y, float* H_T, int B,
+                                  int T, int N, int Nqk, int K, int V, void* stream) {
+  m2rnn_status st = common_checks(q, k, v, a, alpha, beta, W, w_r, y, B, T, N, K, V);
+  if (st != M2RNN_OK) return st;
+  if (Nqk != 1 && Nqk != N) return M2RNN_ERR_INVALID_ARG;
+  if (K > 128 || V > 128) return M2RNN_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (T == 0) return empty_sequence(H0, H_T, B, N, K, V, s);
+  Problem p{q, k, v, a, alpha, beta, W, w_r, H0, y, H_T, B, T, N, K, V, Nqk, 0, nullptr};
+  return launch_fwd_f32(p, s) == cudaSuccess ? M2RNN_OK : M2RNN_ERR_CUDA;
+}
+
 m2rnn_status m2rnn_forward_f32(const float* q, const float* k, const float* v, const float* a,
                                const float* alpha, const float* beta, const float* W,
                                const float* w_r, const float* H0, float* y, float* H_T, int B,
                                int T, int N, int K, int V, void* stream) {
-  m2rnn_status st = common_checks(q, k, v, a, alpha, beta, W, w_r, y, B, T, N, K, V);
-  if (st != M2RNN_OK) return st;
-  if (K > 128 || V > 128) return M2RNN_ERR_UNSUPPORTED;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (T == 0) return empty_sequence(H0, H_T, B, N, K, V, s);
-  Problem p{q, k, v, a, alpha, beta, W, w_r, H0, y, H_T, B, T, N, K, V, 0, nullptr};
-  return launch_fwd_f32(p, s) == cudaSuccess ? M2RNN_OK : M2RNN_ERR_CUDA;
+  return m2rnn_forward_f32_qk(q, k, v, a, alpha, beta, W, w_r, H0, y, H_T, B, T, N, N, K, V,
+                              stream);
 }
 
-m2rnn_status m2rnn_forward_bf16_variant(const uint16_t* q, const uint16_t* k, const uint16_t* v,
-                                        const uint16_t* a, const float* alpha, const float* beta,
-                                        const uint16_t* W, const float* w_r, const float* H0,
-                                        float* y, float* H_T, int B, int T, int N, int K, int V,
-                                        int variant, void* stream) {
+m2rnn_status m2rnn_forward_bf16_qk(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                   const uint16_t* a, const float* alpha, const float* beta,
+                                   const uint16_t* W, const float* w_r, const float* H0, float* y,
+                                   float* H_T, int B, int T, int N, int Nqk, int K, int V,
+                                   int variant, void* stream) {
   m2rnn_status st = common_checks(q, k, v, a, alpha, beta, W, w_r, y, B, T, N, K, V);
   if (st != M2RNN_OK) return st;
+  if (Nqk != 1 && Nqk != N) return M2RNN_ERR_INVALID_ARG;
   const int debug = variant >> 8;
   int base = variant & 0xff;
   if (base < 0 || base >= kNumVariants) return M2RNN_ERR_INVALID_ARG;
@@ -166,7 +176,7 @@ m2rnn_status m2rnn_forward_bf16_variant(const uint16_t* q, const uint16_t* k, co
   int* status = status_address(dev);
   EncodeTiledFn enc = encode_fn();
   if (!status || !enc) return M2RNN_ERR_CUDA;
-  Problem p{q, k, v, a, alpha, beta, W, w_r, H0, y, H_T, B, T, N, K, V, debug, status};
+  Problem p{q, k, v, a, alpha, beta, W, w_r, H0, y, H_T, B, T, N, K, V, Nqk, debug, status};
   cudaError_t err = cudaErrorInvalidValue;
   switch (base) {
     case kMmaRowWarp: err = launch_fwd_bf16_mma_rowwarp(p, enc, s); break;
@@ -176,12 +186,21 @@ m2rnn_status m2rnn_forward_bf16_variant(const uint16_t* q, const uint16_t* k, co
   return err == cudaSuccess ? M2RNN_OK : M2RNN_ERR_CUDA;
 }
 
+m2rnn_status m2rnn_forward_bf16_variant(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                        const uint16_t* a, const float* alpha, const float* beta,
+                                        const uint16_t* W, const float* w_r, const float* H0,
+                                        float* y, float* H_T, int B, int T, int N, int K, int V,
+                                        int variant, void* stream) {
+  return m2rnn_forward_bf16_qk(q, k, v, a, alpha, beta, W, w_r, H0, y, H_T, B, T, N, N, K, V,
+                               variant, stream);
+}
+
 m2rnn_status m2rnn_forward_bf16(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                                 const uint16_t* a, const float* alpha, const float* beta,
                                 const uint16_t* W, const float* w_r, const float* H0, float* y,
                                 float* H_T, int B, int T, int N, int K, int V, void* stream) {
-  return m2rnn_forward_bf16_variant(q, k, v, a, alpha, beta, W, w_r, H0, y, H_T, B, T, N, K, V,
-                                    kAuto, stream);
+  return m2rnn_forward_bf16_qk(q, k, v, a, alpha, beta, W, w_r, H0, y, H_T, B, T, N, N, K, V,
+                               kAuto, stream);
 }
 
 m2rnn_status m2rnn_stream_status(void* stream) {

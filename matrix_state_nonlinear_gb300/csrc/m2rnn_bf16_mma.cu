@@ -81,7 +81,7 @@ __global__ void __launch_bounds__(256, 1)
                          const float* __restrict__ alpha, const float* __restrict__ beta,
                          const uint16_t* __restrict__ W, const float* __restrict__ w_r,
                          const float* H0, float* __restrict__ y, float* H_T, int T, int N, int K,
-                         int Tc, int debug, int* status) {
+                         int Tc, int qk_hs, int debug, int* status) {
   constexpr int V = 16 * VT;
   constexpr int NT = 2 * VT;  // n-tiles of 8 columns
   constexpr int M = 4 * VT;   // readout partial sums per thread
@@ -107,8 +107,8 @@ __global__ void __launch_bounds__(256, 1)
     const int st = cc & 1;
     uint8_t* base = smem + st * L.stage_bytes;
     mbar_arrive_expect_tx(&bar[st], stage_tx);
-    tma_load_4d(base + L.qs, &tm_q, &bar[st], 0, n, cc * Tc, b);
-    tma_load_4d(base + L.ks, &tm_k, &bar[st], 0, n, cc * Tc, b);
+    tma_load_4d(base + L.qs, &tm_q, &bar[st], 0, n * qk_hs, cc * Tc, b);
+    tma_load_4d(base + L.ks, &tm_k, &bar[st], 0, n * qk_hs, cc * Tc, b);
     tma_load_4d(base + L.vs, &tm_v, &bar[st], 0, n, cc * Tc, b);
   };
 
@@ -373,8 +373,8 @@ cudaError_t launch_vt(const Problem& p, EncodeTiledFn enc, cudaStream_t stream) 
     L = make_layout(p.K, V, Tc, WREG);
   }
   CUtensorMap mq, mk, mv;
-  if (!make_map(enc, &mq, p.q, p.K, p.N, p.T, p.B, Tc) ||
-      !make_map(enc, &mk, p.k, p.K, p.N, p.T, p.B, Tc) ||
+  if (!make_map(enc, &mq, p.q, p.K, p.Nqk, p.T, p.B, Tc) ||
+      !make_map(enc, &mk, p.k, p.K, p.Nqk, p.T, p.B, Tc) ||
       !make_map(enc, &mv, p.v, V, p.N, p.T, p.B, Tc))
     return cudaErrorInvalidValue;
   auto kern = fwd_bf16_mma_rowwarp<VT, WREG>;
@@ -383,7 +383,8 @@ cudaError_t launch_vt(const Problem& p, EncodeTiledFn enc, cudaStream_t stream) 
   const unsigned grid = (unsigned)p.B * (unsigned)p.N;
   kern<<<grid, 2 * p.K, L.total, stream>>>(mq, mk, mv, (const uint16_t*)p.a, p.alpha, p.beta,
                                            (const uint16_t*)p.W, p.w_r, p.H0, p.y, p.H_T, p.T,
-                                           p.N, p.K, Tc, p.debug, p.status);
+                                           p.N, p.K, Tc, p.Nqk == 1 ? 0 : 1, p.debug,
+                                           p.status);
   return cudaGetLastError();
 }
 

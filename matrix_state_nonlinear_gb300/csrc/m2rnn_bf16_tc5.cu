@@ -62,7 +62,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                  const __grid_constant__ CUtensorMap tm_v, const uint16_t* __restrict__ a,
                  const float* __restrict__ alpha, const float* __restrict__ beta,
                  const uint16_t* __restrict__ W, const float* __restrict__ w_r, const float* H0,
-                 float* __restrict__ y, float* H_T, int T, int N, int debug, int* status) {
+                 float* __restrict__ y, float* H_T, int T, int N, int qk_hs, int debug,
+                 int* status) {
   extern __shared__ uint8_t smem_raw[];
   // Round the dynamic shared-memory base up to 1024 bytes (128-byte swizzle atoms).
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -95,8 +96,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   auto issue_chunk = [&](int cc) {
     const int st = cc & 1;
     mbar_arrive_expect_tx(&full[st], 3u * kTc * kD * 2u);
-    tma_load_4d(stage(st, 0), &tm_q, &full[st], 0, n, cc * kTc, b);
-    tma_load_4d(stage(st, 1), &tm_k, &full[st], 0, n, cc * kTc, b);
+    tma_load_4d(stage(st, 0), &tm_q, &full[st], 0, n * qk_hs, cc * kTc, b);
+    tma_load_4d(stage(st, 1), &tm_k, &full[st], 0, n * qk_hs, cc * kTc, b);
     tma_load_4d(stage(st, 2), &tm_v, &full[st], 0, n, cc * kTc, b);
   };
   auto chunk_gates = [&](int cc) {
@@ -311,7 +312,8 @@ bool tc5_supports(int K, int V) { return K == kD && V == kD; }
 
 cudaError_t launch_fwd_bf16_tc5(const Problem& p, EncodeTiledFn enc, cudaStream_t stream) {
   CUtensorMap mq, mk, mv;
-  if (!make_map_tc5(enc, &mq, p.q, p.N, p.T, p.B) || !make_map_tc5(enc, &mk, p.k, p.N, p.T, p.B) ||
+  if (!make_map_tc5(enc, &mq, p.q, p.Nqk, p.T, p.B) ||
+      !make_map_tc5(enc, &mk, p.k, p.Nqk, p.T, p.B) ||
       !make_map_tc5(enc, &mv, p.v, p.N, p.T, p.B))
     return cudaErrorInvalidValue;
   cudaError_t err =
@@ -320,7 +322,8 @@ cudaError_t launch_fwd_bf16_tc5(const Problem& p, EncodeTiledFn enc, cudaStream_
   const unsigned grid = (unsigned)p.B * (unsigned)p.N;
   fwd_bf16_tc5<<<grid, kThreads, kSmemBytes, stream>>>(mq, mk, mv, (const uint16_t*)p.a, p.alpha,
                                                        p.beta, (const uint16_t*)p.W, p.w_r, p.H0,
-                                                       p.y, p.H_T, p.T, p.N, p.debug, p.status);
+                                                       p.y, p.H_T, p.T, p.N, p.Nqk == 1 ? 0 : 1,
+                                                       p.debug, p.status);
   return cudaGetLastError();
 }
 

@@ -20,7 +20,8 @@ __global__ void __launch_bounds__(kThreads)
                    const float* __restrict__ v, const float* __restrict__ a,
                    const float* __restrict__ alpha, const float* __restrict__ beta,
                    const float* __restrict__ W, const float* __restrict__ w_r,
-                   const float* H0, float* __restrict__ y, float* H_T, int T, int N, int K, int V) {
+                   const float* H0, float* __restrict__ y, float* H_T, int T, int N, int K, int V,
+                   int Nqk) {
   extern __shared__ float smem[];
   float* Ws = smem;              // [V][V]
   float* Hbuf = Ws + V * V;      // [2][K][V]
@@ -44,9 +45,10 @@ __global__ void __launch_bounds__(kThreads)
     float* qs = st + K;
     float* vs = st + 2 * K;
     const size_t row = ((size_t)b * T + t) * N + n;
+    const size_t qrow = ((size_t)b * T + t) * Nqk + (Nqk == 1 ? 0 : n);  // shared q, k: head 0
     for (int i = tid; i < K; i += kThreads) {
-      ks[i] = k[row * K + i];
-      qs[i] = q[row * K + i];
+      ks[i] = k[qrow * K + i];
+      qs[i] = q[qrow * K + i];
     }
     for (int j = tid; j < V; j += kThreads) vs[j] = v[row * V + j];
     if (tid == 0) {
@@ -93,7 +95,7 @@ cudaError_t launch_fwd_f32(const Problem& p, cudaStream_t stream) {
   const unsigned grid = (unsigned)p.B * (unsigned)p.N;
   fwd_f32_kernel<<<grid, kThreads, smem, stream>>>(
       (const float*)p.q, (const float*)p.k, (const float*)p.v, (const float*)p.a, p.alpha, p.beta,
-      (const float*)p.W, p.w_r, p.H0, p.y, p.H_T, p.T, p.N, p.K, p.V);
+      (const float*)p.W, p.w_r, p.H0, p.y, p.H_T, p.T, p.N, p.K, p.V, p.Nqk);
   return cudaGetLastError();
 }
 

@@ -32,6 +32,7 @@ struct Problem {
   float* y;
   float* H_T;
   int B, T, N, K, V;
+  int Nqk;          // heads of q and k: N (one per head) or 1 (shared by all heads)
   int debug;        // kDebug* bits (tests only)
   int* status;      // device address of this device's status word
 };

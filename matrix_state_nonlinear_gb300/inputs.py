@@ -41,6 +41,7 @@ class Workload:
     alpha_range: tuple = (0.5, 2.0)
     h0: str = "zero"               # "zero" or "uniform" (U[-0.5, 0.5])
     rescale_w: bool = True         # spectral-norm rescale of W (bf16 workloads)
+    shared_qk: bool = False        # one q, k set for all heads: q, k are [B, T, 1, K]
 
     @property
     def units(self) -> int:
@@ -109,7 +110,8 @@ def _randn(shape, std, seed, device, dtype):
 def make_inputs(wl: Workload, device="cpu", seed: int = 0) -> dict:
     """All inputs of one forward pass as torch tensors on ``device``.
 
-    q, k [B,T,N,K]; v [B,T,N,V]; a [B,T,N]; W [N,V,V] in the operand dtype;
+    q, k [B,T,N,K] (or [B,T,1,K] when shared_qk); v [B,T,N,V]; a [B,T,N]; W [N,V,V]
+    in the operand dtype;
     alpha, beta [N]; w_r [N,V]; H0 [B,N,K,V] (or None) in float32.
     All tensors are contiguous.
     """
@@ -125,8 +127,9 @@ def make_inputs(wl: Workload, device="cpu", seed: int = 0) -> dict:
     )
     B, T, N, K, V = wl.B, wl.T, wl.N, wl.K, wl.V
     base = seed * 1000 + 17
-    out["q"] = _randn((B, T, N, K), 1.0 / math.sqrt(K), base + 0, dev, dt)
-    out["k"] = _randn((B, T, N, K), 1.0 / math.sqrt(K), base + 1, dev, dt)
+    Nqk = 1 if wl.shared_qk else N
+    out["q"] = _randn((B, T, Nqk, K), 1.0 / math.sqrt(K), base + 0, dev, dt)
+    out["k"] = _randn((B, T, Nqk, K), 1.0 / math.sqrt(K), base + 1, dev, dt)
     out["v"] = _randn((B, T, N, V), 1.0, base + 2, dev, dt)
     out["a"] = _randn((B, T, N), 1.0, base + 3, dev, dt)
     return out
@@ -146,8 +149,11 @@ def slice_pair(inp: dict, b: int, n: int) -> dict:
     slice gives exactly that pair's outputs of the full problem.
     """
     s = {}
-    for key in ("q", "k", "v", "a"):
+    for key in ("v", "a"):
         s[key] = to_f64_numpy(inp[key][b:b + 1, :, n:n + 1])
+    for key in ("q", "k"):  # a shared q, k (one head) serves every head
+        h = n if inp[key].shape[2] > 1 else 0
+        s[key] = to_f64_numpy(inp[key][b:b + 1, :, h:h + 1])
     s["alpha"] = to_f64_numpy(inp["alpha"][n:n + 1])
     s["beta"] = to_f64_numpy(inp["beta"][n:n + 1])
     s["W"] = to_f64_numpy(inp["W"][n:n + 1])

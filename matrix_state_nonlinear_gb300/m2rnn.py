@@ -24,6 +24,8 @@ SYMBOLS = {
     "m2rnn_forward_f32": (_I, [_P] * 11 + [_I] * 5 + [_P]),
     "m2rnn_forward_bf16": (_I, [_P] * 11 + [_I] * 5 + [_P]),
     "m2rnn_forward_bf16_variant": (_I, [_P] * 11 + [_I] * 6 + [_P]),
+    "m2rnn_forward_f32_qk": (_I, [_P] * 11 + [_I] * 6 + [_P]),
+    "m2rnn_forward_bf16_qk": (_I, [_P] * 11 + [_I] * 7 + [_P]),
     "m2rnn_variant_name": (ctypes.c_char_p, [_I]),
     "m2rnn_pick_variant": (_I, [_I] * 5),
     "m2rnn_variant_supports": (_I, [_I] * 6),
@@ -108,12 +110,18 @@ def _check(t, name, dtype, shape, dev):
 
 
 def _marshal(q, k, v, a, alpha, beta, W, w_r, H0, y, H_T, opdtype):
+    """Checks tensors and returns (pointers, (B, T, N, K, V), y, Nqk).
+
+    q and k may have N heads or a single head shared by all heads of v.
+    """
     if q.device.type != "cuda":
         raise ValueError("inputs must be CUDA tensors")
-    B, T, N, K = q.shape
-    V = v.shape[-1]
+    B, T, Nqk, K = q.shape
+    N, V = v.shape[2], v.shape[3]
     dev = q.device
-    for t, name, dt, shp in [(q, "q", opdtype, (B, T, N, K)), (k, "k", opdtype, (B, T, N, K)),
+    if Nqk not in (1, N):
+        raise ValueError(f"q, k must have 1 or {N} heads, got {Nqk}")
+    for t, name, dt, shp in [(q, "q", opdtype, (B, T, Nqk, K)), (k, "k", opdtype, (B, T, Nqk, K)),
                              (v, "v", opdtype, (B, T, N, V)), (a, "a", opdtype, (B, T, N)),
                              (alpha, "alpha", torch.float32, (N,)),
                              (beta, "beta", torch.float32, (N,)),
@@ -126,14 +134,19 @@ def _marshal(q, k, v, a, alpha, beta, W, w_r, H0, y, H_T, opdtype):
     if H_T is not None:
         _check(H_T, "H_T", torch.float32, (B, N, K, V), dev)
     ptrs = [_ptr(x) for x in (q, k, v, a, alpha, beta, W, w_r, H0, y, H_T)]
-    return ptrs, (B, T, N, K, V), y
+    return ptrs, (B, T, N, K, V), y, Nqk
 
 
 def m2rnn_forward_f32(q, k, v, a, alpha, beta, W, w_r, H0=None, y=None, H_T=None, stream=None):
     """fp32-operand forward (all tensors float32).  Returns (y, H_T)."""
     lib = load_library()
-    ptrs, dims, y = _marshal(q, k, v, a, alpha, beta, W, w_r, H0, y, H_T, torch.float32)
-    st = lib.m2rnn_forward_f32(*ptrs, *dims, ctypes.c_void_p(_stream_ptr(stream)))
+    ptrs, (B, T, N, K, V), y, Nqk = _marshal(q, k, v, a, alpha, beta, W, w_r, H0, y, H_T,
+                                              torch.float32)
+    if Nqk == N:
+        st = lib.m2rnn_forward_f32(*ptrs, B, T, N, K, V, ctypes.c_void_p(_stream_ptr(stream)))
+    else:
+        st = lib.m2rnn_forward_f32_qk(*ptrs, B, T, N, Nqk, K, V,
+                                      ctypes.c_void_p(_stream_ptr(stream)))
     if st != OK:
         raise M2RNNError(st, "m2rnn_forward_f32")
     return y, H_T
@@ -143,19 +156,27 @@ def m2rnn_forward_bf16_variant(q, k, v, a, alpha, beta, W, w_r, H0=None, y=None,
                                variant=0, stream=None):
     """bf16-operand / fp32-state forward with an explicit kernel variant (0 = auto)."""
     lib = load_library()
-    ptrs, dims, y = _marshal(q, k, v, a, alpha, beta, W, w_r, H0, y, H_T, torch.bfloat16)
-    st = lib.m2rnn_forward_bf16_variant(*ptrs, *dims, int(variant),
-                                        ctypes.c_void_p(_stream_ptr(stream)))
+    ptrs, (B, T, N, K, V), y, Nqk = _marshal(q, k, v, a, alpha, beta, W, w_r, H0, y, H_T,
+                                              torch.bfloat16)
+    if Nqk == N:
+        st = lib.m2rnn_forward_bf16_variant(*ptrs, B, T, N, K, V, int(variant),
+                                            ctypes.c_void_p(_stream_ptr(stream)))
+    else:
+        st = lib.m2rnn_forward_bf16_qk(*ptrs, B, T, N, Nqk, K, V, int(variant),
+                                       ctypes.c_void_p(_stream_ptr(stream)))
     if st != OK:
-        raise M2RNNError(st, "m2rnn_forward_bf16_variant")
+        raise M2RNNError(st, "m2rnn_forward_bf16")
     return y, H_T
 
 
 def m2rnn_forward_bf16(q, k, v, a, alpha, beta, W, w_r, H0=None, y=None, H_T=None, stream=None):
     """bf16-operand / fp32-state forward (q, k, v, a, W bfloat16; the rest float32)."""
     lib = load_library()
-    ptrs, dims, y = _marshal(q, k, v, a, alpha, beta, W, w_r, H0, y, H_T, torch.bfloat16)
-    st = lib.m2rnn_forward_bf16(*ptrs, *dims, ctypes.c_void_p(_stream_ptr(stream)))
+    ptrs, (B, T, N, K, V), y, Nqk = _marshal(q, k, v, a, alpha, beta, W, w_r, H0, y, H_T,
+                                              torch.bfloat16)
+    if Nqk != N:
+        return m2rnn_forward_bf16_variant(q, k, v, a, alpha, beta, W, w_r, H0, y, H_T, 0, stream)
+    st = lib.m2rnn_forward_bf16(*ptrs, B, T, N, K, V, ctypes.c_void_p(_stream_ptr(stream)))
     if st != OK:
         raise M2RNNError(st, "m2rnn_forward_bf16")
     return y, H_T
@@ -165,11 +186,12 @@ def m2rnn_forward(inputs: dict, y=None, H_T=None, variant=0, stream=None):
     """Forward pass on a dict keyed like the input generator's output.
 
     Dispatches on the operand dtype of q: float32 -> the fp32 path, bfloat16 ->
-    the tensor-core path.  Allocates y and H_T (torch memory) when not given.
+    the tensor-core path.  q and k with a single head are shared by all heads.
+    Allocates y and H_T (torch memory) when not given.
     """
     q = inputs["q"]
-    B, T, N, K = q.shape
-    V = inputs["v"].shape[-1]
+    B, T, _, K = q.shape
+    N, V = inputs["v"].shape[2], inputs["v"].shape[3]
     if H_T is None:
         H_T = torch.empty((B, N, K, V), dtype=torch.float32, device=q.device)
     args = [inputs[x] for x in ("q", "k", "v", "a", "alpha", "beta", "W", "w_r")]

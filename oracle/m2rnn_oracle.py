@@ -53,20 +53,22 @@ def forget_gate(a: np.ndarray, alpha: np.ndarray, beta: np.ndarray) -> np.ndarra
 def m2rnn_forward(q, k, v, a, alpha, beta, W, w_r, H0=None, return_states=False):
     """The forward recurrence over all (batch, head) pairs, in fp64.
 
-    Shapes (row-major): q, k [B,T,N,K]; v [B,T,N,V]; a [B,T,N]; alpha, beta [N];
+    Shapes (row-major): q, k [B,T,N,K], or [B,T,1,K] when one query/key set is shared
+    by all heads (Sec. 2.4); v [B,T,N,V]; a [B,T,N]; alpha, beta [N];
     W [N,V,V]; w_r [N,V]; H0 [B,N,K,V] or None (zero state).
     Returns y [B,T,N,V] and H_T [B,N,K,V]; with ``return_states`` also every
     H_t as [B,T,N,K,V] (small problems only).
     """
-    q = np.asarray(q, np.float64)
-    k = np.asarray(k, np.float64)
     v = np.asarray(v, np.float64)
     a = np.asarray(a, np.float64)
     W = np.asarray(W, np.float64)
     w_r = np.asarray(w_r, np.float64)
-    B, T, N, K = q.shape
-    V = v.shape[-1]
-    assert k.shape == (B, T, N, K) and v.shape == (B, T, N, V) and a.shape == (B, T, N)
+    B, T, N, V = v.shape
+    K = np.shape(q)[-1]
+    # Multi-value sharing (Sec. 2.4, N_q = N_k = 1): one q_t, k_t for every head.
+    q = np.broadcast_to(np.asarray(q, np.float64), (B, T, N, K))
+    k = np.broadcast_to(np.asarray(k, np.float64), (B, T, N, K))
+    assert a.shape == (B, T, N)
     assert W.shape == (N, V, V) and w_r.shape == (N, V)
 
     H = np.zeros((B, N, K, V)) if H0 is None else np.array(H0, dtype=np.float64)
@@ -94,8 +96,9 @@ def m2rnn_forward_scalar(q, k, v, a, alpha, beta, W, w_r, H0=None):
     shares no vectorised routine with ``m2rnn_forward``.
     Arguments are nested lists / arrays indexable as in ``m2rnn_forward``.
     """
-    B, T, N, K = len(q), len(q[0]), len(q[0][0]), len(q[0][0][0])
-    V = len(v[0][0][0])
+    B, T, N, V = len(v), len(v[0]), len(v[0][0]), len(v[0][0][0])
+    K = len(q[0][0][0])
+    shared = len(q[0][0]) == 1 and N > 1  # one q_t, k_t for all heads (Sec. 2.4)
     y = [[[[0.0] * V for _ in range(N)] for _ in range(T)] for _ in range(B)]
     HT = [[None] * N for _ in range(B)]
     for b in range(B):
@@ -112,13 +115,13 @@ def m2rnn_forward_scalar(q, k, v, a, alpha, beta, W, w_r, H0=None):
                         acc = 0.0
                         for l in range(V):
                             acc += H[i][l] * float(W[n][l][j])
-                        acc += float(k[b][t][n][i]) * float(v[b][t][n][j])
+                        acc += float(k[b][t][0 if shared else n][i]) * float(v[b][t][n][j])
                         newH[i][j] = f * H[i][j] + (1.0 - f) * math.tanh(acc)
                 H = newH
                 for j in range(V):
                     s = 0.0
                     for i in range(K):
-                        s += H[i][j] * float(q[b][t][n][i])
+                        s += H[i][j] * float(q[b][t][0 if shared else n][i])
                     y[b][t][n][j] = s + float(w_r[n][j]) * float(v[b][t][n][j])
             HT[b][n] = H
     return np.array(y, dtype=np.float64), np.array(HT, dtype=np.float64)
