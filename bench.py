@@ -95,6 +95,31 @@ def measured_traffic(variant_name, wl):
     return rec["bytes_per_launch"] * wl.units / rec["units"]
 
 
+# ---------------------------------------------------------------- replicas across ranks
+# The (batch, head) pairs are independent and the recurrence has no exchange step, so
+# N GPUs run N replicas of the workload: rank r owns batch rows [r B, (r + 1) B) of a
+# global batch N B, drawn with seed r.  The only cross-rank operations are the
+# barrier around the timed region and the max of the step times.
+def rank_seed(rank: int) -> int:
+    return rank
+
+
+def max_over_ranks(value: float, world: int, device) -> float:
+    """The largest `value` over all ranks (the slowest rank sets the job's time)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: int, world: int, ms_per_step: float) -> float:
+    """Whole-job units per second: every rank's units over the slowest rank's time."""
+    return world * units_per_rank / (ms_per_step / 1e3)
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -265,7 +290,7 @@ def main():
         dist.barrier()
     pkg.load_library()
 
-    inp = make_inputs(wl, dev, seed=rank)
+    inp = make_inputs(wl, dev, seed=rank_seed(rank))
     B, T, N, K, V = wl.B, wl.T, wl.N, wl.K, wl.V
     y = torch.empty((B, T, N, V), dtype=torch.float32, device=dev)
     HT = torch.empty((B, N, K, V), dtype=torch.float32, device=dev)
@@ -311,12 +336,9 @@ def main():
     clk = clocks.stop()
     if pkg.stream_status(stream) != 0:
         raise RuntimeError("device status not OK after the timed steps")
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, world, dev)
     ms_per_step = total_ms / args.steps
-    value = world * wl.units / (ms_per_step / 1e3)
+    value = job_throughput(wl.units, world, ms_per_step)
 
     # ---- end to end: pinned host inputs -> device -> kernel -> y, H_T back to pinned host
     e2e = None
@@ -349,11 +371,8 @@ def main():
         e1.record(stream)
         torch.cuda.synchronize(dev)
         e_ms = e0.elapsed_time(e1) / e_steps
-        if world > 1:
-            t = torch.tensor([e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
-        e2e = {"value": world * wl.units / (e_ms / 1e3), "unit": UNIT,
+        e_ms = max_over_ranks(e_ms, world, dev)
+        e2e = {"value": job_throughput(wl.units, world, e_ms), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms,
                "steps": e_steps}
 
