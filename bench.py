@@ -61,6 +61,7 @@ KERNEL_SOURCES = {
     "mma_sync_rowwarp": ["m2rnn_bf16_mma.cu"],
     "mma_sync_pipelined": ["m2rnn_bf16_pipe.cu"],
     "tcgen05_k128_v128": ["m2rnn_bf16_tc5.cu"],
+    "mma_sync_cluster4_k64_v128": ["m2rnn_bf16_cluster.cu"],
 }
 
 

@@ -44,7 +44,7 @@ EncodeTiledFn encode_fn() {
 
 bool aligned(const void* p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
 
-enum Variant : int { kAuto = 0, kMmaRowWarp = 1, kMmaPipe = 2, kTc5 = 3, kNumVariants = 4 };
+enum Variant : int { kAuto = 0, kMmaRowWarp = 1, kMmaPipe = 2, kTc5 = 3, kMmaCluster = 4, kNumVariants = 5 };
 
 m2rnn_status common_checks(const void* q, const void* k, const void* v, const void* a,
                            const float* alpha, const float* beta, const void* W, const float* w_r,
@@ -71,6 +71,7 @@ m2rnn_status empty_sequence(const float* H0, float* H_T, int B, int N, int K, in
 
 int pick(int K, int V) {
   if (tc5_supports(K, V)) return kTc5;
+  if (mma_cluster_supports(K, V)) return kMmaCluster;
   if (mma_pipe_supports(K, V)) return kMmaPipe;
   if (mma_rowwarp_supports(K, V)) return kMmaRowWarp;
   return 0;
@@ -81,6 +82,7 @@ bool supports(int variant, int K, int V) {
     case kMmaRowWarp: return mma_rowwarp_supports(K, V);
     case kMmaPipe: return mma_pipe_supports(K, V);
     case kTc5: return tc5_supports(K, V);
+    case kMmaCluster: return mma_cluster_supports(K, V);
   }
   return false;
 }
@@ -111,6 +113,7 @@ const char* m2rnn_variant_name(int variant) {
     case kMmaRowWarp: return "mma_sync_rowwarp";
     case kMmaPipe: return "mma_sync_pipelined";
     case kTc5: return "tcgen05_k128_v128";
+    case kMmaCluster: return "mma_sync_cluster4_k64_v128";
   }
   return nullptr;
 }
@@ -182,6 +185,7 @@ m2rnn_status m2rnn_forward_bf16_qk(const uint16_t* q, const uint16_t* k, const u
     case kMmaRowWarp: err = launch_fwd_bf16_mma_rowwarp(p, enc, s); break;
     case kMmaPipe: err = launch_fwd_bf16_mma_pipe(p, enc, s); break;
     case kTc5: err = launch_fwd_bf16_tc5(p, enc, s); break;
+    case kMmaCluster: err = launch_fwd_bf16_mma_cluster(p, enc, s); break;
   }
   return err == cudaSuccess ? M2RNN_OK : M2RNN_ERR_CUDA;
 }

@@ -59,4 +59,9 @@ cudaError_t launch_fwd_bf16_mma_pipe(const Problem& p, EncodeTiledFn enc, cudaSt
 bool tc5_supports(int K, int V);
 cudaError_t launch_fwd_bf16_tc5(const Problem& p, EncodeTiledFn enc, cudaStream_t stream);
 
+// bf16 warp-MMA path with a 4-CTA thread-block cluster per pair (rows split over four
+// SMs, readout partials exchanged through distributed shared memory): K = 64, V = 128.
+bool mma_cluster_supports(int K, int V);
+cudaError_t launch_fwd_bf16_mma_cluster(const Problem& p, EncodeTiledFn enc, cudaStream_t stream);
+
 }  // namespace m2rnn

@@ -61,6 +61,9 @@ def test_variant_support_table(lib):
     assert binding.variant_supports(3, 1, 8, 1, 128, 128)      # tcgen05: K = V = 128 only
     assert not binding.variant_supports(3, 1, 8, 1, 64, 128)
     assert binding.pick_variant(16, 8192, 32, 128, 128) == 3
+    assert binding.variant_supports(4, 1, 8, 1, 64, 128)       # 4-CTA cluster: K = 64, V = 128
+    assert not binding.variant_supports(4, 1, 8, 1, 64, 64)
+    assert binding.pick_variant(1, 65536, 16, 64, 128) == 4
     assert binding.variant_name(2) is not None
 
 

@@ -99,11 +99,12 @@ def test_f32_shapes(B, T, N, K, V, h0):
 # ---------------------------------------------------------------- bf16 path
 BF16_SHAPES = [(1, 1, 1, 16, 16), (1, 2, 1, 16, 32), (3, 17, 1, 16, 64), (1, 63, 3, 32, 16),
                (2, 64, 1, 64, 64), (1, 65, 3, 64, 64), (1, 130, 2, 48, 32), (2, 97, 1, 128, 64),
-               (1, 70, 2, 64, 128), (1, 33, 3, 128, 128), (2, 200, 1, 112, 128)]
+               (1, 70, 2, 64, 128), (1, 33, 3, 128, 128), (2, 200, 1, 112, 128),
+               (1, 1, 1, 64, 128), (1, 129, 1, 64, 128), (2, 300, 3, 64, 128)]
 
 
 def bf16_variants():
-    return [1, 2, 3]
+    return [1, 2, 3, 4]
 
 
 @pytest.mark.parametrize("B,T,N,K,V", BF16_SHAPES)
@@ -261,11 +262,12 @@ def test_unsupported_and_invalid_from_binding():
     assert e.value.status == binding.ERR_UNSUPPORTED
 
 
-def test_forced_wait_timeout_is_reported_and_context_survives():
-    inp = bf16_inputs(T=70)
-    y = torch.empty((2, 70, 2, 64), device=DEV)
+@pytest.mark.parametrize("variant,K,V", [(1, 64, 64), (2, 64, 64), (3, 128, 128), (4, 64, 128)])
+def test_forced_wait_timeout_is_reported_and_context_survives(variant, K, V):
+    inp = bf16_inputs(T=70, K=K, V=V)
+    y = torch.empty((2, 70, 2, V), device=DEV)
     HT = torch.empty_like(inp["H0"])
-    pkg.m2rnn_forward(inp, y=y, H_T=HT, variant=1 | (1 << 8))
+    pkg.m2rnn_forward(inp, y=y, H_T=HT, variant=variant | (1 << 8))
     assert pkg.stream_status() == binding.ERR_TIMEOUT
     assert pkg.stream_status() == binding.OK          # the word is cleared by the read
     y2, HT2 = run_gpu(inp)                            # the context is still usable
