@@ -40,6 +40,7 @@
 #ifndef M2RNN_H
 #define M2RNN_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -113,6 +114,78 @@ m2rnn_status m2rnn_forward_bf16_qk(const uint16_t* q, const uint16_t* k, const u
                                    const uint16_t* W, const float* w_r, const float* H0, float* y,
                                    float* H_T, int B, int T, int N, int Nqk, int K, int V,
                                    int variant, void* stream);
+
+/*
+ * Training support (the notes' Sec. 2.6-2.7).  The backward pass re-runs the
+ * recurrence while keeping every step's state in HBM, then scans time in reverse.
+ *
+ * m2rnn_forward_train_*: the forward pass of m2rnn_forward_*_qk that also writes
+ *   Hs     [B, N, T, K, V]  float32: Hs[b][n][t] = H_t after step t (t = 0..T-1),
+ *                           the states the backward reads (B·N·T·K·V·4 bytes).
+ *   Hs is required when T > 0.  The bf16 entry takes the pipelined warp-MMA
+ *   kernel, so it supports K a multiple of 16 with K <= 64 and V in {16, 32, 64}
+ *   (UNSUPPORTED otherwise); the fp32 entry supports 1 <= K, V <= 128.
+ */
+m2rnn_status m2rnn_forward_train_f32(const float* q, const float* k, const float* v,
+                                     const float* a, const float* alpha, const float* beta,
+                                     const float* W, const float* w_r, const float* H0, float* y,
+                                     float* H_T, float* Hs, int B, int T, int N, int Nqk, int K,
+                                     int V, void* stream);
+m2rnn_status m2rnn_forward_train_bf16(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                      const uint16_t* a, const float* alpha, const float* beta,
+                                      const uint16_t* W, const float* w_r, const float* H0,
+                                      float* y, float* H_T, float* Hs, int B, int T, int N,
+                                      int Nqk, int K, int V, void* stream);
+
+/*
+ * Bytes of device workspace m2rnn_backward_* needs for these sizes (0 for an
+ * invalid shape).  Per (b, n) pair it holds the running state gradient and the
+ * pair's partial sums of dW, dw_r, dalpha, dbeta; with Nqk == 1 < N also the
+ * per-head dq, dk before they are summed over heads.
+ */
+size_t m2rnn_backward_workspace_bytes(int B, int T, int N, int Nqk, int K, int V);
+
+/*
+ * Backward pass: gradients of a loss L that depends on y (dy = dL/dy) and on the
+ * final state (dH_T = dL/dH_T, NULL for zero), given the inputs of the forward and
+ * its kept states Hs (from m2rnn_forward_train_*, same inputs).  The reverse scan
+ * is the notes' Sec. 2.7 with u_t = dy_t, C_T = dH_T:
+ *   R_t = C_t + q_t u_t^T,  D_t = ((1 - f_t) R_t) ⊙ (1 - Z_t ⊙ Z_t),
+ *   C_{t-1} = f_t R_t + D_t W^T,  dL/df_t = <R_t, H_{t-1} - Z_t>,
+ *   dW = sum over b, t of H_{t-1}^T D_t,  dk_t = D_t v_t,
+ *   dv_t = D_t^T k_t + w_r ⊙ u_t,  dq_t = H_t u_t,  dH0 = C_{-1},
+ * with Z_t = tanh(H_{t-1} W + k_t v_t^T) recomputed from Hs, and the gate of
+ * Eq. (13)/(17) differentiated (x = a + beta):
+ *   da_t = dL/df_t · (-alpha f sigmoid(x)),  dalpha = sum dL/df_t · (-f softplus(x)),
+ *   dbeta = sum da_t,  dw_r = sum over b, t of u_t ⊙ v_t.
+ * Outputs (float32, written, caller-owned):
+ *   dq, dk [B, T, Nqk, K]  (summed over heads when Nqk == 1)
+ *   dv [B, T, N, V], da [B, T, N], dalpha [N], dbeta [N], dW [N, V, V], dw_r [N, V],
+ *   dH0 [B, N, K, V] (not written when NULL).
+ * dy [B, T, N, V] is float32.  `workspace` is caller-owned device memory of at least
+ * m2rnn_backward_workspace_bytes(...) bytes (INVALID_ARG otherwise); it is
+ * overwritten, so two calls in flight at once need two workspaces.  Sums over the
+ * batch run in a fixed order: results are deterministic.
+ * Errors: INVALID_ARG for a null required pointer (q, k, v, a, Hs, dy, dq, dk, dv,
+ * da are required only when T > 0) or a bad size; UNSUPPORTED for K or V > 128.
+ * The bf16 entry takes bf16 q, k, v, a, W; its `variant` is 0 (automatic) or 1
+ * (SIMT fp32 arithmetic); fp32 arithmetic throughout on both entries.
+ */
+m2rnn_status m2rnn_backward_f32(const float* q, const float* k, const float* v, const float* a,
+                                const float* alpha, const float* beta, const float* W,
+                                const float* w_r, const float* H0, const float* Hs,
+                                const float* dy, const float* dH_T, float* dq, float* dk,
+                                float* dv, float* da, float* dalpha, float* dbeta, float* dW,
+                                float* dw_r, float* dH0, int B, int T, int N, int Nqk, int K,
+                                int V, void* workspace, size_t workspace_bytes, void* stream);
+m2rnn_status m2rnn_backward_bf16(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                 const uint16_t* a, const float* alpha, const float* beta,
+                                 const uint16_t* W, const float* w_r, const float* H0,
+                                 const float* Hs, const float* dy, const float* dH_T, float* dq,
+                                 float* dk, float* dv, float* da, float* dalpha, float* dbeta,
+                                 float* dW, float* dw_r, float* dH0, int B, int T, int N, int Nqk,
+                                 int K, int V, int variant, void* workspace,
+                                 size_t workspace_bytes, void* stream);
 
 /* Name of a bf16 kernel variant (NULL for an unknown id).  Id 0 is "auto". */
 const char* m2rnn_variant_name(int variant);

@@ -69,6 +69,23 @@ m2rnn_status empty_sequence(const float* H0, float* H_T, int B, int N, int K, in
   return err == cudaSuccess ? M2RNN_OK : M2RNN_ERR_CUDA;
 }
 
+m2rnn_status backward_checks(const BackwardProblem& p, size_t workspace_bytes) {
+  if (p.B < 1 || p.N < 1 || p.K < 1 || p.V < 1 || p.T < 0) return M2RNN_ERR_INVALID_ARG;
+  if (p.Nqk != 1 && p.Nqk != p.N) return M2RNN_ERR_INVALID_ARG;
+  if ((long long)p.B * p.N > 0x7fffffffLL) return M2RNN_ERR_UNSUPPORTED;
+  if (p.K > 128 || p.V > 128) return M2RNN_ERR_UNSUPPORTED;
+  if (!p.alpha || !p.beta || !p.W || !p.w_r || !p.dalpha || !p.dbeta || !p.dW || !p.dw_r ||
+      !p.ws)
+    return M2RNN_ERR_INVALID_ARG;
+  if (p.T > 0 && (!p.q || !p.k || !p.v || !p.a || !p.Hs || !p.dy || !p.dq || !p.dk || !p.dv ||
+                  !p.da))
+    return M2RNN_ERR_INVALID_ARG;
+  if (workspace_bytes < sizeof(float) * backward_workspace_floats(p.B, p.T, p.N, p.Nqk, p.K, p.V))
+    return M2RNN_ERR_INVALID_ARG;
+  if (!aligned(p.ws, 16)) return M2RNN_ERR_INVALID_ARG;
+  return M2RNN_OK;
+}
+
 int pick(int K, int V) {
   if (tc5_supports(K, V)) return kTc5;
   if (mma_cluster_supports(K, V)) return kMmaCluster;
@@ -205,6 +222,88 @@ m2rnn_status m2rnn_forward_bf16(const uint16_t* q, const uint16_t* k, const uint
                                 float* H_T, int B, int T, int N, int K, int V, void* stream) {
   return m2rnn_forward_bf16_qk(q, k, v, a, alpha, beta, W, w_r, H0, y, H_T, B, T, N, N, K, V,
                                kAuto, stream);
+}
+
+m2rnn_status m2rnn_forward_train_f32(const float* q, const float* k, const float* v,
+                                     const float* a, const float* alpha, const float* beta,
+                                     const float* W, const float* w_r, const float* H0, float* y,
+                                     float* H_T, float* Hs, int B, int T, int N, int Nqk, int K,
+                                     int V, void* stream) {
+  m2rnn_status st = common_checks(q, k, v, a, alpha, beta, W, w_r, y, B, T, N, K, V);
+  if (st != M2RNN_OK) return st;
+  if (Nqk != 1 && Nqk != N) return M2RNN_ERR_INVALID_ARG;
+  if (T > 0 && !Hs) return M2RNN_ERR_INVALID_ARG;
+  if (K > 128 || V > 128) return M2RNN_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (T == 0) return empty_sequence(H0, H_T, B, N, K, V, s);
+  Problem p{q, k, v, a, alpha, beta, W, w_r, H0, y, H_T, B, T, N, K, V, Nqk, 0, nullptr, Hs};
+  return launch_fwd_f32(p, s) == cudaSuccess ? M2RNN_OK : M2RNN_ERR_CUDA;
+}
+
+m2rnn_status m2rnn_forward_train_bf16(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                      const uint16_t* a, const float* alpha, const float* beta,
+                                      const uint16_t* W, const float* w_r, const float* H0,
+                                      float* y, float* H_T, float* Hs, int B, int T, int N,
+                                      int Nqk, int K, int V, void* stream) {
+  m2rnn_status st = common_checks(q, k, v, a, alpha, beta, W, w_r, y, B, T, N, K, V);
+  if (st != M2RNN_OK) return st;
+  if (Nqk != 1 && Nqk != N) return M2RNN_ERR_INVALID_ARG;
+  if (T > 0 && !Hs) return M2RNN_ERR_INVALID_ARG;
+  if (!mma_pipe_supports(K, V)) return M2RNN_ERR_UNSUPPORTED;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(W, 16) ||
+      !aligned(y, 16) || !aligned(H0, 16) || !aligned(H_T, 16) || !aligned(Hs, 16) ||
+      !aligned(a, 2))
+    return M2RNN_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (T == 0) return empty_sequence(H0, H_T, B, N, K, V, s);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return M2RNN_ERR_CUDA;
+  int* status = status_address(dev);
+  EncodeTiledFn enc = encode_fn();
+  if (!status || !enc) return M2RNN_ERR_CUDA;
+  Problem p{q, k, v, a, alpha, beta, W, w_r, H0, y, H_T, B, T, N, K, V, Nqk, 0, status, Hs};
+  return launch_fwd_bf16_mma_pipe(p, enc, s) == cudaSuccess ? M2RNN_OK : M2RNN_ERR_CUDA;
+}
+
+size_t m2rnn_backward_workspace_bytes(int B, int T, int N, int Nqk, int K, int V) {
+  if (B < 1 || N < 1 || K < 1 || V < 1 || T < 0 || K > 128 || V > 128) return 0;
+  if (Nqk != 1 && Nqk != N) return 0;
+  return sizeof(float) * backward_workspace_floats(B, T, N, Nqk, K, V);
+}
+
+m2rnn_status m2rnn_backward_f32(const float* q, const float* k, const float* v, const float* a,
+                                const float* alpha, const float* beta, const float* W,
+                                const float* w_r, const float* H0, const float* Hs,
+                                const float* dy, const float* dH_T, float* dq, float* dk,
+                                float* dv, float* da, float* dalpha, float* dbeta, float* dW,
+                                float* dw_r, float* dH0, int B, int T, int N, int Nqk, int K,
+                                int V, void* workspace, size_t workspace_bytes, void* stream) {
+  BackwardProblem p{q,  k,  v,  a,      alpha, beta, W,  w_r,  H0, Hs, dy, dH_T, dq, dk,
+                    dv, da, dalpha, dbeta, dW,   dw_r, dH0, static_cast<float*>(workspace),
+                    B,  T,  N,  K,      V,     Nqk};
+  m2rnn_status st = backward_checks(p, workspace_bytes);
+  if (st != M2RNN_OK) return st;
+  return launch_bwd_f32(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? M2RNN_OK
+                                                                               : M2RNN_ERR_CUDA;
+}
+
+m2rnn_status m2rnn_backward_bf16(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                 const uint16_t* a, const float* alpha, const float* beta,
+                                 const uint16_t* W, const float* w_r, const float* H0,
+                                 const float* Hs, const float* dy, const float* dH_T, float* dq,
+                                 float* dk, float* dv, float* da, float* dalpha, float* dbeta,
+                                 float* dW, float* dw_r, float* dH0, int B, int T, int N, int Nqk,
+                                 int K, int V, int variant, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+  BackwardProblem p{q,  k,  v,  a,      alpha, beta, W,  w_r,  H0, Hs, dy, dH_T, dq, dk,
+                    dv, da, dalpha, dbeta, dW,   dw_r, dH0, static_cast<float*>(workspace),
+                    B,  T,  N,  K,      V,     Nqk};
+  m2rnn_status st = backward_checks(p, workspace_bytes);
+  if (st != M2RNN_OK) return st;
+  if (variant != 0 && variant != 1) return M2RNN_ERR_INVALID_ARG;
+  return launch_bwd_simt_bf16(p, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? M2RNN_OK
+             : M2RNN_ERR_CUDA;
 }
 
 m2rnn_status m2rnn_stream_status(void* stream) {

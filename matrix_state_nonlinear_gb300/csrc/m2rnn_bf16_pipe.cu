@@ -70,15 +70,15 @@ __host__ __device__ inline PipeLayout pipe_layout(int K, int V, int Tc) {
   return L;
 }
 
-template <int VT>
+template <int VT, bool kCache>
 __global__ void __launch_bounds__(160, 1)
     fwd_bf16_mma_pipe(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const uint16_t* __restrict__ a,
                       const float* __restrict__ alpha, const float* __restrict__ beta,
                       const uint16_t* __restrict__ W, const float* __restrict__ w_r,
-                      const float* H0, float* __restrict__ y, float* H_T, int T, int N, int K,
-                      int Tc, int qk_hs, int debug, int* status) {
+                      const float* H0, float* __restrict__ y, float* H_T, float* __restrict__ Hs,
+                      int T, int N, int K, int Tc, int qk_hs, int debug, int* status) {
   constexpr int V = 16 * VT;
   constexpr int NT = 2 * VT;  // n-tiles of 8 columns
   constexpr int M = 4 * VT;   // readout partial sums per thread
@@ -379,6 +379,14 @@ __global__ void __launch_bounds__(160, 1)
     // This step's partial sums are reduced during the next step (or at chunk end).
 #pragma unroll
     for (int i = 0; i < M; ++i) pout[i] = p[i];
+    if constexpr (kCache) {  // keep H_t for the backward pass (streaming stores)
+      float* hp = Hs + ((size_t)pair * T + (size_t)cc * Tc + s) * K * V;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        __stcs(reinterpret_cast<float2*>(hp + (size_t)r0 * V + 8 * nt + 2 * c), h[nt][0]);
+        __stcs(reinterpret_cast<float2*>(hp + (size_t)r1 * V + 8 * nt + 2 * c), h[nt][1]);
+      }
+    }
   };
 
   float pA[M], pB[M];
@@ -463,14 +471,14 @@ cudaError_t launch_pipe_vt(const Problem& p, EncodeTiledFn enc, cudaStream_t str
       !make_map_pipe(enc, &mk, p.k, p.K, p.Nqk, p.T, p.B, Tc) ||
       !make_map_pipe(enc, &mv, p.v, V, p.N, p.T, p.B, Tc))
     return cudaErrorInvalidValue;
-  auto kern = fwd_bf16_mma_pipe<VT>;
+  auto kern = p.Hs ? fwd_bf16_mma_pipe<VT, true> : fwd_bf16_mma_pipe<VT, false>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
   if (err != cudaSuccess) return err;
   const unsigned grid = (unsigned)p.B * (unsigned)p.N;
   const int threads = 32 * (p.K / 16 + 1);
   kern<<<grid, threads, L.total, stream>>>(mq, mk, mv, (const uint16_t*)p.a, p.alpha, p.beta,
-                                           (const uint16_t*)p.W, p.w_r, p.H0, p.y, p.H_T, p.T, p.N,
-                                           p.K, Tc, p.Nqk == 1 ? 0 : 1, p.debug, p.status);
+                                           (const uint16_t*)p.W, p.w_r, p.H0, p.y, p.H_T, p.Hs, p.T,
+                                           p.N, p.K, Tc, p.Nqk == 1 ? 0 : 1, p.debug, p.status);
   return cudaGetLastError();
 }
 

@@ -8,6 +8,9 @@
 // the K x V state live in shared memory; every element is fp32 and tanh / exp /
 // log1p are the accurate CUDA math functions.  This path serves small problems
 // and the 1e-4 parity bar; the tensor-core paths carry the large workloads.
+// With a non-null Hs the kernel also keeps every step's state, Hs[b][n][t] = H_t,
+// for the backward pass (the notes' Sec. 2.6: states are kept, then scanned in
+// reverse).
 #include "m2rnn_internal.h"
 
 namespace m2rnn {
@@ -20,8 +23,8 @@ __global__ void __launch_bounds__(kThreads)
                    const float* __restrict__ v, const float* __restrict__ a,
                    const float* __restrict__ alpha, const float* __restrict__ beta,
                    const float* __restrict__ W, const float* __restrict__ w_r,
-                   const float* H0, float* __restrict__ y, float* H_T, int T, int N, int K, int V,
-                   int Nqk) {
+                   const float* H0, float* __restrict__ y, float* H_T, float* __restrict__ Hs,
+                   int T, int N, int K, int V, int Nqk) {
   extern __shared__ float smem[];
   float* Ws = smem;              // [V][V]
   float* Hbuf = Ws + V * V;      // [2][K][V]
@@ -67,7 +70,9 @@ __global__ void __launch_bounds__(kThreads)
       float acc = ks[i] * vs[j];                       // rank-1 write k_t v_t^T
       const float* hrow = Hc + i * V;
       for (int l = 0; l < V; ++l) acc = fmaf(hrow[l], Ws[l * V + j], acc);  // H_{t-1} W
-      Hn[e] = f * Hc[e] + g * tanhf(acc);              // Eq. (10)-(11)
+      const float hn = f * Hc[e] + g * tanhf(acc);     // Eq. (10)-(11)
+      Hn[e] = hn;
+      if (Hs) Hs[((size_t)pair * T + t) * KV + e] = hn;
     }
     __syncthreads();
     for (int j = tid; j < V; j += kThreads) {          // Eq. (12), sum over the K rows
@@ -95,7 +100,7 @@ cudaError_t launch_fwd_f32(const Problem& p, cudaStream_t stream) {
   const unsigned grid = (unsigned)p.B * (unsigned)p.N;
   fwd_f32_kernel<<<grid, kThreads, smem, stream>>>(
       (const float*)p.q, (const float*)p.k, (const float*)p.v, (const float*)p.a, p.alpha, p.beta,
-      (const float*)p.W, p.w_r, p.H0, p.y, p.H_T, p.T, p.N, p.K, p.V, p.Nqk);
+      (const float*)p.W, p.w_r, p.H0, p.y, p.H_T, p.Hs, p.T, p.N, p.K, p.V, p.Nqk);
   return cudaGetLastError();
 }
 

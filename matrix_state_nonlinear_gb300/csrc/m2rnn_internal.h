@@ -35,7 +35,56 @@ struct Problem {
   int Nqk;          // heads of q and k: N (one per head) or 1 (shared by all heads)
   int debug;        // kDebug* bits (tests only)
   int* status;      // device address of this device's status word
+  float* Hs = nullptr;  // optional: every step's state, fp32 [B, N, T, K, V]
 };
+
+// Backward pass (reverse scan of the notes' Sec. 2.7).  Pointers as in the C ABI;
+// `ws` is the caller's workspace (backward_workspace_floats floats).
+struct BackwardProblem {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* a;
+  const float* alpha;
+  const float* beta;
+  const void* W;
+  const float* w_r;
+  const float* H0;   // may be null (zero initial state)
+  const float* Hs;   // [B, N, T, K, V] states of the training forward
+  const float* dy;   // [B, T, N, V]
+  const float* dH_T; // may be null (zero)
+  float* dq;         // [B, T, Nqk, K]
+  float* dk;         // [B, T, Nqk, K]
+  float* dv;         // [B, T, N, V]
+  float* da;         // [B, T, N]
+  float* dalpha;     // [N]
+  float* dbeta;      // [N]
+  float* dW;         // [N, V, V]
+  float* dw_r;       // [N, V]
+  float* dH0;        // [B, N, K, V], may be null
+  float* ws;
+  int B, T, N, K, V, Nqk;
+};
+
+// Floats of the per-pair partial block: C (K V), dW partial (V V), dw_r partial (V),
+// dalpha and dbeta partials (2), padded to a multiple of 4.
+__host__ __device__ inline size_t backward_pair_floats(int K, int V) {
+  return ((size_t)K * V + (size_t)V * V + V + 2 + 3) & ~(size_t)3;
+}
+// Workspace floats: the pair blocks, plus per-head dq, dk when q, k are shared.
+inline size_t backward_workspace_floats(int B, int T, int N, int Nqk, int K, int V) {
+  size_t n = (size_t)B * N * backward_pair_floats(K, V);
+  if (Nqk == 1 && N > 1) n += 2 * (size_t)B * T * N * K;
+  return n;
+}
+
+// fp32 SIMT backward (any 1 <= K, V <= 128), then the reduction over the batch.
+cudaError_t launch_bwd_f32(const BackwardProblem& p, cudaStream_t stream);
+// The same SIMT backward on bf16 q, k, v, a, W (fp32 arithmetic), then the reduction.
+cudaError_t launch_bwd_simt_bf16(const BackwardProblem& p, cudaStream_t stream);
+// Sum the per-pair partials over the batch (and per-head dq, dk over heads when q, k
+// are shared) into dW, dw_r, dalpha, dbeta (dq, dk).  Deterministic order.
+cudaError_t launch_bwd_reduce(const BackwardProblem& p, cudaStream_t stream);
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,

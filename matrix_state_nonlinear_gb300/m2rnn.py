@@ -32,6 +32,11 @@ SYMBOLS = {
     "m2rnn_stream_status": (_I, [_P]),
     "m2rnn_status_string": (ctypes.c_char_p, [_I]),
     "m2rnn_version": (_I, []),
+    "m2rnn_forward_train_f32": (_I, [_P] * 12 + [_I] * 6 + [_P]),
+    "m2rnn_forward_train_bf16": (_I, [_P] * 12 + [_I] * 6 + [_P]),
+    "m2rnn_backward_workspace_bytes": (ctypes.c_size_t, [_I] * 6),
+    "m2rnn_backward_f32": (_I, [_P] * 21 + [_I] * 6 + [_P, ctypes.c_size_t, _P]),
+    "m2rnn_backward_bf16": (_I, [_P] * 21 + [_I] * 7 + [_P, ctypes.c_size_t, _P]),
 }
 
 _lib = None
@@ -199,3 +204,83 @@ def m2rnn_forward(inputs: dict, y=None, H_T=None, variant=0, stream=None):
         return m2rnn_forward_f32(*args, inputs.get("H0"), y, H_T, stream=stream)
     return m2rnn_forward_bf16_variant(*args, inputs.get("H0"), y, H_T, variant=variant,
                                       stream=stream)
+
+
+# ---------------------------------------------------------------- training support
+def _shape_of(inputs):
+    q, v = inputs["q"], inputs["v"]
+    B, T, Nqk, K = q.shape
+    return B, T, v.shape[2], Nqk, K, v.shape[3]
+
+
+def m2rnn_forward_train(inputs: dict, y=None, H_T=None, Hs=None, stream=None):
+    """Forward pass that also keeps every step's state for the backward pass.
+
+    Returns (y, H_T, Hs) with Hs float32 [B, N, T, K, V] (Hs[:, :, t] = H_t).
+    Dispatches on the operand dtype of q like ``m2rnn_forward``.
+    """
+    lib = load_library()
+    B, T, N, Nqk, K, V = _shape_of(inputs)
+    q = inputs["q"]
+    dev = q.device
+    if H_T is None:
+        H_T = torch.empty((B, N, K, V), dtype=torch.float32, device=dev)
+    if Hs is None:
+        Hs = torch.empty((B, N, T, K, V), dtype=torch.float32, device=dev)
+    _check(Hs, "Hs", torch.float32, (B, N, T, K, V), dev)
+    opdtype = torch.float32 if q.dtype == torch.float32 else torch.bfloat16
+    args = [inputs[x] for x in ("q", "k", "v", "a", "alpha", "beta", "W", "w_r")]
+    ptrs, _, y, _ = _marshal(*args, inputs.get("H0"), y, H_T, opdtype)
+    fn = lib.m2rnn_forward_train_f32 if opdtype == torch.float32 else lib.m2rnn_forward_train_bf16
+    st = fn(*ptrs, _ptr(Hs), B, T, N, Nqk, K, V, ctypes.c_void_p(_stream_ptr(stream)))
+    if st != OK:
+        raise M2RNNError(st, "m2rnn_forward_train")
+    return y, H_T, Hs
+
+
+def backward_workspace_bytes(B, T, N, Nqk, K, V) -> int:
+    return int(load_library().m2rnn_backward_workspace_bytes(B, T, N, Nqk, K, V))
+
+
+def m2rnn_backward(inputs: dict, Hs, dy, dH_T=None, grads=None, workspace=None, variant=0,
+                   stream=None):
+    """Backward pass: gradients of a loss through y (dy) and H_T (dH_T, optional).
+
+    ``Hs`` is the state history from ``m2rnn_forward_train`` on the same inputs.
+    Returns a dict dq, dk, dv, da, dalpha, dbeta, dW, dw_r, dH0 (float32; ``grads``
+    may supply any of them preallocated).  The workspace is allocated (torch
+    memory) when not given.
+    """
+    lib = load_library()
+    B, T, N, Nqk, K, V = _shape_of(inputs)
+    q = inputs["q"]
+    dev = q.device
+    opdtype = torch.float32 if q.dtype == torch.float32 else torch.bfloat16
+    args = [inputs[x] for x in ("q", "k", "v", "a", "alpha", "beta", "W", "w_r")]
+    ptrs, _, _, _ = _marshal(*args, inputs.get("H0"), dy, None, opdtype)
+    _check(Hs, "Hs", torch.float32, (B, N, T, K, V), dev)
+    _check(dy, "dy", torch.float32, (B, T, N, V), dev)
+    _check(dH_T, "dH_T", torch.float32, (B, N, K, V), dev)
+    shapes = {"dq": (B, T, Nqk, K), "dk": (B, T, Nqk, K), "dv": (B, T, N, V), "da": (B, T, N),
+              "dalpha": (N,), "dbeta": (N,), "dW": (N, V, V), "dw_r": (N, V),
+              "dH0": (B, N, K, V)}
+    out = dict(grads or {})
+    for name, shp in shapes.items():
+        if name not in out:
+            out[name] = torch.empty(shp, dtype=torch.float32, device=dev)
+        _check(out[name], name, torch.float32, shp, dev)
+    nbytes = backward_workspace_bytes(B, T, N, Nqk, K, V)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
+    gptrs = [_ptr(out[n]) for n in shapes]
+    common = ptrs[:9] + [_ptr(Hs), _ptr(dy), _ptr(dH_T)] + gptrs
+    sp = ctypes.c_void_p(_stream_ptr(stream))
+    if opdtype == torch.float32:
+        st = lib.m2rnn_backward_f32(*common, B, T, N, Nqk, K, V, _ptr(workspace),
+                                    workspace.numel() * workspace.element_size(), sp)
+    else:
+        st = lib.m2rnn_backward_bf16(*common, B, T, N, Nqk, K, V, int(variant), _ptr(workspace),
+                                     workspace.numel() * workspace.element_size(), sp)
+    if st != OK:
+        raise M2RNNError(st, "m2rnn_backward")
+    return out

@@ -136,3 +136,45 @@ def test_binding_refuses_cpu_tensors(lib):
     inp = make_inputs(WORKLOADS["tiny_f32_b1_t64_n2_k8_v8"], "cpu")
     with pytest.raises(ValueError):
         binding.m2rnn_forward(inp)
+
+
+# ---------------------------------------------------------------- training entry points
+def call_bwd(lib, ptrs, dims, ws_bytes, bf16=False, variant=0):
+    # ptrs: 21 pointers (inputs, Hs, dy, dH_T, gradients), dims: (B, T, N, Nqk, K, V)
+    ws = (1 << 30) if ws_bytes else None
+    if bf16:
+        return lib.m2rnn_backward_bf16(*ptrs, *dims, variant, ws, ws_bytes, None)
+    return lib.m2rnn_backward_f32(*ptrs, *dims, ws, ws_bytes, None)
+
+
+def test_workspace_bytes_formula(lib):
+    # per pair: K V + V V + V + 2 floats, padded to 4; plus 2 B T N K floats when q, k shared
+    def pair(K, V):
+        return (K * V + V * V + V + 2 + 3) // 4 * 4
+    assert binding.backward_workspace_bytes(2, 5, 3, 3, 8, 8) == 4 * 6 * pair(8, 8)
+    assert binding.backward_workspace_bytes(2, 5, 3, 1, 8, 16) == 4 * (6 * pair(8, 16) + 2 * 2 * 5 * 3 * 8)
+    assert binding.backward_workspace_bytes(1, 5, 1, 1, 8, 8) == 4 * pair(8, 8)   # N = 1: nothing to sum
+    assert binding.backward_workspace_bytes(1, 5, 2, 3, 8, 8) == 0                # bad Nqk
+    assert binding.backward_workspace_bytes(1, 5, 1, 1, 129, 8) == 0
+
+
+def test_backward_argument_checks(lib):
+    dims = (1, 4, 2, 2, 8, 8)
+    need = binding.backward_workspace_bytes(*dims)
+    p = fake_ptrs(21)
+    assert call_bwd(lib, p, dims, need - 4) == binding.ERR_INVALID_ARG          # workspace too small
+    assert call_bwd(lib, p, (1, 4, 2, 2, 8, 129), 1 << 30) == binding.ERR_UNSUPPORTED
+    assert call_bwd(lib, p, (1, 4, 2, 3, 8, 8), need) == binding.ERR_INVALID_ARG   # Nqk not 1 or N
+    for which in (0, 4, 6, 9, 10, 12, 16, 18):   # q, alpha, W, Hs, dy, dq, dalpha, dW
+        pp = list(p)
+        pp[which] = None
+        assert call_bwd(lib, pp, dims, need) == binding.ERR_INVALID_ARG, which
+    assert call_bwd(lib, p, dims, need, bf16=True, variant=9) == binding.ERR_INVALID_ARG
+
+
+def test_forward_train_argument_checks(lib):
+    p = fake_ptrs(12)
+    p[11] = None                                   # Hs missing with T > 0
+    assert lib.m2rnn_forward_train_f32(*p, 1, 4, 1, 1, 8, 8, None) == binding.ERR_INVALID_ARG
+    p = fake_ptrs(12)
+    assert lib.m2rnn_forward_train_bf16(*p, 1, 4, 1, 1, 128, 128, None) == binding.ERR_UNSUPPORTED

@@ -1,0 +1,154 @@
+"""Training support on the GPU: the state-keeping forward and the backward pass
+against the fp64 oracle (the notes' Sec. 2.6-2.7), through the C ABI.
+
+Tolerances (max-abs error per gradient tensor, scaled by max(1, max |oracle|)):
+  * fp32 path: 1e-4.  Every step is fp32 with accurate tanh/exp; the reverse scan
+    adds one rounding per operation along T steps, far below 1e-4 at these sizes.
+  * bf16 path: 3e-2.  The kept states come from the bf16-operand forward, whose
+    states differ from the exact ones by up to its own bar (3e-2); the gradients
+    are smooth in the states, so they carry errors of the same relative size.
+"""
+import numpy as np
+import pytest
+import torch
+
+import __graft_entry__
+import matrix_state_nonlinear_gb300 as pkg
+from matrix_state_nonlinear_gb300 import m2rnn as binding
+from matrix_state_nonlinear_gb300.inputs import Workload, all_f64, make_inputs
+from oracle import m2rnn_backward_inputs, m2rnn_forward_inputs
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+TOL = {"f32": 1e-4, "bf16": 3e-2}
+GRADS = ["dq", "dk", "dv", "da", "dalpha", "dbeta", "dW", "dw_r", "dH0"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    __graft_entry__.build()
+    pkg.load_library()
+
+
+def upstream(B, T, N, K, V, seed, with_dHT=True):
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    dy = torch.randn((B, T, N, V), generator=g).to(DEV)
+    dHT = torch.randn((B, N, K, V), generator=g).to(DEV) if with_dHT else None
+    return dy, dHT
+
+
+def rel_err(got, want):
+    got = got.double().cpu().numpy() if torch.is_tensor(got) else np.asarray(got)
+    want = np.asarray(want, np.float64)
+    return float(np.abs(got - want).max()) / max(1.0, float(np.abs(want).max())) if want.size else 0.0
+
+
+def run_case(dtype, B, T, N, K, V, h0="uniform", shared=False, with_dHT=True, seed=0):
+    wl = Workload("bwd", B, T, N, K, V, dtype=dtype, h0=h0, shared_qk=shared,
+                  rescale_w=dtype == "bf16")
+    inp = make_inputs(wl, DEV, seed)
+    y, HT, Hs = pkg.m2rnn_forward_train(inp)
+    dy, dHT = upstream(B, T, N, K, V, seed + 1, with_dHT)
+    g = pkg.m2rnn_backward(inp, Hs, dy, dHT)
+    assert pkg.stream_status() == binding.OK
+    ref = m2rnn_backward_inputs(all_f64(inp), dy.double().cpu().numpy(),
+                                None if dHT is None else dHT.double().cpu().numpy())
+    errs = {n: rel_err(g[n], ref[n]) for n in GRADS}
+    return inp, (y, HT, Hs), g, errs
+
+
+F32_SHAPES = [(1, 1, 1, 1, 1), (2, 5, 3, 8, 8), (1, 64, 2, 8, 8), (1, 17, 2, 24, 40),
+              (2, 33, 1, 16, 128), (1, 9, 1, 128, 128), (3, 2, 2, 5, 7)]
+
+
+@pytest.mark.parametrize("shape", F32_SHAPES)
+@pytest.mark.parametrize("h0", ["zero", "uniform"])
+def test_backward_f32_matches_oracle(shape, h0):
+    _, _, _, errs = run_case("f32", *shape, h0=h0)
+    assert max(errs.values()) <= TOL["f32"], errs
+
+
+@pytest.mark.parametrize("shape", [(2, 7, 3, 8, 16), (1, 20, 4, 16, 8)])
+def test_backward_f32_shared_qk(shape):
+    _, _, g, errs = run_case("f32", *shape, shared=True)
+    assert g["dq"].shape[2] == 1
+    assert max(errs.values()) <= TOL["f32"], errs
+
+
+def test_backward_without_dHT_and_without_dH0():
+    wl = Workload("bwd", 2, 11, 2, 8, 8, dtype="f32", rescale_w=False, h0="uniform")
+    inp = make_inputs(wl, DEV, 4)
+    _, _, Hs = pkg.m2rnn_forward_train(inp)
+    dy, _ = upstream(2, 11, 2, 8, 8, 5, False)
+    lib = binding.load_library()
+    g = pkg.m2rnn_backward(inp, Hs, dy)
+    ref = m2rnn_backward_inputs(all_f64(inp), dy.double().cpu().numpy())
+    assert max(rel_err(g[n], ref[n]) for n in GRADS) <= TOL["f32"]
+    # dH0 == NULL: everything else is unchanged
+    grads = {n: torch.full_like(g[n], float("nan")) for n in GRADS if n != "dH0"}
+    out = {n: grads[n] for n in grads}
+    ws = torch.empty(binding.backward_workspace_bytes(2, 11, 2, 2, 8, 8), dtype=torch.uint8,
+                     device=DEV)
+    args = [inp[x] for x in ("q", "k", "v", "a", "alpha", "beta", "W", "w_r", "H0")]
+    st = lib.m2rnn_backward_f32(*[t.data_ptr() for t in args], Hs.data_ptr(), dy.data_ptr(), None,
+                                *[out[n].data_ptr() for n in GRADS if n != "dH0"], None,
+                                2, 11, 2, 2, 8, 8, ws.data_ptr(), ws.numel(), None)
+    assert st == binding.OK and pkg.stream_status() == binding.OK
+    for n in out:
+        assert torch.equal(out[n], g[n]), n
+
+
+def test_forward_train_keeps_states_and_matches_plain_forward():
+    for dtype, shape in [("f32", (2, 37, 3, 8, 24)), ("bf16", (2, 150, 3, 64, 64)),
+                         ("bf16", (1, 70, 2, 32, 16))]:
+        B, T, N, K, V = shape
+        wl = Workload("tr", B, T, N, K, V, dtype=dtype, h0="uniform", rescale_w=dtype == "bf16")
+        inp = make_inputs(wl, DEV, 7)
+        y, HT, Hs = pkg.m2rnn_forward_train(inp)
+        y2, HT2 = pkg.m2rnn_forward(inp)
+        assert torch.equal(y, y2) and torch.equal(HT, HT2)     # same arithmetic, bit for bit
+        assert torch.equal(Hs[:, :, T - 1], HT)
+        _, _, states = m2rnn_forward_inputs(all_f64(inp), return_states=True)
+        err = float(np.abs(Hs.double().cpu().numpy() - np.moveaxis(states, 1, 2)).max())
+        assert err <= TOL[dtype], err
+
+
+BF16_SHAPES = [(1, 1, 1, 16, 16), (2, 65, 3, 64, 64), (1, 130, 2, 32, 32), (2, 40, 2, 48, 16)]
+
+
+@pytest.mark.parametrize("shape", BF16_SHAPES)
+def test_backward_bf16_matches_oracle(shape):
+    _, _, _, errs = run_case("bf16", *shape)
+    assert max(errs.values()) <= TOL["bf16"], errs
+
+
+def test_backward_bf16_shared_qk():
+    _, _, g, errs = run_case("bf16", 2, 50, 4, 64, 64, shared=True)
+    assert g["dq"].shape[2] == 1
+    assert max(errs.values()) <= TOL["bf16"], errs
+
+
+def test_backward_is_deterministic():
+    wl = Workload("det", 3, 40, 2, 16, 32, dtype="bf16", h0="uniform")
+    inp = make_inputs(wl, DEV, 2)
+    _, _, Hs = pkg.m2rnn_forward_train(inp)
+    dy, dHT = upstream(3, 40, 2, 16, 32, 3)
+    g1 = pkg.m2rnn_backward(inp, Hs, dy, dHT)
+    g2 = pkg.m2rnn_backward(inp, Hs, dy, dHT)
+    for n in GRADS:
+        assert torch.equal(g1[n], g2[n]), n
+
+
+def test_backward_empty_sequence():
+    wl = Workload("e", 2, 0, 2, 8, 8, dtype="f32", h0="uniform", rescale_w=False)
+    inp = make_inputs(wl, DEV, 1)
+    Hs = torch.empty((2, 2, 0, 8, 8), device=DEV)
+    dy = torch.empty((2, 0, 2, 8), device=DEV)
+    dHT = torch.randn((2, 2, 8, 8), device=DEV)
+    g = pkg.m2rnn_backward(inp, Hs, dy, dHT)
+    assert pkg.stream_status() == binding.OK
+    assert torch.equal(g["dH0"], dHT)
+    for n in ("dW", "dw_r", "dalpha", "dbeta"):
+        assert float(g[n].abs().max()) == 0.0
