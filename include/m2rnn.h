@@ -187,6 +187,27 @@ m2rnn_status m2rnn_backward_bf16(const uint16_t* q, const uint16_t* k, const uin
                                  int K, int V, int variant, void* workspace,
                                  size_t workspace_bytes, void* stream);
 
+/*
+ * m2rnn_backward_bf16 without a caller workspace: the workspace comes from a fixed
+ * 16 MiB scratch array inside the library (one per device).  The M²RNN notes have
+ * no counterpart to this entry point; it computes exactly what m2rnn_backward_bf16
+ * (variant 0) computes.
+ *   * Shapes whose workspace (m2rnn_backward_workspace_bytes) exceeds 16 MiB return
+ *     UNSUPPORTED before anything is enqueued; no memory is ever allocated.
+ *   * Every call on a device shares its scratch: calls whose work could overlap in
+ *     time (other streams or host threads, unordered) race and give wrong results.
+ *     Order them on one stream or with events.
+ *   * The first call on a device resolves the scratch address (it may load the
+ *     module); make that first call before capturing a stream into a CUDA graph.
+ */
+m2rnn_status m2rnn_backward_bf16_noalloc(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                         const uint16_t* a, const float* alpha, const float* beta,
+                                         const uint16_t* W, const float* w_r, const float* H0,
+                                         const float* Hs, const float* dy, const float* dH_T,
+                                         float* dq, float* dk, float* dv, float* da, float* dalpha,
+                                         float* dbeta, float* dW, float* dw_r, float* dH0, int B,
+                                         int T, int N, int Nqk, int K, int V, void* stream);
+
 /* Name of a bf16 kernel variant (NULL for an unknown id).  Id 0 is "auto". */
 const char* m2rnn_variant_name(int variant);
 

@@ -37,6 +37,7 @@ SYMBOLS = {
     "m2rnn_backward_workspace_bytes": (ctypes.c_size_t, [_I] * 6),
     "m2rnn_backward_f32": (_I, [_P] * 21 + [_I] * 6 + [_P, ctypes.c_size_t, _P]),
     "m2rnn_backward_bf16": (_I, [_P] * 21 + [_I] * 7 + [_P, ctypes.c_size_t, _P]),
+    "m2rnn_backward_bf16_noalloc": (_I, [_P] * 21 + [_I] * 6 + [_P]),
 }
 
 _lib = None
@@ -283,4 +284,31 @@ def m2rnn_backward(inputs: dict, Hs, dy, dH_T=None, grads=None, workspace=None, 
                                      workspace.numel() * workspace.element_size(), sp)
     if st != OK:
         raise M2RNNError(st, "m2rnn_backward")
+    return out
+
+
+def m2rnn_backward_noalloc(inputs: dict, Hs, dy, dH_T=None, grads=None, stream=None):
+    """``m2rnn_backward`` on bf16 inputs with the library's own fixed scratch instead of a
+    workspace (at most 16 MiB of workspace; calls on one device must not overlap)."""
+    lib = load_library()
+    B, T, N, Nqk, K, V = _shape_of(inputs)
+    q = inputs["q"]
+    dev = q.device
+    args = [inputs[x] for x in ("q", "k", "v", "a", "alpha", "beta", "W", "w_r")]
+    ptrs, _, _, _ = _marshal(*args, inputs.get("H0"), dy, None, torch.bfloat16)
+    _check(Hs, "Hs", torch.float32, (B, N, T, K, V), dev)
+    _check(dH_T, "dH_T", torch.float32, (B, N, K, V), dev)
+    shapes = {"dq": (B, T, Nqk, K), "dk": (B, T, Nqk, K), "dv": (B, T, N, V), "da": (B, T, N),
+              "dalpha": (N,), "dbeta": (N,), "dW": (N, V, V), "dw_r": (N, V),
+              "dH0": (B, N, K, V)}
+    out = dict(grads or {})
+    for name, shp in shapes.items():
+        if name not in out:
+            out[name] = torch.empty(shp, dtype=torch.float32, device=dev)
+        _check(out[name], name, torch.float32, shp, dev)
+    st = lib.m2rnn_backward_bf16_noalloc(*ptrs[:9], _ptr(Hs), _ptr(dy), _ptr(dH_T),
+                                         *[_ptr(out[n]) for n in shapes], B, T, N, Nqk, K, V,
+                                         ctypes.c_void_p(_stream_ptr(stream)))
+    if st != OK:
+        raise M2RNNError(st, "m2rnn_backward_bf16_noalloc")
     return out
