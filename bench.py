@@ -47,6 +47,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--batch", type=int, default=None,
                     help="override B of the workload (smaller cases for profiling)")
+    ap.add_argument("--pass", dest="which", default="forward", choices=["forward", "train"],
+                    help="forward: the forward pass (default); train: the state-keeping "
+                         "forward plus the backward pass")
     return ap.parse_args()
 
 
@@ -263,6 +266,194 @@ def workload_config(wl):
             "parallelism": "replicas (one independent workload per GPU)"}
 
 
+# ---------------------------------------------------------------- training step
+METRIC_TRAIN = "M²RNN training step (state-keeping forward + backward) tokens·heads/s"
+
+
+def oracle_train_sample(wl, seconds: float):
+    """Times the fp64 oracle's forward + backward on every pair over a bounded prefix of T."""
+    import numpy as np
+    from matrix_state_nonlinear_gb300.inputs import make_inputs, to_f64_numpy
+    from oracle import m2rnn_backward
+
+    T_s = 4
+    while True:
+        inp = make_inputs(wl.with_(T=T_s), "cpu", 0)
+        arrs = {k: to_f64_numpy(v) for k, v in inp.items()}
+        dy = np.random.default_rng(1).normal(0, 1, (wl.B, T_s, wl.N, wl.V))
+        c0 = time.process_time()
+        t0 = time.perf_counter()
+        m2rnn_backward(arrs["q"], arrs["k"], arrs["v"], arrs["a"], arrs["alpha"], arrs["beta"],
+                       arrs["W"], arrs["w_r"], dy, arrs["H0"])   # re-runs the forward inside
+        wall = time.perf_counter() - t0
+        cpu = time.process_time() - c0
+        if wall >= seconds or T_s >= wl.T:
+            break
+        T_s = min(wl.T, int(T_s * max(2.0, min(8.0, 1.1 * seconds / max(wall, 1e-3)))))
+    units = wl.B * wl.N * T_s
+    desc = (f"all {wl.B * wl.N} (batch, head) pairs of {wl.name} over the first {T_s} of "
+            f"{wl.T} steps (fp64 NumPy oracle, forward keeping states + backward, {units} "
+            f"token-heads, {wall:.1f} s wall)")
+    return units / wall, desc, max(1, round(cpu / wall)) if wall > 0 else 1
+
+
+def main_train(args, wl):
+    """One step = m2rnn_forward_train (y, H_T and every state H_t) + m2rnn_backward
+    (all gradients) over the workload, with a fixed synthetic upstream gradient dy."""
+    import torch
+    import torch.distributed as dist
+
+    import __graft_entry__
+    import matrix_state_nonlinear_gb300 as pkg
+    from matrix_state_nonlinear_gb300.inputs import make_inputs
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0 or world == 1:
+        __graft_entry__.build()
+    if world > 1:
+        dist.barrier()
+    pkg.load_library()
+
+    inp = make_inputs(wl, dev, seed=rank_seed(rank))
+    B, T, N, K, V = wl.B, wl.T, wl.N, wl.K, wl.V
+    Nqk = 1 if wl.shared_qk else N
+    g = torch.Generator(device=dev)
+    g.manual_seed(1000 + rank)
+    dy = torch.randn((B, T, N, V), generator=g, device=dev)
+    y = torch.empty((B, T, N, V), dtype=torch.float32, device=dev)
+    HT = torch.empty((B, N, K, V), dtype=torch.float32, device=dev)
+    Hs = torch.empty((B, N, T, K, V), dtype=torch.float32, device=dev)
+    grads = {"dq": (B, T, Nqk, K), "dk": (B, T, Nqk, K), "dv": (B, T, N, V), "da": (B, T, N),
+             "dalpha": (N,), "dbeta": (N,), "dW": (N, V, V), "dw_r": (N, V), "dH0": (B, N, K, V)}
+    grads = {n: torch.empty(shp, dtype=torch.float32, device=dev) for n, shp in grads.items()}
+    ws = torch.empty(max(16, pkg.backward_workspace_bytes(B, T, N, Nqk, K, V)), dtype=torch.uint8,
+                     device=dev)
+    stream = torch.cuda.current_stream(dev)
+    marks = []
+
+    def step(record=False):
+        if record:
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            e[0].record(stream)
+        pkg.m2rnn_forward_train(inp, y=y, H_T=HT, Hs=Hs, stream=stream)
+        if record:
+            e[1].record(stream)
+        pkg.m2rnn_backward(inp, Hs, dy, grads=grads, workspace=ws, variant=args.variant,
+                           stream=stream)
+        if record:
+            e[2].record(stream)
+            marks.append(e)
+
+    for _ in range(args.warmup):
+        step()
+    if pkg.stream_status(stream) != 0:
+        raise RuntimeError("device status not OK after warm-up")
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step(record=True)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    total_ms = ev0.elapsed_time(ev1)
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    if pkg.stream_status(stream) != 0:
+        raise RuntimeError("device status not OK after the timed steps")
+    fwd_ms = statistics.mean(a.elapsed_time(b) for a, b, _ in marks)
+    bwd_ms = statistics.mean(b.elapsed_time(c) for _, b, c in marks)
+    total_ms = max_over_ranks(total_ms, world, dev)
+    ms_per_step = total_ms / args.steps
+    value = job_throughput(wl.units, world, ms_per_step)
+
+    e2e = None
+    if not args.no_e2e:
+        names = ["q", "k", "v", "a", "alpha", "beta", "W", "w_r", "H0"]
+        host = {k: inp[k].cpu().pin_memory() for k in names if inp.get(k) is not None}
+        dinp = {k: torch.empty_like(inp[k]) for k in host}
+        if "H0" not in dinp:
+            dinp["H0"] = None
+        dy_h = dy.cpu().pin_memory()
+        dy_d = torch.empty_like(dy)
+        out_h = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for n, t in grads.items()}
+        h2d = sum(v.numel() * v.element_size() for v in host.values()) + dy_h.numel() * 4
+        d2h = sum(t.numel() * 4 for t in out_h.values())
+
+        def e2e_step():
+            for k, v in host.items():
+                dinp[k].copy_(v, non_blocking=True)
+            dy_d.copy_(dy_h, non_blocking=True)
+            pkg.m2rnn_forward_train(dinp, y=y, H_T=HT, Hs=Hs, stream=stream)
+            pkg.m2rnn_backward(dinp, Hs, dy_d, grads=grads, workspace=ws, variant=args.variant,
+                               stream=stream)
+            for n, t in grads.items():
+                out_h[n].copy_(t, non_blocking=True)
+
+        e_steps = max(3, min(args.steps, 5))
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e_ms = max_over_ranks(e0.elapsed_time(e1) / e_steps, world, dev)
+        e2e = {"value": job_throughput(wl.units, world, e_ms), "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms,
+               "steps": e_steps}
+
+    # ---- roofline of the dominant kernel: the backward's reverse scan
+    peaks, peak_src = load_peaks()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    flops = 6.0 * K * V * V * wl.units   # H_{t-1} W (recomputed), D_t W^T, H_{t-1}^T D_t
+    e = 2 if wl.dtype == "bf16" else 4
+    bwd_bytes = wl.units * (4 * K * V + 4 * V + e * (2 * K + V + 1) + 4 * (2 * K + V + 1))
+    fwd_bytes = wl.units * (4 * K * V + e * (2 * K + V + 1) + 4 * V)
+    # fp32 SIMT arithmetic: peak = SMs x 128 FMA lanes x 2 flop x max SM clock
+    max_mhz = clk.get("sm_max_mhz") or 2070.0
+    alu_peak = sms * 128 * 2 * max_mhz * 1e6 / 1e12
+    achieved = flops / (bwd_ms / 1e3) / 1e12
+    roof = {"bound": "alu", "achieved": achieved, "peak": alu_peak, "unit": "TFLOP/s",
+            "frac": achieved / alu_peak,
+            "peak_source": "fp32 FMA peak from unit counts and the maximum SM clock",
+            "kernel": "backward_simt_f32_arith", "traffic": None,
+            "algorithmic_flops_per_launch": flops, "algorithmic_bytes_per_launch": bwd_bytes,
+            "hbm_frac": bwd_bytes / (bwd_ms / 1e3) / 1e9 / float(peaks["hbm_gbs"]),
+            "backward_ms": bwd_ms, "forward_train_ms": fwd_ms,
+            "forward_train_hbm_frac": fwd_bytes / (fwd_ms / 1e3) / 1e9 / float(peaks["hbm_gbs"]),
+            "t_hbm_roofline_ms": (fwd_bytes + bwd_bytes) / (float(peaks["hbm_gbs"]) * 1e9) * 1e3,
+            "hbm_peak_gbs": float(peaks["hbm_gbs"]), "hbm_peak_source": peak_src}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        v, desc, cores = oracle_train_sample(wl, args.cpu_seconds)
+        cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
+    launches = 2 + (1 if Nqk == 1 and N > 1 else 0) + 1    # forward, backward, reduce(s)
+    if rank == 0:
+        line = {"metric": METRIC_TRAIN, "value": value, "unit": UNIT, "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16" if wl.dtype == "bf16" else "f32", "data": "synthetic",
+                "config": dict(workload_config(wl), **{"pass": "train"}), "clocks": clk,
+                "e2e": e2e, "gpu_launches": args.steps * launches, "roofline": roof,
+                "cpu_baseline": cpu}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
 # ---------------------------------------------------------------- GPU arm
 def main():
     args = parse()
@@ -272,6 +463,8 @@ def main():
         wl = wl.with_(B=args.batch, name=f"{wl.name}_b{args.batch}")
     if args.impl == "reference":
         return reference_arm(args, wl)
+    if args.which == "train":
+        return main_train(args, wl)
 
     import torch
     import torch.distributed as dist
