@@ -65,6 +65,8 @@ KERNEL_SOURCES = {
     "mma_sync_pipelined": ["m2rnn_bf16_pipe.cu"],
     "tcgen05_k128_v128": ["m2rnn_bf16_tc5.cu"],
     "mma_sync_cluster4_k64_v128": ["m2rnn_bf16_cluster.cu"],
+    "backward_mma_k64_v64": ["m2rnn_bwd_bf16_mma.cu"],
+    "backward_simt": ["m2rnn_bwd_f32.cu"],
 }
 
 
@@ -326,7 +328,8 @@ def main_train(args, wl):
     dy = torch.randn((B, T, N, V), generator=g, device=dev)
     y = torch.empty((B, T, N, V), dtype=torch.float32, device=dev)
     HT = torch.empty((B, N, K, V), dtype=torch.float32, device=dev)
-    Hs = torch.empty((B, N, T, K, V), dtype=torch.float32, device=dev)
+    Hs = torch.empty((B, N, T, K, V), dtype=torch.bfloat16 if wl.dtype == "bf16" else torch.float32,
+                     device=dev)
     grads = {"dq": (B, T, Nqk, K), "dk": (B, T, Nqk, K), "dv": (B, T, N, V), "da": (B, T, N),
              "dalpha": (N,), "dbeta": (N,), "dW": (N, V, V), "dw_r": (N, V), "dH0": (B, N, K, V)}
     grads = {n: torch.empty(shp, dtype=torch.float32, device=dev) for n, shp in grads.items()}
@@ -417,17 +420,21 @@ def main_train(args, wl):
     peaks, peak_src = load_peaks()
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     flops = 6.0 * K * V * V * wl.units   # H_{t-1} W (recomputed), D_t W^T, H_{t-1}^T D_t
-    e = 2 if wl.dtype == "bf16" else 4
-    bwd_bytes = wl.units * (4 * K * V + 4 * V + e * (2 * K + V + 1) + 4 * (2 * K + V + 1))
-    fwd_bytes = wl.units * (4 * K * V + e * (2 * K + V + 1) + 4 * V)
-    # fp32 SIMT arithmetic: peak = SMs x 128 FMA lanes x 2 flop x max SM clock
-    max_mhz = clk.get("sm_max_mhz") or 2070.0
-    alu_peak = sms * 128 * 2 * max_mhz * 1e6 / 1e12
+    e = 2 if wl.dtype == "bf16" else 4   # operand bytes; the kept states use the same dtype
+    bwd_bytes = wl.units * (e * K * V + 4 * V + e * (2 * K + V + 1) + 4 * (2 * K + V + 1))
+    fwd_bytes = wl.units * (e * K * V + e * (2 * K + V + 1) + 4 * V)
     achieved = flops / (bwd_ms / 1e3) / 1e12
-    roof = {"bound": "alu", "achieved": achieved, "peak": alu_peak, "unit": "TFLOP/s",
-            "frac": achieved / alu_peak,
-            "peak_source": "fp32 FMA peak from unit counts and the maximum SM clock",
-            "kernel": "backward_simt_f32_arith", "traffic": None,
+    mma = wl.dtype == "bf16" and K == 64 and V == 64 and args.variant in (0, 2)
+    if mma:   # bf16 warp-MMA products: the measured bf16 dense peak
+        peak, bound = float(peaks["bf16_tflops"]), "tensor"
+        psrc, kname = f"{peak_src} bf16 dense burst (kernel timed alone)", "backward_mma_k64_v64"
+    else:     # fp32 SIMT arithmetic: SMs x 128 FMA lanes x 2 flop x max SM clock
+        max_mhz = clk.get("sm_max_mhz") or 2070.0
+        peak, bound = sms * 128 * 2 * max_mhz * 1e6 / 1e12, "alu"
+        psrc, kname = "fp32 FMA peak from unit counts and the maximum SM clock", "backward_simt"
+    roof = {"bound": bound, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+            "frac": achieved / peak, "peak_source": psrc,
+            "kernel": kname, "traffic": measured_traffic(kname, wl),
             "algorithmic_flops_per_launch": flops, "algorithmic_bytes_per_launch": bwd_bytes,
             "hbm_frac": bwd_bytes / (bwd_ms / 1e3) / 1e9 / float(peaks["hbm_gbs"]),
             "backward_ms": bwd_ms, "forward_train_ms": fwd_ms,

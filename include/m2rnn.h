@@ -120,9 +120,12 @@ m2rnn_status m2rnn_forward_bf16_qk(const uint16_t* q, const uint16_t* k, const u
  * recurrence while keeping every step's state in HBM, then scans time in reverse.
  *
  * m2rnn_forward_train_*: the forward pass of m2rnn_forward_*_qk that also writes
- *   Hs     [B, N, T, K, V]  float32: Hs[b][n][t] = H_t after step t (t = 0..T-1),
- *                           the states the backward reads (B·N·T·K·V·4 bytes).
- *   Hs is required when T > 0.  The bf16 entry takes the pipelined warp-MMA
+ *   Hs     [B, N, T, K, V]  Hs[b][n][t] = H_t after step t (t = 0..T-1), the states
+ *                           the backward reads.  fp32 entry: float32.  bf16 entry:
+ *                           bfloat16 (uint16_t bits), the round-to-nearest-even
+ *                           rounding of H_t, i.e. exactly the tensor-core operand
+ *                           the next step multiplies by W (B·N·T·K·V·2 bytes).
+ *   Hs is required when T > 0 (16-byte aligned on the bf16 entry).  The bf16 entry takes the pipelined warp-MMA
  *   kernel, so it supports K a multiple of 16 with K <= 64 and V in {16, 32, 64}
  *   (UNSUPPORTED otherwise); the fp32 entry supports 1 <= K, V <= 128.
  */
@@ -134,7 +137,7 @@ m2rnn_status m2rnn_forward_train_f32(const float* q, const float* k, const float
 m2rnn_status m2rnn_forward_train_bf16(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                                       const uint16_t* a, const float* alpha, const float* beta,
                                       const uint16_t* W, const float* w_r, const float* H0,
-                                      float* y, float* H_T, float* Hs, int B, int T, int N,
+                                      float* y, float* H_T, uint16_t* Hs, int B, int T, int N,
                                       int Nqk, int K, int V, void* stream);
 
 /*
@@ -162,14 +165,19 @@ size_t m2rnn_backward_workspace_bytes(int B, int T, int N, int Nqk, int K, int V
  *   dq, dk [B, T, Nqk, K]  (summed over heads when Nqk == 1)
  *   dv [B, T, N, V], da [B, T, N], dalpha [N], dbeta [N], dW [N, V, V], dw_r [N, V],
  *   dH0 [B, N, K, V] (not written when NULL).
- * dy [B, T, N, V] is float32.  `workspace` is caller-owned device memory of at least
+ * dy [B, T, N, V] is float32; Hs has the dtype its forward entry wrote (float32 on
+ * the fp32 entry, bf16 bits on the bf16 entry).  On the bf16 entry, t = 0 uses the
+ * bf16 rounding of H0, as the forward's first step did.  `workspace` is caller-owned device memory of at least
  * m2rnn_backward_workspace_bytes(...) bytes (INVALID_ARG otherwise); it is
  * overwritten, so two calls in flight at once need two workspaces.  Sums over the
  * batch run in a fixed order: results are deterministic.
  * Errors: INVALID_ARG for a null required pointer (q, k, v, a, Hs, dy, dq, dk, dv,
  * da are required only when T > 0) or a bad size; UNSUPPORTED for K or V > 128.
- * The bf16 entry takes bf16 q, k, v, a, W; its `variant` is 0 (automatic) or 1
- * (SIMT fp32 arithmetic); fp32 arithmetic throughout on both entries.
+ * The bf16 entry takes bf16 q, k, v, a, W; its `variant` is 0 (automatic: 2 when
+ * K = V = 64 and T > 0, else 1), 1 (SIMT kernel, fp32 arithmetic, any K, V <= 128) or
+ * 2 (tensor-core kernel: H_{t-1} W, D_t W^T and H_{t-1}^T D_t as bf16 warp MMAs with
+ * fp32 accumulation, K = V = 64 only, UNSUPPORTED otherwise; q, k, v, W, Hs, dy, dv,
+ * H0, dH_T, dH0 16-byte aligned).  Bits 8 and up of `variant` are test hooks (0).
  */
 m2rnn_status m2rnn_backward_f32(const float* q, const float* k, const float* v, const float* a,
                                 const float* alpha, const float* beta, const float* W,
@@ -181,7 +189,7 @@ m2rnn_status m2rnn_backward_f32(const float* q, const float* k, const float* v, 
 m2rnn_status m2rnn_backward_bf16(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                                  const uint16_t* a, const float* alpha, const float* beta,
                                  const uint16_t* W, const float* w_r, const float* H0,
-                                 const float* Hs, const float* dy, const float* dH_T, float* dq,
+                                 const uint16_t* Hs, const float* dy, const float* dH_T, float* dq,
                                  float* dk, float* dv, float* da, float* dalpha, float* dbeta,
                                  float* dW, float* dw_r, float* dH0, int B, int T, int N, int Nqk,
                                  int K, int V, int variant, void* workspace,
@@ -203,7 +211,7 @@ m2rnn_status m2rnn_backward_bf16(const uint16_t* q, const uint16_t* k, const uin
 m2rnn_status m2rnn_backward_bf16_noalloc(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                                          const uint16_t* a, const float* alpha, const float* beta,
                                          const uint16_t* W, const float* w_r, const float* H0,
-                                         const float* Hs, const float* dy, const float* dH_T,
+                                         const uint16_t* Hs, const float* dy, const float* dH_T,
                                          float* dq, float* dk, float* dv, float* da, float* dalpha,
                                          float* dbeta, float* dW, float* dw_r, float* dH0, int B,
                                          int T, int N, int Nqk, int K, int V, void* stream);

@@ -243,7 +243,7 @@ m2rnn_status m2rnn_forward_train_f32(const float* q, const float* k, const float
 m2rnn_status m2rnn_forward_train_bf16(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                                       const uint16_t* a, const float* alpha, const float* beta,
                                       const uint16_t* W, const float* w_r, const float* H0,
-                                      float* y, float* H_T, float* Hs, int B, int T, int N,
+                                      float* y, float* H_T, uint16_t* Hs, int B, int T, int N,
                                       int Nqk, int K, int V, void* stream) {
   m2rnn_status st = common_checks(q, k, v, a, alpha, beta, W, w_r, y, B, T, N, K, V);
   if (st != M2RNN_OK) return st;
@@ -290,7 +290,7 @@ m2rnn_status m2rnn_backward_f32(const float* q, const float* k, const float* v, 
 m2rnn_status m2rnn_backward_bf16(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                                  const uint16_t* a, const float* alpha, const float* beta,
                                  const uint16_t* W, const float* w_r, const float* H0,
-                                 const float* Hs, const float* dy, const float* dH_T, float* dq,
+                                 const uint16_t* Hs, const float* dy, const float* dH_T, float* dq,
                                  float* dk, float* dv, float* da, float* dalpha, float* dbeta,
                                  float* dW, float* dw_r, float* dH0, int B, int T, int N, int Nqk,
                                  int K, int V, int variant, void* workspace,
@@ -300,10 +300,25 @@ m2rnn_status m2rnn_backward_bf16(const uint16_t* q, const uint16_t* k, const uin
                     B,  T,  N,  K,      V,     Nqk};
   m2rnn_status st = backward_checks(p, workspace_bytes);
   if (st != M2RNN_OK) return st;
-  if (variant != 0 && variant != 1) return M2RNN_ERR_INVALID_ARG;
-  return launch_bwd_simt_bf16(p, static_cast<cudaStream_t>(stream)) == cudaSuccess
-             ? M2RNN_OK
-             : M2RNN_ERR_CUDA;
+  const int debug = variant >> 8;
+  int base = variant & 0xff;
+  if (base < 0 || base > 2) return M2RNN_ERR_INVALID_ARG;
+  const bool mma_ok = bwd_mma_supports(K, V) && T > 0;
+  if (base == 0) base = mma_ok ? 2 : 1;
+  if (base == 2 && !mma_ok) return M2RNN_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (base == 1) return launch_bwd_simt_bf16(p, s) == cudaSuccess ? M2RNN_OK : M2RNN_ERR_CUDA;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(W, 16) ||
+      !aligned(Hs, 16) || !aligned(dy, 16) || !aligned(dv, 16) || !aligned(dH0, 16) ||
+      !aligned(dH_T, 16) || !aligned(H0, 16) || !aligned(w_r, 8))
+    return M2RNN_ERR_INVALID_ARG;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return M2RNN_ERR_CUDA;
+  int* status = status_address(dev);
+  EncodeTiledFn enc = encode_fn();
+  if (!status || !enc) return M2RNN_ERR_CUDA;
+  return launch_bwd_bf16_mma(p, enc, debug, status, s) == cudaSuccess ? M2RNN_OK
+                                                                      : M2RNN_ERR_CUDA;
 }
 
 m2rnn_status m2rnn_stream_status(void* stream) {

@@ -77,7 +77,7 @@ __global__ void __launch_bounds__(160, 1)
                       const __grid_constant__ CUtensorMap tm_v, const uint16_t* __restrict__ a,
                       const float* __restrict__ alpha, const float* __restrict__ beta,
                       const uint16_t* __restrict__ W, const float* __restrict__ w_r,
-                      const float* H0, float* __restrict__ y, float* H_T, float* __restrict__ Hs,
+                      const float* H0, float* __restrict__ y, float* H_T, uint16_t* __restrict__ Hs,
                       int T, int N, int K, int Tc, int qk_hs, int debug, int* status) {
   constexpr int V = 16 * VT;
   constexpr int NT = 2 * VT;  // n-tiles of 8 columns
@@ -379,12 +379,16 @@ __global__ void __launch_bounds__(160, 1)
     // This step's partial sums are reduced during the next step (or at chunk end).
 #pragma unroll
     for (int i = 0; i < M; ++i) pout[i] = p[i];
-    if constexpr (kCache) {  // keep H_t for the backward pass (streaming stores)
-      float* hp = Hs + ((size_t)pair * T + (size_t)cc * Tc + s) * K * V;
+    if constexpr (kCache) {
+      // Keep H_t for the backward pass as the bf16 A fragments just packed from it:
+      // exactly the tensor-core operand step t+1 uses (streaming stores).
+      uint16_t* hp = Hs + ((size_t)pair * T + (size_t)cc * Tc + s) * K * V;
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        __stcs(reinterpret_cast<float2*>(hp + (size_t)r0 * V + 8 * nt + 2 * c), h[nt][0]);
-        __stcs(reinterpret_cast<float2*>(hp + (size_t)r1 * V + 8 * nt + 2 * c), h[nt][1]);
+      for (int kt = 0; kt < VT; ++kt) {
+        __stcs(reinterpret_cast<unsigned int*>(hp + (size_t)r0 * V + 16 * kt + 2 * c), af[kt][0]);
+        __stcs(reinterpret_cast<unsigned int*>(hp + (size_t)r1 * V + 16 * kt + 2 * c), af[kt][1]);
+        __stcs(reinterpret_cast<unsigned int*>(hp + (size_t)r0 * V + 16 * kt + 8 + 2 * c), af[kt][2]);
+        __stcs(reinterpret_cast<unsigned int*>(hp + (size_t)r1 * V + 16 * kt + 8 + 2 * c), af[kt][3]);
       }
     }
   };
@@ -477,7 +481,8 @@ cudaError_t launch_pipe_vt(const Problem& p, EncodeTiledFn enc, cudaStream_t str
   const unsigned grid = (unsigned)p.B * (unsigned)p.N;
   const int threads = 32 * (p.K / 16 + 1);
   kern<<<grid, threads, L.total, stream>>>(mq, mk, mv, (const uint16_t*)p.a, p.alpha, p.beta,
-                                           (const uint16_t*)p.W, p.w_r, p.H0, p.y, p.H_T, p.Hs, p.T,
+                                           (const uint16_t*)p.W, p.w_r, p.H0, p.y, p.H_T,
+                                           static_cast<uint16_t*>(p.Hs), p.T,
                                            p.N, p.K, Tc, p.Nqk == 1 ? 0 : 1, p.debug, p.status);
   return cudaGetLastError();
 }

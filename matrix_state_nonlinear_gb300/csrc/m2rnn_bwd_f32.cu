@@ -12,7 +12,8 @@
 // and through the gate of Eq. (13)/(17), x = a + beta:
 //   da_t = dL/df_t · (-alpha f sigmoid(x)),  dalpha += dL/df_t · (-f softplus(x)),
 //   dbeta += da_t,  dw_r += u_t ⊙ v_t.
-// The states H_t come from the training forward (kept in HBM, the notes' Sec. 2.6).
+// The states H_t come from the training forward (kept in HBM, the notes' Sec. 2.6):
+// fp32 on the fp32 path, the bf16-rounded state on the bf16 path.
 //
 // One thread block per pair.  W and D_t live in shared memory; the running state
 // gradient C and the pair's partial sums of dW, dw_r, dalpha, dbeta live in the
@@ -33,6 +34,17 @@ __device__ __forceinline__ float ld_in(const uint16_t* p, size_t i) {
   return __uint_as_float((uint32_t)p[i] << 16);
 }
 
+// The value the kept state would hold: itself for fp32 states, its bf16 rounding
+// (round to nearest even, as the tensor-core operand is formed) for bf16 states.
+template <typename Th>
+__device__ __forceinline__ float round_like(float x);
+template <>
+__device__ __forceinline__ float round_like<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ float round_like<uint16_t>(float x) {
+  return __bfloat162float(__float2bfloat16_rn(x));
+}
+
 __device__ __forceinline__ float block_sum(float x, float* red) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
@@ -48,13 +60,13 @@ __device__ __forceinline__ float block_sum(float x, float* red) {
   return red[kThreads / 32];
 }
 
-template <typename Tin>
+template <typename Tin, typename Th>
 __global__ void __launch_bounds__(kThreads)
     bwd_simt_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* __restrict__ v,
                     const Tin* __restrict__ a, const float* __restrict__ alpha,
                     const float* __restrict__ beta, const Tin* __restrict__ W,
                     const float* __restrict__ w_r, const float* __restrict__ H0,
-                    const float* __restrict__ Hs, const float* __restrict__ dy,
+                    const Th* __restrict__ Hs, const float* __restrict__ dy,
                     const float* __restrict__ dH_T, float* __restrict__ dq, float* __restrict__ dk,
                     float* __restrict__ dv, float* __restrict__ da, float* __restrict__ dH0,
                     float* __restrict__ ws, float* __restrict__ dqk_heads, int T, int N, int K,
@@ -110,24 +122,29 @@ __global__ void __launch_bounds__(kThreads)
     }
     __syncthreads();
     const float f = gate[0], g = gate[1];
-    const float* Hp = t > 0 ? Hs + ((size_t)pair * T + t - 1) * KV
-                            : (H0 ? H0 + (size_t)pair * KV : nullptr);  // H_{t-1}
-    const float* Hc = Hs + ((size_t)pair * T + t) * KV;                // H_t
+    // H_{t-1} from the kept states (H_0 itself for t = 0; the bf16 path keeps the
+    // bf16-rounded states and rounds H_0 the same way), and H_t.
+    const Th* Hp = t > 0 ? Hs + ((size_t)pair * T + t - 1) * KV : nullptr;
+    const float* H0p = H0 ? H0 + (size_t)pair * KV : nullptr;
+    const Th* Hc = Hs + ((size_t)pair * T + t) * KV;
+    auto hprev = [&](size_t e) -> float {
+      if (Hp) return ld_in(Hp, e);
+      return H0p ? round_like<Th>(H0p[e]) : 0.f;
+    };
+    const bool have_prev = Hp || H0p;
 
     // Phase 1: Z_t, R_t, D_t and the partial <R_t, H_{t-1} - Z_t>.
     float dfl = 0.f;
     for (int e = tid; e < KV; e += kThreads) {
       const int i = e / V, j = e - (e / V) * V;
       float acc = ks[i] * vs[j];  // same order as the fp32 forward: rank-1, then l = 0..V-1
-      if (Hp) {
-        const float* hrow = Hp + (size_t)i * V;
-        for (int l = 0; l < V; ++l) acc = fmaf(hrow[l], Ws[l * V + j], acc);
-      }
+      if (have_prev)
+        for (int l = 0; l < V; ++l) acc = fmaf(hprev((size_t)i * V + l), Ws[l * V + j], acc);
       const float Z = tanhf(acc);
       const float R = Cw[e] + qs[i] * us[j];
       Ds[e] = g * R * (1.f - Z * Z);
       Cw[e] = R;
-      dfl += R * ((Hp ? Hp[e] : 0.f) - Z);
+      dfl += R * (hprev(e) - Z);
     }
     const float df = block_sum(dfl, red);  // also orders Ds writes before the reads below
 
@@ -141,11 +158,11 @@ __global__ void __launch_bounds__(kThreads)
       Cw[e] = fmaf(f, Cw[e], acc);
     }
     // dW partial += H_{t-1}^T D_t.
-    if (Hp) {
+    if (have_prev) {
       for (int e = tid; e < VV; e += kThreads) {
         const int l = e / V, j = e - (e / V) * V;
         float acc = dWp[e];
-        for (int i = 0; i < K; ++i) acc = fmaf(Hp[(size_t)i * V + l], Ds[i * V + j], acc);
+        for (int i = 0; i < K; ++i) acc = fmaf(hprev((size_t)i * V + l), Ds[i * V + j], acc);
         dWp[e] = acc;
       }
     }
@@ -154,7 +171,7 @@ __global__ void __launch_bounds__(kThreads)
       float sk = 0.f, sq = 0.f;
       for (int j = 0; j < V; ++j) {
         sk = fmaf(Ds[i * V + j], vs[j], sk);
-        sq = fmaf(Hc[(size_t)i * V + j], us[j], sq);
+        sq = fmaf(ld_in(Hc, (size_t)i * V + j), us[j], sq);
       }
       if (shared_qk) {
         dqk_heads[row * K + i] = sq;
@@ -228,18 +245,18 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
-template <typename Tin>
+template <typename Tin, typename Th>
 cudaError_t launch_simt(const BackwardProblem& p, cudaStream_t stream) {
   const size_t smem = sizeof(float) * ((size_t)p.V * p.V + (size_t)p.K * p.V + 2 * p.K +
                                        2 * p.V + 4 + kThreads / 32 + 1);
-  cudaError_t err = cudaFuncSetAttribute(bwd_simt_kernel<Tin>,
+  cudaError_t err = cudaFuncSetAttribute(bwd_simt_kernel<Tin, Th>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   const unsigned pairs = (unsigned)p.B * (unsigned)p.N;
   float* heads = p.ws + (size_t)p.B * p.N * backward_pair_floats(p.K, p.V);
-  bwd_simt_kernel<Tin><<<pairs, kThreads, smem, stream>>>(
+  bwd_simt_kernel<Tin, Th><<<pairs, kThreads, smem, stream>>>(
       (const Tin*)p.q, (const Tin*)p.k, (const Tin*)p.v, (const Tin*)p.a, p.alpha, p.beta,
-      (const Tin*)p.W, p.w_r, p.H0, p.Hs, p.dy, p.dH_T, p.dq, p.dk, p.dv, p.da, p.dH0, p.ws, heads,
+      (const Tin*)p.W, p.w_r, p.H0, (const Th*)p.Hs, p.dy, p.dH_T, p.dq, p.dk, p.dv, p.da, p.dH0, p.ws, heads,
       p.T, p.N, p.K, p.V, p.Nqk);
   return cudaGetLastError();
 }
@@ -264,12 +281,12 @@ cudaError_t launch_bwd_reduce(const BackwardProblem& p, cudaStream_t stream) {
 }
 
 cudaError_t launch_bwd_f32(const BackwardProblem& p, cudaStream_t stream) {
-  cudaError_t err = launch_simt<float>(p, stream);
+  cudaError_t err = launch_simt<float, float>(p, stream);
   return err == cudaSuccess ? launch_bwd_reduce(p, stream) : err;
 }
 
 cudaError_t launch_bwd_simt_bf16(const BackwardProblem& p, cudaStream_t stream) {
-  cudaError_t err = launch_simt<uint16_t>(p, stream);
+  cudaError_t err = launch_simt<uint16_t, uint16_t>(p, stream);
   return err == cudaSuccess ? launch_bwd_reduce(p, stream) : err;
 }
 

@@ -100,7 +100,8 @@ cudaError_t launch_fwd_f32(const Problem& p, cudaStream_t stream) {
   const unsigned grid = (unsigned)p.B * (unsigned)p.N;
   fwd_f32_kernel<<<grid, kThreads, smem, stream>>>(
       (const float*)p.q, (const float*)p.k, (const float*)p.v, (const float*)p.a, p.alpha, p.beta,
-      (const float*)p.W, p.w_r, p.H0, p.y, p.H_T, p.Hs, p.T, p.N, p.K, p.V, p.Nqk);
+      (const float*)p.W, p.w_r, p.H0, p.y, p.H_T, static_cast<float*>(p.Hs), p.T, p.N, p.K, p.V,
+      p.Nqk);
   return cudaGetLastError();
 }
 

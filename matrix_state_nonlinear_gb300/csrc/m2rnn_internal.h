@@ -35,7 +35,8 @@ struct Problem {
   int Nqk;          // heads of q and k: N (one per head) or 1 (shared by all heads)
   int debug;        // kDebug* bits (tests only)
   int* status;      // device address of this device's status word
-  float* Hs = nullptr;  // optional: every step's state, fp32 [B, N, T, K, V]
+  void* Hs = nullptr;  // optional: every step's state [B, N, T, K, V] (fp32 path: float;
+                      // bf16 path: the bf16-rounded state, uint16_t bits)
 };
 
 // Backward pass (reverse scan of the notes' Sec. 2.7).  Pointers as in the C ABI;
@@ -50,7 +51,7 @@ struct BackwardProblem {
   const void* W;
   const float* w_r;
   const float* H0;   // may be null (zero initial state)
-  const float* Hs;   // [B, N, T, K, V] states of the training forward
+  const void* Hs;    // [B, N, T, K, V] states of the training forward (fp32 or bf16 bits)
   const float* dy;   // [B, T, N, V]
   const float* dH_T; // may be null (zero)
   float* dq;         // [B, T, Nqk, K]
@@ -112,5 +113,11 @@ cudaError_t launch_fwd_bf16_tc5(const Problem& p, EncodeTiledFn enc, cudaStream_
 // SMs, readout partials exchanged through distributed shared memory): K = 64, V = 128.
 bool mma_cluster_supports(int K, int V);
 cudaError_t launch_fwd_bf16_mma_cluster(const Problem& p, EncodeTiledFn enc, cudaStream_t stream);
+
+// Tensor-core backward (warp-level MMA, TMA-staged bf16 states), K = V = 64, then the
+// reduction.  `debug` takes the kDebug* bits; `status` is the device status word.
+bool bwd_mma_supports(int K, int V);
+cudaError_t launch_bwd_bf16_mma(const BackwardProblem& p, EncodeTiledFn enc, int debug,
+                                int* status, cudaStream_t stream);
 
 }  // namespace m2rnn

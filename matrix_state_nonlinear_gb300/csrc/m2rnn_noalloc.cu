@@ -52,7 +52,7 @@ using namespace m2rnn;
 
 extern "C" m2rnn_status m2rnn_backward_bf16_noalloc(
     const uint16_t* q, const uint16_t* k, const uint16_t* v, const uint16_t* a, const float* alpha,
-    const float* beta, const uint16_t* W, const float* w_r, const float* H0, const float* Hs,
+    const float* beta, const uint16_t* W, const float* w_r, const float* H0, const uint16_t* Hs,
     const float* dy, const float* dH_T, float* dq, float* dk, float* dv, float* da, float* dalpha,
     float* dbeta, float* dW, float* dw_r, float* dH0, int B, int T, int N, int Nqk, int K, int V,
     void* stream) {

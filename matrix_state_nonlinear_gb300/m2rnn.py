@@ -217,7 +217,8 @@ def _shape_of(inputs):
 def m2rnn_forward_train(inputs: dict, y=None, H_T=None, Hs=None, stream=None):
     """Forward pass that also keeps every step's state for the backward pass.
 
-    Returns (y, H_T, Hs) with Hs float32 [B, N, T, K, V] (Hs[:, :, t] = H_t).
+    Returns (y, H_T, Hs) with Hs [B, N, T, K, V] (Hs[:, :, t] = H_t): float32 on the
+    fp32 path, bfloat16 (the rounding the tensor cores consume) on the bf16 path.
     Dispatches on the operand dtype of q like ``m2rnn_forward``.
     """
     lib = load_library()
@@ -226,10 +227,10 @@ def m2rnn_forward_train(inputs: dict, y=None, H_T=None, Hs=None, stream=None):
     dev = q.device
     if H_T is None:
         H_T = torch.empty((B, N, K, V), dtype=torch.float32, device=dev)
-    if Hs is None:
-        Hs = torch.empty((B, N, T, K, V), dtype=torch.float32, device=dev)
-    _check(Hs, "Hs", torch.float32, (B, N, T, K, V), dev)
     opdtype = torch.float32 if q.dtype == torch.float32 else torch.bfloat16
+    if Hs is None:
+        Hs = torch.empty((B, N, T, K, V), dtype=opdtype, device=dev)
+    _check(Hs, "Hs", opdtype, (B, N, T, K, V), dev)
     args = [inputs[x] for x in ("q", "k", "v", "a", "alpha", "beta", "W", "w_r")]
     ptrs, _, y, _ = _marshal(*args, inputs.get("H0"), y, H_T, opdtype)
     fn = lib.m2rnn_forward_train_f32 if opdtype == torch.float32 else lib.m2rnn_forward_train_bf16
@@ -259,7 +260,7 @@ def m2rnn_backward(inputs: dict, Hs, dy, dH_T=None, grads=None, workspace=None, 
     opdtype = torch.float32 if q.dtype == torch.float32 else torch.bfloat16
     args = [inputs[x] for x in ("q", "k", "v", "a", "alpha", "beta", "W", "w_r")]
     ptrs, _, _, _ = _marshal(*args, inputs.get("H0"), dy, None, opdtype)
-    _check(Hs, "Hs", torch.float32, (B, N, T, K, V), dev)
+    _check(Hs, "Hs", opdtype, (B, N, T, K, V), dev)
     _check(dy, "dy", torch.float32, (B, T, N, V), dev)
     _check(dH_T, "dH_T", torch.float32, (B, N, K, V), dev)
     shapes = {"dq": (B, T, Nqk, K), "dk": (B, T, Nqk, K), "dv": (B, T, N, V), "da": (B, T, N),
@@ -296,7 +297,7 @@ def m2rnn_backward_noalloc(inputs: dict, Hs, dy, dH_T=None, grads=None, stream=N
     dev = q.device
     args = [inputs[x] for x in ("q", "k", "v", "a", "alpha", "beta", "W", "w_r")]
     ptrs, _, _, _ = _marshal(*args, inputs.get("H0"), dy, None, torch.bfloat16)
-    _check(Hs, "Hs", torch.float32, (B, N, T, K, V), dev)
+    _check(Hs, "Hs", torch.bfloat16, (B, N, T, K, V), dev)
     _check(dH_T, "dH_T", torch.float32, (B, N, K, V), dev)
     shapes = {"dq": (B, T, Nqk, K), "dk": (B, T, Nqk, K), "dv": (B, T, N, V), "da": (B, T, N),
               "dalpha": (N,), "dbeta": (N,), "dW": (N, V, V), "dw_r": (N, V),

@@ -5,8 +5,9 @@ Tolerances (max-abs error per gradient tensor, scaled by max(1, max |oracle|)):
   * fp32 path: 1e-4.  Every step is fp32 with accurate tanh/exp; the reverse scan
     adds one rounding per operation along T steps, far below 1e-4 at these sizes.
   * bf16 path: 3e-2.  The kept states come from the bf16-operand forward, whose
-    states differ from the exact ones by up to its own bar (3e-2); the gradients
-    are smooth in the states, so they carry errors of the same relative size.
+    states differ from the exact ones by up to its own bar (3e-2), and are kept
+    rounded to bf16 (relative 2^-9); the gradients are smooth in the states, so
+    they carry errors of the same relative size.
 """
 import numpy as np
 import pytest
@@ -45,13 +46,13 @@ def rel_err(got, want):
     return float(np.abs(got - want).max()) / max(1.0, float(np.abs(want).max())) if want.size else 0.0
 
 
-def run_case(dtype, B, T, N, K, V, h0="uniform", shared=False, with_dHT=True, seed=0):
+def run_case(dtype, B, T, N, K, V, h0="uniform", shared=False, with_dHT=True, seed=0, variant=0):
     wl = Workload("bwd", B, T, N, K, V, dtype=dtype, h0=h0, shared_qk=shared,
                   rescale_w=dtype == "bf16")
     inp = make_inputs(wl, DEV, seed)
     y, HT, Hs = pkg.m2rnn_forward_train(inp)
     dy, dHT = upstream(B, T, N, K, V, seed + 1, with_dHT)
-    g = pkg.m2rnn_backward(inp, Hs, dy, dHT)
+    g = pkg.m2rnn_backward(inp, Hs, dy, dHT, variant=variant)
     assert pkg.stream_status() == binding.OK
     ref = m2rnn_backward_inputs(all_f64(inp), dy.double().cpu().numpy(),
                                 None if dHT is None else dHT.double().cpu().numpy())
@@ -109,25 +110,67 @@ def test_forward_train_keeps_states_and_matches_plain_forward():
         y, HT, Hs = pkg.m2rnn_forward_train(inp)
         y2, HT2 = pkg.m2rnn_forward(inp)
         assert torch.equal(y, y2) and torch.equal(HT, HT2)     # same arithmetic, bit for bit
-        assert torch.equal(Hs[:, :, T - 1], HT)
+        assert torch.equal(Hs[:, :, T - 1], HT.to(Hs.dtype))    # bf16: round to nearest even
         _, _, states = m2rnn_forward_inputs(all_f64(inp), return_states=True)
         err = float(np.abs(Hs.double().cpu().numpy() - np.moveaxis(states, 1, 2)).max())
         assert err <= TOL[dtype], err
 
 
-BF16_SHAPES = [(1, 1, 1, 16, 16), (2, 65, 3, 64, 64), (1, 130, 2, 32, 32), (2, 40, 2, 48, 16)]
+BF16_SHAPES = [(1, 1, 1, 16, 16), (2, 65, 3, 64, 64), (1, 130, 2, 32, 32), (2, 40, 2, 48, 16),
+               (1, 1, 1, 64, 64), (1, 4, 2, 64, 64), (1, 5, 1, 64, 64), (2, 131, 2, 64, 64),
+               (1, 7, 2, 64, 64)]
+
+
+def bwd_variants(K, V):
+    # 1: SIMT (any shape); 2: tensor-core kernel (K = V = 64)
+    return [1, 2] if (K, V) == (64, 64) else [1]
 
 
 @pytest.mark.parametrize("shape", BF16_SHAPES)
-def test_backward_bf16_matches_oracle(shape):
-    _, _, _, errs = run_case("bf16", *shape)
-    assert max(errs.values()) <= TOL["bf16"], errs
+@pytest.mark.parametrize("h0", ["zero", "uniform"])
+def test_backward_bf16_matches_oracle(shape, h0):
+    for variant in bwd_variants(shape[3], shape[4]):
+        _, _, _, errs = run_case("bf16", *shape, h0=h0, variant=variant)
+        assert max(errs.values()) <= TOL["bf16"], (variant, errs)
 
 
-def test_backward_bf16_shared_qk():
-    _, _, g, errs = run_case("bf16", 2, 50, 4, 64, 64, shared=True)
+@pytest.mark.parametrize("variant", [1, 2])
+def test_backward_bf16_shared_qk(variant):
+    _, _, g, errs = run_case("bf16", 2, 50, 4, 64, 64, shared=True, variant=variant)
     assert g["dq"].shape[2] == 1
     assert max(errs.values()) <= TOL["bf16"], errs
+
+
+def test_backward_mma_without_dHT():
+    _, _, _, errs = run_case("bf16", 2, 37, 2, 64, 64, with_dHT=False, variant=2)
+    assert max(errs.values()) <= TOL["bf16"], errs
+
+
+def test_backward_mma_close_to_simt():
+    """Both kernels differentiate the same kept states; they differ only by rounding
+    (bf16 D in the MMA products vs fp32 SIMT sums)."""
+    wl = Workload("cmp", 2, 90, 3, 64, 64, h0="uniform")
+    inp = make_inputs(wl, DEV, 8)
+    _, _, Hs = pkg.m2rnn_forward_train(inp)
+    dy, dHT = upstream(2, 90, 3, 64, 64, 9)
+    g1 = pkg.m2rnn_backward(inp, Hs, dy, dHT, variant=1)
+    g2 = pkg.m2rnn_backward(inp, Hs, dy, dHT, variant=2)
+    for n in GRADS:
+        assert rel_err(g2[n], g1[n].double().cpu().numpy()) <= 1e-2, n
+
+
+def test_backward_mma_forced_timeout_is_reported():
+    wl = Workload("to", 2, 20, 2, 64, 64, h0="uniform")
+    inp = make_inputs(wl, DEV, 3)
+    _, _, Hs = pkg.m2rnn_forward_train(inp)
+    dy, dHT = upstream(2, 20, 2, 64, 64, 4)
+    pkg.m2rnn_backward(inp, Hs, dy, dHT, variant=2 | (1 << 8))
+    assert pkg.stream_status() == binding.ERR_TIMEOUT
+    assert pkg.stream_status() == binding.OK
+    g = pkg.m2rnn_backward(inp, Hs, dy, dHT, variant=2)     # the context still works
+    ref = m2rnn_backward_inputs(all_f64(inp), dy.double().cpu().numpy(),
+                                dHT.double().cpu().numpy())
+    assert max(rel_err(g[n], ref[n]) for n in GRADS) <= TOL["bf16"]
 
 
 def test_backward_is_deterministic():
@@ -144,7 +187,7 @@ def test_backward_is_deterministic():
 def test_backward_empty_sequence():
     wl = Workload("e", 2, 0, 2, 8, 8, dtype="f32", h0="uniform", rescale_w=False)
     inp = make_inputs(wl, DEV, 1)
-    Hs = torch.empty((2, 2, 0, 8, 8), device=DEV)
+    Hs = torch.empty((2, 2, 0, 8, 8), device=DEV)      # fp32 path: float32 states
     dy = torch.empty((2, 0, 2, 8), device=DEV)
     dHT = torch.randn((2, 2, 8, 8), device=DEV)
     g = pkg.m2rnn_backward(inp, Hs, dy, dHT)
