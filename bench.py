@@ -47,9 +47,10 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--batch", type=int, default=None,
                     help="override B of the workload (smaller cases for profiling)")
-    ap.add_argument("--pass", dest="which", default="forward", choices=["forward", "train"],
+    ap.add_argument("--pass", dest="which", default="forward",
+                    choices=["forward", "train", "decode"],
                     help="forward: the forward pass (default); train: the state-keeping "
-                         "forward plus the backward pass")
+                         "forward plus the backward pass; decode: one-token decode steps")
     return ap.parse_args()
 
 
@@ -67,6 +68,7 @@ KERNEL_SOURCES = {
     "mma_sync_cluster4_k64_v128": ["m2rnn_bf16_cluster.cu"],
     "backward_mma_k64_v64": ["m2rnn_bwd_bf16_mma.cu"],
     "backward_simt": ["m2rnn_bwd_f32.cu"],
+    "decode_bf16_mma": ["m2rnn_decode.cu"],
 }
 
 
@@ -461,10 +463,188 @@ def main_train(args, wl):
     return 0
 
 
+# ---------------------------------------------------------------- decode step
+METRIC_DECODE = "M²RNN decode step (T = 1, state in / out) tokens·heads/s"
+# Serving batches for the headline head shape (N = 16, K = V = 64).  The large batch
+# keeps 268 MB of fp32 state, more than L2, so each step streams the state from HBM.
+DECODE_BATCHES = {"decode_b1024_n16_k64_v64": 1024, "decode_b8_n16_k64_v64": 8}
+
+
+def decode_reference(args):
+    """The fp64 oracle on the same decode step (one token, the whole batch)."""
+    rank, _, _ = dist_env()
+    if rank != 0:
+        return 0
+    from matrix_state_nonlinear_gb300.inputs import Workload, make_inputs, to_f64_numpy
+    from oracle import m2rnn_forward
+
+    name = args.workload if args.workload in DECODE_BATCHES else "decode_b1024_n16_k64_v64"
+    B, N, K, V = DECODE_BATCHES[name], 16, 64, 64
+    arrs = {k: to_f64_numpy(v) for k, v in
+            make_inputs(Workload(name, B, 1, N, K, V, h0="uniform"), "cpu", 0).items()}
+    vals = []
+    c0, t_all = time.process_time(), time.perf_counter()
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        m2rnn_forward(arrs["q"], arrs["k"], arrs["v"], arrs["a"], arrs["alpha"], arrs["beta"],
+                      arrs["W"], arrs["w_r"], arrs["H0"])
+        if i >= args.warmup:
+            vals.append(B * N / (time.perf_counter() - t0))
+    cores = max(1, round((time.process_time() - c0) / (time.perf_counter() - t_all)))
+    value = statistics.median(vals)
+    desc = f"one decode step of {name} (fp64 NumPy oracle, {B * N} token-heads per step)"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC_DECODE, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": None,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": name, "B": B, "T": 1, "N": N, "K": K, "V": V,
+                                        "pass": "decode"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+    return 0
+
+
+def main_decode(args):
+    """One step = one m2rnn_decode_step_bf16 call over the batch (state updated in place).
+    Also reports the per-step latency with the steps replayed from a CUDA graph."""
+    import torch
+
+    import __graft_entry__
+    import matrix_state_nonlinear_gb300 as pkg
+    from matrix_state_nonlinear_gb300.inputs import Workload, make_inputs
+
+    name = args.workload if args.workload in DECODE_BATCHES else "decode_b1024_n16_k64_v64"
+    B, N, K, V = DECODE_BATCHES[name], 16, 64, 64
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    __graft_entry__.build()
+    pkg.load_library()
+    wl = Workload(name, B, 1, N, K, V, h0="uniform")
+    inp = make_inputs(wl, dev, seed=rank_seed(rank))
+    args_ = (inp["q"][:, 0].contiguous(), inp["k"][:, 0].contiguous(), inp["v"][:, 0].contiguous(),
+             inp["a"][:, 0].contiguous(), inp["alpha"], inp["beta"], inp["W"], inp["w_r"])
+    H = inp["H0"].clone()
+    y = torch.empty((B, N, V), device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        pkg.m2rnn_decode_step(*args_, H, y=y, stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    if pkg.stream_status(stream) != 0:
+        raise RuntimeError("device status not OK after warm-up")
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize(dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = ev0.elapsed_time(ev1) / args.steps
+    # the same steps replayed from a CUDA graph (no per-call host work)
+    g_steps = 64
+    s2 = torch.cuda.Stream(dev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s2):
+        with torch.cuda.graph(graph, stream=s2):
+            for _ in range(g_steps):
+                pkg.m2rnn_decode_step(*args_, H, y=y, stream=s2)
+    graph.replay()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    graph_ms = e0.elapsed_time(e1) / g_steps
+    clk = clocks.stop()
+    if pkg.stream_status(stream) != 0:
+        raise RuntimeError("device status not OK after the timed steps")
+    units = B * N
+    value = units / (ms / 1e3)
+
+    e2e = None
+    if not args.no_e2e:
+        names = ["q", "k", "v", "a"]
+        host = [x.cpu().pin_memory() for x in args_[:4]]
+        dev_in = [torch.empty_like(x) for x in args_[:4]]
+        y_h = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
+        h2d = sum(x.numel() * x.element_size() for x in host)
+        d2h = y_h.numel() * 4
+
+        def e2e_step():
+            for d, h in zip(dev_in, host):
+                d.copy_(h, non_blocking=True)
+            pkg.m2rnn_decode_step(*dev_in, *args_[4:], H, y=y, stream=stream)
+            y_h.copy_(y, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        e_steps = max(10, min(args.steps, 200))
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(e_steps):
+            e2e_step()
+        a1.record(stream)
+        torch.cuda.synchronize(dev)
+        e_ms = a0.elapsed_time(a1) / e_steps
+        e2e = {"value": units / (e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e_ms, "steps": e_steps,
+               "note": "token inputs host->device, y device->host; the state stays resident"}
+
+    peaks, peak_src = load_peaks()
+    hbm = units * (2 * K * V * 4 + 2 * (2 * K + V + 1) + 4 * V) + N * V * V * 2
+    achieved = hbm / (ms / 1e3) / 1e9
+    roof = {"bound": "hbm", "achieved": achieved, "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
+            "frac": achieved / float(peaks["hbm_gbs"]),
+            "peak_source": f"{peak_src} HBM copy bandwidth", "kernel": "decode_bf16_mma",
+            "traffic": measured_traffic("decode_bf16_mma", wl),
+            "algorithmic_bytes_per_launch": hbm, "graph_replay_ms_per_step": graph_ms,
+            "graph_achieved_gbs": hbm / (graph_ms / 1e3) / 1e9}
+    line = {"metric": METRIC_DECODE, "value": value, "unit": UNIT, "n_gpus": 1,
+            "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": name, "B": B, "T": 1, "N": N, "K": K, "V": V,
+                       "operands": "bf16", "state": "f32", "pass": "decode",
+                       "l2": ("state larger than L2 (no flush between steps)" if
+                              B * N * K * V * 4 > L2_BYTES else
+                              "state fits in L2 (latency case; not flushed)"),
+                       "parallelism": "replicas (one independent workload per GPU)"},
+            "clocks": clk, "e2e": e2e, "gpu_launches": args.steps, "roofline": roof,
+            "cpu_baseline": None}
+    if not args.no_cpu_baseline:   # the oracle on the same step, on the host cores
+        from matrix_state_nonlinear_gb300.inputs import to_f64_numpy
+        from oracle import m2rnn_forward
+        Bs = max(1, min(B, 256))   # a bounded sample of the batch
+        arrs = {k_: to_f64_numpy(v_[:Bs] if k_ in ("q", "k", "v", "a", "H0") else v_)
+                for k_, v_ in inp.items()}
+        c0, t0 = time.process_time(), time.perf_counter()
+        m2rnn_forward(arrs["q"], arrs["k"], arrs["v"], arrs["a"], arrs["alpha"], arrs["beta"],
+                      arrs["W"], arrs["w_r"], arrs["H0"])
+        wall = time.perf_counter() - t0
+        line["cpu_baseline"] = {
+            "value": Bs * N / wall, "unit": UNIT, "kind": "oracle",
+            "cores": max(1, round((time.process_time() - c0) / wall)),
+            "sample": f"one decode step of the first {Bs} of {B} batch rows "
+                      f"(fp64 NumPy oracle, {Bs * N} token-heads, {wall:.2f} s wall)"}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 # ---------------------------------------------------------------- GPU arm
 def main():
     args = parse()
     from matrix_state_nonlinear_gb300.inputs import HEADLINE, WORKLOADS
+    if args.which == "decode":
+        return main_decode(args) if args.impl == "ours" else decode_reference(args)
     wl = WORKLOADS[args.workload or HEADLINE]
     if args.batch:
         wl = wl.with_(B=args.batch, name=f"{wl.name}_b{args.batch}")

@@ -216,6 +216,28 @@ m2rnn_status m2rnn_backward_bf16_noalloc(const uint16_t* q, const uint16_t* k, c
                                          float* dbeta, float* dW, float* dw_r, float* dH0, int B,
                                          int T, int N, int Nqk, int K, int V, void* stream);
 
+/*
+ * One decode step (T = 1) for serving with a fixed-size state: the forward pass of a
+ * single token per (b, n), state in, state out.
+ *   q, k   [B, Nqk, K] bf16 (Nqk == N, or 1 shared by all heads)
+ *   v      [B, N, V] bf16,  a [B, N] bf16
+ *   H_in   [B, N, K, V] float32 state before the token (NULL: zero state)
+ *   H_out  [B, N, K, V] float32 state after the token (required; H_out == H_in updates
+ *          the state in place)
+ *   y      [B, N, V] float32
+ * The arithmetic is exactly one step of m2rnn_forward_bf16 (K <= 64, V <= 64 path),
+ * so T successive calls reproduce a T-step forward bit for bit.  No TMA and no
+ * pipelining: the launch is a single small kernel, suitable for CUDA-graph capture.
+ * Supports K a multiple of 16 with K <= 128 and V in {16, 32, 64} (UNSUPPORTED
+ * otherwise).  Same pointer and size errors as m2rnn_forward_bf16 (INVALID_ARG for a
+ * null H_out, or W not 16-byte aligned).
+ */
+m2rnn_status m2rnn_decode_step_bf16(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                    const uint16_t* a, const float* alpha, const float* beta,
+                                    const uint16_t* W, const float* w_r, const float* H_in,
+                                    float* H_out, float* y, int B, int N, int Nqk, int K, int V,
+                                    void* stream);
+
 /* Name of a bf16 kernel variant (NULL for an unknown id).  Id 0 is "auto". */
 const char* m2rnn_variant_name(int variant);
 

@@ -321,6 +321,25 @@ m2rnn_status m2rnn_backward_bf16(const uint16_t* q, const uint16_t* k, const uin
                                                                       : M2RNN_ERR_CUDA;
 }
 
+m2rnn_status m2rnn_decode_step_bf16(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                    const uint16_t* a, const float* alpha, const float* beta,
+                                    const uint16_t* W, const float* w_r, const float* H_in,
+                                    float* H_out, float* y, int B, int N, int Nqk, int K, int V,
+                                    void* stream) {
+  m2rnn_status st = common_checks(q, k, v, a, alpha, beta, W, w_r, y, B, 1, N, K, V);
+  if (st != M2RNN_OK) return st;
+  if (!H_out) return M2RNN_ERR_INVALID_ARG;
+  if (Nqk != 1 && Nqk != N) return M2RNN_ERR_INVALID_ARG;
+  if (!decode_supports(K, V)) return M2RNN_ERR_UNSUPPORTED;
+  if (!aligned(v, 4) || !aligned(W, 16) || !aligned(H_in, 8) || !aligned(H_out, 8) ||
+      !aligned(q, 2) || !aligned(k, 2) || !aligned(a, 2))
+    return M2RNN_ERR_INVALID_ARG;
+  Problem p{q, k, v, a, alpha, beta, W, w_r, H_in, y, H_out, B, 1, N, K, V, Nqk, 0, nullptr};
+  return launch_decode_bf16(p, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? M2RNN_OK
+             : M2RNN_ERR_CUDA;
+}
+
 m2rnn_status m2rnn_stream_status(void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return M2RNN_ERR_CUDA;

@@ -120,4 +120,10 @@ bool bwd_mma_supports(int K, int V);
 cudaError_t launch_bwd_bf16_mma(const BackwardProblem& p, EncodeTiledFn enc, int debug,
                                 int* status, cudaStream_t stream);
 
+// One decode step (T = 1) on the warp MMA, no TMA: K % 16 == 0, K <= 128,
+// V in {16, 32, 64}.  Uses q, k, v, a, alpha, beta, W, w_r, H0 (state in, may be
+// null), H_T (state out, may equal H0), y, B, N, K, V, Nqk of the problem.
+bool decode_supports(int K, int V);
+cudaError_t launch_decode_bf16(const Problem& p, cudaStream_t stream);
+
 }  // namespace m2rnn

@@ -38,6 +38,7 @@ SYMBOLS = {
     "m2rnn_backward_f32": (_I, [_P] * 21 + [_I] * 6 + [_P, ctypes.c_size_t, _P]),
     "m2rnn_backward_bf16": (_I, [_P] * 21 + [_I] * 7 + [_P, ctypes.c_size_t, _P]),
     "m2rnn_backward_bf16_noalloc": (_I, [_P] * 21 + [_I] * 6 + [_P]),
+    "m2rnn_decode_step_bf16": (_I, [_P] * 11 + [_I] * 5 + [_P]),
 }
 
 _lib = None
@@ -313,3 +314,37 @@ def m2rnn_backward_noalloc(inputs: dict, Hs, dy, dH_T=None, grads=None, stream=N
     if st != OK:
         raise M2RNNError(st, "m2rnn_backward_bf16_noalloc")
     return out
+
+
+def m2rnn_decode_step(q, k, v, a, alpha, beta, W, w_r, H_in, H_out=None, y=None, stream=None):
+    """One decode step (bf16 operands): q, k [B, Nqk, K]; v [B, N, V]; a [B, N]; state
+    H_in [B, N, K, V] float32 (None: zero).  Writes H_out (defaults to H_in, in place,
+    when H_in is given) and y [B, N, V]; returns (y, H_out)."""
+    lib = load_library()
+    B, Nqk, K = q.shape
+    N, V = v.shape[1], v.shape[2]
+    dev = q.device
+    if q.device.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    for t, name, dt, shp in [(q, "q", torch.bfloat16, (B, Nqk, K)),
+                             (k, "k", torch.bfloat16, (B, Nqk, K)),
+                             (v, "v", torch.bfloat16, (B, N, V)), (a, "a", torch.bfloat16, (B, N)),
+                             (alpha, "alpha", torch.float32, (N,)),
+                             (beta, "beta", torch.float32, (N,)),
+                             (W, "W", torch.bfloat16, (N, V, V)),
+                             (w_r, "w_r", torch.float32, (N, V)),
+                             (H_in, "H_in", torch.float32, (B, N, K, V))]:
+        _check(t, name, dt, shp, dev)
+    if H_out is None:
+        H_out = H_in if H_in is not None else torch.empty((B, N, K, V), dtype=torch.float32,
+                                                          device=dev)
+    _check(H_out, "H_out", torch.float32, (B, N, K, V), dev)
+    if y is None:
+        y = torch.empty((B, N, V), dtype=torch.float32, device=dev)
+    _check(y, "y", torch.float32, (B, N, V), dev)
+    st = lib.m2rnn_decode_step_bf16(*[_ptr(x) for x in (q, k, v, a, alpha, beta, W, w_r, H_in,
+                                                        H_out, y)],
+                                    B, N, Nqk, K, V, ctypes.c_void_p(_stream_ptr(stream)))
+    if st != OK:
+        raise M2RNNError(st, "m2rnn_decode_step_bf16")
+    return y, H_out

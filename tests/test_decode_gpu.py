@@ -1,0 +1,95 @@
+"""Decode step (T = 1, state in / state out) on the GPU.
+
+The decode kernel performs exactly one step of the pipelined forward kernel, so:
+  * one call equals the forward over a single token, bit for bit;
+  * T calls with the state updated in place equal a T-step forward, bit for bit
+    (every y_t and the final state);
+and it matches the fp64 oracle within the bf16 path's 3e-2.  A CUDA graph of
+several decode steps replays to the same bits as the eager calls.
+"""
+import numpy as np
+import pytest
+import torch
+
+import __graft_entry__
+import matrix_state_nonlinear_gb300 as pkg
+from matrix_state_nonlinear_gb300 import m2rnn as binding
+from matrix_state_nonlinear_gb300.inputs import Workload, all_f64, make_inputs
+from oracle import m2rnn_forward_inputs
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    __graft_entry__.build()
+    pkg.load_library()
+
+
+def step_args(inp, t):
+    return (inp["q"][:, t].contiguous(), inp["k"][:, t].contiguous(), inp["v"][:, t].contiguous(),
+            inp["a"][:, t].contiguous(), inp["alpha"], inp["beta"], inp["W"], inp["w_r"])
+
+
+@pytest.mark.parametrize("shape,shared", [((2, 37, 3, 64, 64), False), ((3, 20, 2, 32, 16), False),
+                                          ((2, 9, 4, 48, 32), True), ((1, 70, 2, 16, 64), False)])
+def test_decode_steps_reproduce_the_forward_bitwise(shape, shared):
+    B, T, N, K, V = shape
+    inp = make_inputs(Workload("dec", B, T, N, K, V, h0="uniform", shared_qk=shared), DEV, 5)
+    y_ref, H_ref = pkg.m2rnn_forward(inp)
+    H = inp["H0"].clone()
+    for t in range(T):
+        y, _ = pkg.m2rnn_decode_step(*step_args(inp, t), H)   # in place
+        assert torch.equal(y, y_ref[:, t]), t
+    assert pkg.stream_status() == binding.OK
+    assert torch.equal(H, H_ref)
+
+
+@pytest.mark.parametrize("shape", [(2, 5, 3, 128, 64), (4, 3, 2, 112, 16)])
+def test_decode_large_K_matches_oracle(shape):
+    B, T, N, K, V = shape
+    inp = make_inputs(Workload("decK", B, T, N, K, V, h0="uniform"), DEV, 6)
+    H = inp["H0"].clone()
+    ys = []
+    for t in range(T):
+        y, _ = pkg.m2rnn_decode_step(*step_args(inp, t), H)
+        ys.append(y.clone())
+    yo, Ho = m2rnn_forward_inputs(all_f64(inp))
+    err_y = float(np.abs(torch.stack(ys, 1).double().cpu().numpy() - yo).max())
+    err_h = float(np.abs(H.double().cpu().numpy() - Ho).max())
+    assert err_y <= 3e-2 and err_h <= 3e-2, (err_y, err_h)
+
+
+def test_decode_zero_state_and_separate_output():
+    inp = make_inputs(Workload("dec0", 3, 1, 2, 64, 64, h0="zero"), DEV, 7)
+    y_ref, H_ref = pkg.m2rnn_forward(inp)
+    H_out = torch.full((3, 2, 64, 64), float("nan"), device=DEV)
+    y, _ = pkg.m2rnn_decode_step(*step_args(inp, 0), None, H_out=H_out)
+    assert torch.equal(y, y_ref[:, 0]) and torch.equal(H_out, H_ref)
+
+
+def test_decode_cuda_graph_replay():
+    B, T, N, K, V = 4, 8, 4, 64, 64
+    inp = make_inputs(Workload("decg", B, T, N, K, V, h0="uniform"), DEV, 8)
+    steps = [step_args(inp, t) for t in range(T)]
+    H_eager = inp["H0"].clone()
+    ys_eager = [pkg.m2rnn_decode_step(*steps[t], H_eager)[0].clone() for t in range(T)]
+    H = inp["H0"].clone()
+    ys = [torch.empty((B, N, V), device=DEV) for _ in range(T)]
+    pkg.m2rnn_decode_step(*steps[0], H.clone(), y=ys[0])       # first call outside capture
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            for t in range(T):
+                pkg.m2rnn_decode_step(*steps[t], H, y=ys[t], stream=s)
+    H.copy_(inp["H0"])
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(H, H_eager)
+    for t in range(T):
+        assert torch.equal(ys[t], ys_eager[t]), t
