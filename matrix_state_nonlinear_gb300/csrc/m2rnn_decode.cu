@@ -28,15 +28,17 @@ namespace {
 
 constexpr int kMaxWarps = 8;  // K <= 128
 
-template <int VT>
-__global__ void __launch_bounds__(32 * kMaxWarps)
+// MAXW: the most warps a launch uses (K / 16 <= MAXW).  Four-warp launches (K <= 64)
+// are register-capped so that six blocks fit on an SM: more state loads in flight.
+template <int VT, int MAXW>
+__global__ void __launch_bounds__(32 * MAXW, MAXW <= 4 ? 6 : 1)
     decode_bf16_mma(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
                     const uint16_t* __restrict__ v, const uint16_t* __restrict__ a,
                     const float* __restrict__ alpha, const float* __restrict__ beta,
                     const uint16_t* __restrict__ W, const float* __restrict__ w_r,
                     const float* H_in, float* H_out, float* __restrict__ y, int N, int Nqk, int K) {
   constexpr int V = 16 * VT, NT = 2 * VT, M = 4 * VT;
-  __shared__ __align__(16) float ypart[kMaxWarps][V];
+  __shared__ __align__(16) float ypart[MAXW][V];
   const int nw = K / 16;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int pair = blockIdx.x, b = pair / N, n = pair - (pair / N) * N;
@@ -66,19 +68,7 @@ __global__ void __launch_bounds__(32 * kMaxWarps)
                    : make_float2(0.f, 0.f);
   }
   __syncthreads();
-  uint32_t wb[VT][NT][2];
   const int lr = lane & 7, lq = lane >> 3;
-#pragma unroll
-  for (int kt = 0; kt < VT; ++kt)
-#pragma unroll
-    for (int np = 0; np < NT / 2; ++np) {  // b0, b1 of n-tiles 2 np and 2 np + 1
-      uint32_t r4[4];
-      ldmatrix_x4_trans(r4, wsm + (16 * kt + lr + 8 * (lq & 1)) * WS + 16 * np + 8 * (lq >> 1));
-      wb[kt][2 * np][0] = r4[0];
-      wb[kt][2 * np][1] = r4[1];
-      wb[kt][2 * np + 1][0] = r4[2];
-      wb[kt][2 * np + 1][1] = r4[3];
-    }
   const float2 fg = gate_fg(bf16_bits_to_float(a[row]), alpha[n], beta[n]);
   const float2 ff = make_float2(fg.x, fg.x), gg = make_float2(fg.y, fg.y);
 
@@ -104,7 +94,12 @@ __global__ void __launch_bounds__(32 * kMaxWarps)
     af[2] = pack_bf16x2(h[2 * kt + 1][0].x, h[2 * kt + 1][0].y);
     af[3] = pack_bf16x2(h[2 * kt + 1][1].x, h[2 * kt + 1][1].y);
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) mma2(acc[nt], af, wb[kt][nt][0], wb[kt][nt][1]);
+    for (int np = 0; np < NT / 2; ++np) {  // B fragments of n-tiles 2 np, 2 np + 1
+      uint32_t wb[4];
+      ldmatrix_x4_trans(wb, wsm + (16 * kt + lr + 8 * (lq & 1)) * WS + 16 * np + 8 * (lq >> 1));
+      mma2(acc[2 * np], af, wb[0], wb[1]);
+      mma2(acc[2 * np + 1], af, wb[2], wb[3]);
+    }
   }
   // H' = f H + (1 - f) tanh(P)
 #pragma unroll
@@ -187,10 +182,11 @@ cudaError_t launch_decode_bf16(const Problem& p, cudaStream_t stream) {
                                        (const uint16_t*)p.W, p.w_r, p.H0, p.H_T, p.y, p.N, p.Nqk,
                                        p.K);
   };
+  const bool small = p.K <= 64;
   switch (p.V) {
-    case 16: args(decode_bf16_mma<1>); break;
-    case 32: args(decode_bf16_mma<2>); break;
-    case 64: args(decode_bf16_mma<4>); break;
+    case 16: small ? args(decode_bf16_mma<1, 4>) : args(decode_bf16_mma<1, kMaxWarps>); break;
+    case 32: small ? args(decode_bf16_mma<2, 4>) : args(decode_bf16_mma<2, kMaxWarps>); break;
+    case 64: small ? args(decode_bf16_mma<4, 4>) : args(decode_bf16_mma<4, kMaxWarps>); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
