@@ -48,9 +48,10 @@ def parse():
     ap.add_argument("--batch", type=int, default=None,
                     help="override B of the workload (smaller cases for profiling)")
     ap.add_argument("--pass", dest="which", default="forward",
-                    choices=["forward", "train", "decode"],
+                    choices=["forward", "train", "decode", "block"],
                     help="forward: the forward pass (default); train: the state-keeping "
-                         "forward plus the backward pass; decode: one-token decode steps")
+                         "forward plus the backward pass; decode: one-token decode steps; "
+                         "block: conv/SiLU prologue + forward + gate/RMSNorm epilogue")
     return ap.parse_args()
 
 
@@ -69,6 +70,8 @@ KERNEL_SOURCES = {
     "backward_mma_k64_v64": ["m2rnn_bwd_bf16_mma.cu"],
     "backward_simt": ["m2rnn_bwd_f32.cu"],
     "decode_bf16_mma": ["m2rnn_decode.cu"],
+    "conv_silu": ["m2rnn_block.cu"],
+    "gate_rmsnorm": ["m2rnn_block.cu"],
 }
 
 
@@ -639,6 +642,109 @@ def main_decode(args):
     return 0
 
 
+# ---------------------------------------------------------------- block (prologue + forward + epilogue)
+METRIC_BLOCK = ("M²RNN block recurrence path (conv/SiLU on q, k, v + forward + gate/RMSNorm) "
+                "tokens·heads/s")
+
+
+def main_block(args, wl):
+    """One step = m2rnn_conv_silu_bf16 on the q, k, v projections, the forward recurrence,
+    and m2rnn_gate_rmsnorm_bf16 on its readout (the GEMM projections are not included)."""
+    import torch
+
+    import __graft_entry__
+    import matrix_state_nonlinear_gb300 as pkg
+    from matrix_state_nonlinear_gb300.inputs import make_inputs
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    __graft_entry__.build()
+    pkg.load_library()
+    if wl.dtype != "bf16":
+        raise SystemExit("--pass block runs the bf16 path")
+    inp = make_inputs(wl, dev, seed=rank_seed(rank))
+    B, T, N, K, V = wl.B, wl.T, wl.N, wl.K, wl.V
+    Nqk = 1 if wl.shared_qk else N
+    g = torch.Generator(device=dev)
+    g.manual_seed(2000 + rank)
+    pre = {n: torch.randn((B, T, c), generator=g, device=dev).to(torch.bfloat16)
+           for n, c in (("q", Nqk * K), ("k", Nqk * K), ("v", N * V))}
+    cw = {n: 0.5 * torch.randn((x.shape[2], 4), generator=g, device=dev) for n, x in pre.items()}
+    gpre = torch.randn((B, T, N * V), generator=g, device=dev).to(torch.bfloat16)
+    wn = 1.0 + 0.1 * torch.randn(N * V, generator=g, device=dev)
+    run = dict(inp)
+    for n in ("q", "k", "v"):
+        run[n] = torch.empty_like(pre[n]).view(B, T, -1, K if n != "v" else V)
+    y = torch.empty((B, T, N, V), device=dev)
+    HT = torch.empty((B, N, K, V), device=dev)
+    out = torch.empty((B, T, N * V), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    marks = []
+
+    def step(record=False):
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(4)] if record else None
+        if record:
+            e[0].record(stream)
+        for n in ("q", "k", "v"):
+            pkg.conv_silu(pre[n], cw[n], out=run[n].view(B, T, -1), stream=stream)
+        if record:
+            e[1].record(stream)
+        pkg.m2rnn_forward(run, y=y, H_T=HT, stream=stream)
+        if record:
+            e[2].record(stream)
+        pkg.gate_rmsnorm(y.view(B, T, N * V), gpre, wn, 1e-6, out=out, stream=stream)
+        if record:
+            e[3].record(stream)
+            marks.append(e)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    if pkg.stream_status(stream) != 0:
+        raise RuntimeError("device status not OK after warm-up")
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize(dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step(record=True)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    if pkg.stream_status(stream) != 0:
+        raise RuntimeError("device status not OK after the timed steps")
+    ms = ev0.elapsed_time(ev1) / args.steps
+    pro_ms = statistics.mean(a.elapsed_time(b) for a, b, _, _ in marks)
+    fwd_ms = statistics.mean(b.elapsed_time(c) for _, b, c, _ in marks)
+    epi_ms = statistics.mean(c.elapsed_time(d) for _, _, c, d in marks)
+    peaks, peak_src = load_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    pro_bytes = sum(x.numel() for x in pre.values()) * 4          # bf16 in + bf16 out
+    epi_bytes = B * T * N * V * (4 + 2 + 2)                        # y f32, g bf16 in; out bf16
+    flops = 2.0 * K * V * V * wl.units
+    peak_t = float(peaks["bf16_tflops"])
+    roof = {"bound": "tensor", "achieved": flops / (fwd_ms / 1e3) / 1e12, "peak": peak_t,
+            "unit": "TFLOP/s", "frac": flops / (fwd_ms / 1e3) / 1e12 / peak_t,
+            "peak_source": f"{peak_src} bf16 dense burst (kernel timed alone)",
+            "kernel": pkg.variant_name(pkg.pick_variant(B, T, N, K, V)),
+            "traffic": measured_traffic(pkg.variant_name(pkg.pick_variant(B, T, N, K, V)), wl),
+            "forward_ms": fwd_ms, "prologue_ms": pro_ms, "epilogue_ms": epi_ms,
+            "prologue_hbm_frac": pro_bytes / (pro_ms / 1e3) / 1e9 / hbm,
+            "epilogue_hbm_frac": epi_bytes / (epi_ms / 1e3) / 1e9 / hbm,
+            "prologue_bytes": pro_bytes, "epilogue_bytes": epi_bytes,
+            "hbm_peak_gbs": hbm}
+    line = {"metric": METRIC_BLOCK, "value": wl.units / (ms / 1e3), "unit": UNIT, "n_gpus": 1,
+            "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "config": dict(workload_config(wl), **{"pass": "block"}),
+            "clocks": clk, "e2e": None, "gpu_launches": args.steps * 5, "roofline": roof,
+            "cpu_baseline": None}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 # ---------------------------------------------------------------- GPU arm
 def main():
     args = parse()
@@ -652,6 +758,8 @@ def main():
         return reference_arm(args, wl)
     if args.which == "train":
         return main_train(args, wl)
+    if args.which == "block":
+        return main_block(args, wl)
 
     import torch
     import torch.distributed as dist

@@ -238,6 +238,31 @@ m2rnn_status m2rnn_decode_step_bf16(const uint16_t* q, const uint16_t* k, const 
                                     float* H_out, float* y, int B, int N, int Nqk, int K, int V,
                                     void* stream);
 
+/*
+ * The block's elementwise stages around the recurrence (the notes' Sec. 2.3,
+ * Eq. (14)-(23); the projections W_q, W_k, W_v, W_g, W_f, W_o are plain GEMMs outside).
+ *
+ * m2rnn_conv_silu_bf16: prologue of q, k and v (call once per tensor).
+ *   out[b,t,c] = SiLU(bias[c] + sum_{j=0..3} w[c][j] * x[b, t-3+j, c]),  x[b, t<0, c] = 0
+ *   x, out [B, T, C] bf16 (16-byte aligned, C % 8 == 0, else UNSUPPORTED; out must not
+ *   overlap x); w [C, 4] float32 (16-byte aligned); bias [C] float32 or NULL (none).
+ *   Its output, viewed as [B, T, N, K] or [B, T, N, V], is the recurrence's q, k or v.
+ *
+ * m2rnn_gate_rmsnorm_bf16: epilogue.  For each of `rows` rows of D values (a token's
+ *   readout over all heads, D = N V, the recurrence's y viewed as [B T, D]):
+ *   z = y ⊙ SiLU(g_pre),  out = w_norm ⊙ z / sqrt(mean(z^2) + eps)
+ *   (output gate first, then RMSNorm over the whole token).  y float32, g_pre and out
+ *   bf16, w_norm [D] float32, eps >= 0; all 16-byte aligned; D % 8 == 0 (else
+ *   UNSUPPORTED).  out is ready to be the W_o GEMM's operand.
+ * Both: fp32 arithmetic, results rounded to bf16 (nearest even); memory-bound, every
+ * element read and written once.
+ */
+m2rnn_status m2rnn_conv_silu_bf16(const uint16_t* x, const float* w, const float* bias,
+                                  uint16_t* out, int B, int T, int C, void* stream);
+m2rnn_status m2rnn_gate_rmsnorm_bf16(const float* y, const uint16_t* g_pre, const float* w_norm,
+                                     float eps, uint16_t* out, long long rows, int D,
+                                     void* stream);
+
 /* Name of a bf16 kernel variant (NULL for an unknown id).  Id 0 is "auto". */
 const char* m2rnn_variant_name(int variant);
 

@@ -340,6 +340,35 @@ m2rnn_status m2rnn_decode_step_bf16(const uint16_t* q, const uint16_t* k, const 
              : M2RNN_ERR_CUDA;
 }
 
+m2rnn_status m2rnn_conv_silu_bf16(const uint16_t* x, const float* w, const float* bias,
+                                  uint16_t* out, int B, int T, int C, void* stream) {
+  if (B < 1 || T < 0 || C < 1) return M2RNN_ERR_INVALID_ARG;
+  if (T > 0 && (!x || !w || !out)) return M2RNN_ERR_INVALID_ARG;
+  if (C % 8 != 0) return M2RNN_ERR_UNSUPPORTED;
+  if (!aligned(x, 16) || !aligned(out, 16) || !aligned(w, 16) || !aligned(bias, 4))
+    return M2RNN_ERR_INVALID_ARG;
+  if (T == 0) return M2RNN_OK;
+  return launch_conv_silu(x, w, bias, out, B, T, C, static_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? M2RNN_OK
+             : M2RNN_ERR_CUDA;
+}
+
+m2rnn_status m2rnn_gate_rmsnorm_bf16(const float* y, const uint16_t* g_pre, const float* w_norm,
+                                     float eps, uint16_t* out, long long rows, int D,
+                                     void* stream) {
+  if (rows < 0 || D < 1 || !(eps >= 0.f)) return M2RNN_ERR_INVALID_ARG;
+  if (rows > 0 && (!y || !g_pre || !w_norm || !out)) return M2RNN_ERR_INVALID_ARG;
+  if (D % 8 != 0) return M2RNN_ERR_UNSUPPORTED;
+  if (!aligned(y, 16) || !aligned(g_pre, 16) || !aligned(w_norm, 16) || !aligned(out, 16))
+    return M2RNN_ERR_INVALID_ARG;
+  if (rows == 0) return M2RNN_OK;
+  return launch_gate_rmsnorm(y, g_pre, w_norm, eps, out, rows, D,
+                             static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? M2RNN_OK
+             : M2RNN_ERR_CUDA;
+}
+
 m2rnn_status m2rnn_stream_status(void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return M2RNN_ERR_CUDA;

@@ -126,4 +126,13 @@ cudaError_t launch_bwd_bf16_mma(const BackwardProblem& p, EncodeTiledFn enc, int
 bool decode_supports(int K, int V);
 cudaError_t launch_decode_bf16(const Problem& p, cudaStream_t stream);
 
+// Block prologue / epilogue (memory-bound): causal depthwise Conv1D (kernel 4) + SiLU
+// over [B, T, C] bf16 (C % 8 == 0), and the output gate + RMSNorm over rows of D
+// (D % 8 == 0) values.
+cudaError_t launch_conv_silu(const uint16_t* x, const float* w, const float* bias, uint16_t* out,
+                             int B, int T, int C, cudaStream_t stream);
+cudaError_t launch_gate_rmsnorm(const float* y, const uint16_t* g_pre, const float* w_norm,
+                                float eps, uint16_t* out, long long rows, int D,
+                                cudaStream_t stream);
+
 }  // namespace m2rnn

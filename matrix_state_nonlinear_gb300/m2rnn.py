@@ -39,6 +39,8 @@ SYMBOLS = {
     "m2rnn_backward_bf16": (_I, [_P] * 21 + [_I] * 7 + [_P, ctypes.c_size_t, _P]),
     "m2rnn_backward_bf16_noalloc": (_I, [_P] * 21 + [_I] * 6 + [_P]),
     "m2rnn_decode_step_bf16": (_I, [_P] * 11 + [_I] * 5 + [_P]),
+    "m2rnn_conv_silu_bf16": (_I, [_P] * 4 + [_I] * 3 + [_P]),
+    "m2rnn_gate_rmsnorm_bf16": (_I, [_P] * 3 + [ctypes.c_float, _P, ctypes.c_longlong, _I, _P]),
 }
 
 _lib = None
@@ -348,3 +350,47 @@ def m2rnn_decode_step(q, k, v, a, alpha, beta, W, w_r, H_in, H_out=None, y=None,
     if st != OK:
         raise M2RNNError(st, "m2rnn_decode_step_bf16")
     return y, H_out
+
+
+# ---------------------------------------------------------------- block prologue / epilogue
+def conv_silu(x, w, bias=None, out=None, stream=None):
+    """SiLU(causal depthwise Conv1D, kernel 4) over time: x [B, T, C] bf16, w [C, 4] float32,
+    bias [C] float32 or None.  Returns out [B, T, C] bf16."""
+    lib = load_library()
+    if x.device.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    B, T, C = x.shape
+    dev = x.device
+    _check(x, "x", torch.bfloat16, (B, T, C), dev)
+    _check(w, "w", torch.float32, (C, 4), dev)
+    _check(bias, "bias", torch.float32, (C,), dev)
+    if out is None:
+        out = torch.empty_like(x)
+    _check(out, "out", torch.bfloat16, (B, T, C), dev)
+    st = lib.m2rnn_conv_silu_bf16(_ptr(x), _ptr(w), _ptr(bias), _ptr(out), B, T, C,
+                                  ctypes.c_void_p(_stream_ptr(stream)))
+    if st != OK:
+        raise M2RNNError(st, "m2rnn_conv_silu_bf16")
+    return out
+
+
+def gate_rmsnorm(y, g_pre, w_norm, eps=1e-6, out=None, stream=None):
+    """RMSNorm(y ⊙ SiLU(g_pre)) over the last axis: y [..., D] float32, g_pre [..., D] bf16,
+    w_norm [D] float32.  Returns out [..., D] bf16."""
+    lib = load_library()
+    if y.device.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    D = y.shape[-1]
+    rows = y.numel() // D if D else 0
+    dev = y.device
+    _check(y, "y", torch.float32, tuple(y.shape), dev)
+    _check(g_pre, "g_pre", torch.bfloat16, tuple(y.shape), dev)
+    _check(w_norm, "w_norm", torch.float32, (D,), dev)
+    if out is None:
+        out = torch.empty(y.shape, dtype=torch.bfloat16, device=dev)
+    _check(out, "out", torch.bfloat16, tuple(y.shape), dev)
+    st = lib.m2rnn_gate_rmsnorm_bf16(_ptr(y), _ptr(g_pre), _ptr(w_norm), float(eps), _ptr(out),
+                                     rows, D, ctypes.c_void_p(_stream_ptr(stream)))
+    if st != OK:
+        raise M2RNNError(st, "m2rnn_gate_rmsnorm_bf16")
+    return out

@@ -188,3 +188,14 @@ def test_decode_argument_checks(lib):
     assert lib.m2rnn_decode_step_bf16(*p, 2, 3, 3, 24, 64, None) == binding.ERR_UNSUPPORTED
     assert lib.m2rnn_decode_step_bf16(*p, 2, 3, 3, 64, 128, None) == binding.ERR_UNSUPPORTED
     assert lib.m2rnn_decode_step_bf16(*p, 2, 3, 2, 64, 64, None) == binding.ERR_INVALID_ARG
+
+
+def test_block_argument_checks(lib):
+    p = fake_ptrs(4)
+    assert lib.m2rnn_conv_silu_bf16(*p, 2, 5, 12, None) == binding.ERR_UNSUPPORTED      # C % 8
+    assert lib.m2rnn_conv_silu_bf16(None, p[1], None, p[3], 2, 5, 16, None) == binding.ERR_INVALID_ARG
+    assert lib.m2rnn_conv_silu_bf16(*p, 2, 0, 16, None) == binding.OK                  # T = 0: nothing
+    q = fake_ptrs(4)
+    assert lib.m2rnn_gate_rmsnorm_bf16(q[0], q[1], q[2], 1e-6, q[3], 4, 12, None) == binding.ERR_UNSUPPORTED
+    assert lib.m2rnn_gate_rmsnorm_bf16(q[0], q[1], q[2], -1.0, q[3], 4, 16, None) == binding.ERR_INVALID_ARG
+    assert lib.m2rnn_gate_rmsnorm_bf16(q[0], None, q[2], 1e-6, q[3], 4, 16, None) == binding.ERR_INVALID_ARG
