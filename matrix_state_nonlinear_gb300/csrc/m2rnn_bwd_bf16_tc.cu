@@ -1,0 +1,652 @@
+// m2rnn_bwd_bf16_tc.cu — backward pass of the M²RNN recurrence, K = V = 64, with the two
+// products that are off the serial chain on the 5th-generation tensor cores.
+//
+// Same reverse scan as m2rnn_bwd_bf16_mma.cu (the M²RNN study notes, Sec. 2.7; gate of
+// Eq. (13)/(17)), same kept bf16 states.  The work of one step splits by dependency:
+//   * H_{t-1} W (recomputing P_t) only needs the kept state: one thread issues it as
+//     four tcgen05.mma (M = N = 64, K = 16) into one of four tensor-memory slots, up to
+//     three steps ahead of the scan;
+//   * H_{t-1}^T D_t (the dW sum) needs D_t: the same thread issues it into one tensor-
+//     memory accumulator that sums every step of the sequence (read once at the end);
+//   * the chain C_t -> R_t -> D_t -> C_{t-1} = f R_t + D_t W^T stays with four compute
+//     warps (16 rows each, C and W^T in registers, D_t W^T on the warp-level MMA), which
+//     also form dq, dk, dv and dL/df.
+// Operands in shared memory use the 128-byte swizzle: the TMA-loaded state tiles
+// (K-major for H_{t-1} W, read M-major for H_{t-1}^T D_t), W^T (K-major) and D_t^T,
+// which the compute warps write with stmatrix.trans.  Each chunk's TMA box covers the
+// states t0 - 1 .. t0 + Tc - 1, so every read of a step stays inside its own stage.
+//
+// Roles: warps 0-3 compute, warp 4 producer (TMA, gates, per-chunk dv / da / dalpha /
+// dbeta / dw_r), warp 5 tensor-core issuer (one thread).  mbarriers: full (TMA),
+// done (compute warps finished a chunk), mmadone (the chunk's MMAs finished), pready /
+// pfree (P slots), dtready / dtfree (D^T slots).  Every wait is bounded.
+#include <cuda_bf16.h>
+
+#include "m2rnn_internal.h"
+#include "ptx_util.cuh"
+
+namespace m2rnn {
+namespace {
+
+constexpr int kK = 64, kV = 64;
+constexpr int kNW = 4;                   // compute warps
+constexpr int kNT = kV / 8, kVT = kV / 16;
+constexpr int kTc = 4;                   // steps per chunk
+constexpr int kS = 4;                    // P slots in tensor memory (issue up to kS - 1 ahead)
+constexpr int kThreads = 32 * (kNW + 2);
+constexpr int kProducer = kNW, kIssuer = kNW + 1;
+constexpr int kTile = kK * kV * 2;       // one bf16 64 x 64 tile (64 rows of 128 bytes)
+constexpr int kStageTiles = kTc + 1;     // states t0 - 1 .. t0 + Tc - 1
+constexpr uint32_t kTmemCols = 512;      // P slots: columns 0 .. 255; dW: 256 .. 319
+constexpr uint32_t kDwCol = 256;
+
+struct TcLayout {
+  int hs, h0t, wt, dt, in, in_stage, qs, ks, vs, dys, gates, dfp, dvp, bar, total;
+};
+
+__host__ __device__ inline TcLayout tc_layout() {
+  TcLayout L;
+  int o = 0;
+  L.hs = o;
+  o += 2 * kStageTiles * kTile;
+  L.h0t = o;
+  o += kTile;
+  L.wt = o;
+  o += kTile;
+  L.dt = o;
+  o += 2 * kTile;
+  L.qs = 0;
+  L.ks = kTc * kK * 2;
+  L.vs = L.ks + kTc * kK * 2;
+  L.dys = L.vs + kTc * kV * 2;
+  L.in_stage = (L.dys + kTc * kV * 4 + 127) & ~127;
+  L.in = o;
+  o += 2 * L.in_stage;
+  L.gates = o;
+  o += 2 * kTc * 16;
+  L.dfp = o;
+  o += 2 * kNW * kTc * 4;
+  L.dvp = o;
+  o += 2 * kNW * kTc * kV * 4;
+  L.bar = o;
+  o += 256;
+  L.total = o + 1024;
+  return L;
+}
+
+// Barrier block: full[2] done[2] mmadone[2] pready[kS] pfree[kS] dtready[2] dtfree[2] never
+struct Bars {
+  uint64_t* full;
+  uint64_t* done;
+  uint64_t* mmadone;
+  uint64_t* pready;
+  uint64_t* pfree;
+  uint64_t* dtready;
+  uint64_t* dtfree;
+  uint64_t* never;
+  volatile int* abort_flag;
+  uint32_t* tmem_slot;
+};
+
+__device__ inline Bars bars_at(uint8_t* p) {
+  Bars B;
+  uint64_t* b = reinterpret_cast<uint64_t*>(p);
+  B.full = b;
+  B.done = b + 2;
+  B.mmadone = b + 4;
+  B.pready = b + 6;
+  B.pfree = b + 6 + kS;
+  B.dtready = b + 6 + 2 * kS;
+  B.dtfree = b + 8 + 2 * kS;
+  B.never = b + 10 + 2 * kS;
+  B.abort_flag = reinterpret_cast<volatile int*>(b + 11 + 2 * kS);
+  B.tmem_slot = reinterpret_cast<uint32_t*>(b + 12 + 2 * kS);
+  return B;
+}
+
+// Walks the steps in processing order: chunks from last to first, steps within a chunk
+// from last to first.
+struct Cursor {
+  int p, s, steps, u;  // processed-chunk index, step in chunk, steps of the chunk, step count
+};
+__device__ inline int chunk_steps(int p, int nchunks, int T) {
+  const int t0 = (nchunks - 1 - p) * kTc;
+  return min(kTc, T - t0);
+}
+__device__ inline void cursor_next(Cursor& c, int nchunks, int T) {
+  ++c.u;
+  if (c.s > 0) {
+    --c.s;
+  } else {
+    ++c.p;
+    if (c.p < nchunks) {
+      c.steps = chunk_steps(c.p, nchunks, T);
+      c.s = c.steps - 1;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_bf16_tc(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_q,
+                const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                const __grid_constant__ CUtensorMap tm_dy, const uint16_t* __restrict__ a,
+                const float* __restrict__ alpha, const float* __restrict__ beta,
+                const uint16_t* __restrict__ W, const float* __restrict__ w_r,
+                const float* __restrict__ H0, const float* __restrict__ dH_T,
+                float* __restrict__ dq, float* __restrict__ dk, float* __restrict__ dv,
+                float* __restrict__ da, float* __restrict__ dH0, float* __restrict__ ws,
+                float* __restrict__ dqk_heads, int T, int N, int Nqk, int debug, int* status) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const TcLayout L = tc_layout();
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const uint32_t sbase = smem_u32(smem);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int pair = blockIdx.x, b = pair / N, n = pair - (pair / N) * N;
+  const int nchunks = (T + kTc - 1) / kTc;
+  const int nq = Nqk == 1 ? 0 : n;
+  const bool shared_qk = Nqk == 1 && N > 1;
+  const Bars Bs = bars_at(smem + L.bar);
+  float4* gates = reinterpret_cast<float4*>(smem + L.gates);
+  float* dfp = reinterpret_cast<float*>(smem + L.dfp);
+  float* dvp = reinterpret_cast<float*>(smem + L.dvp);
+  float* wsp = ws + (size_t)pair * backward_pair_floats(kK, kV);
+  float* dWp = wsp + kK * kV;
+  float* dwr_p = dWp + kV * kV;
+  float* ab_p = dwr_p + kV;
+  const long long limit = kWaitLimitCycles;
+
+  if (tid == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&Bs.full[i], 32);
+      mbar_init(&Bs.done[i], 32 * kNW);
+      mbar_init(&Bs.mmadone[i], 1);
+      mbar_init(&Bs.dtready[i], kNW);
+      mbar_init(&Bs.dtfree[i], 1);
+    }
+    for (int i = 0; i < kS; ++i) {
+      mbar_init(&Bs.pready[i], 1);
+      mbar_init(&Bs.pfree[i], kNW);
+    }
+    mbar_init(Bs.never, 1);
+    *Bs.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) tmem_alloc(Bs.tmem_slot, kTmemCols);
+  // W^T (K-major: row j holds W[0..63][j]) and bf16(H_0) into swizzled tiles.
+  const uint16_t* Wn = W + (size_t)n * kV * kV;
+  const float* h0p = H0 ? H0 + (size_t)pair * kK * kV : nullptr;
+  for (int e = tid; e < kV * 8; e += kThreads) {
+    const int row = e >> 3, ch = e & 7;
+    uint32_t wv[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      wv[i] = (uint32_t)Wn[(8 * ch + 2 * i) * kV + row] |
+              ((uint32_t)Wn[(8 * ch + 2 * i + 1) * kV + row] << 16);
+    *reinterpret_cast<uint4*>(smem + (sw128_addr(sbase + L.wt, row, ch) - sbase)) =
+        make_uint4(wv[0], wv[1], wv[2], wv[3]);
+    uint4 hv = make_uint4(0u, 0u, 0u, 0u);
+    if (h0p) {
+      const float4 x0 = *reinterpret_cast<const float4*>(h0p + row * kV + 8 * ch);
+      const float4 x1 = *reinterpret_cast<const float4*>(h0p + row * kV + 8 * ch + 4);
+      hv = make_uint4(pack_bf16x2(x0.x, x0.y), pack_bf16x2(x0.z, x0.w), pack_bf16x2(x1.x, x1.y),
+                      pack_bf16x2(x1.z, x1.w));
+    }
+    *reinterpret_cast<uint4*>(smem + (sw128_addr(sbase + L.h0t, row, ch) - sbase)) = hv;
+  }
+  fence_proxy_async_smem();  // the tiles are read by the tensor cores
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *Bs.tmem_slot;
+
+  // State tile of state t0 - 1 + i in chunk stage st, or the H_0 tile for t = 0.
+  auto hprev_tile = [&](int st, int s, int p) -> uint32_t {
+    const int t = (nchunks - 1 - p) * kTc + s;
+    return t == 0 ? sbase + L.h0t : sbase + L.hs + (st * kStageTiles + s) * kTile;
+  };
+
+  if (warp == kProducer) {
+    // ======================================================= producer warp
+    const float al = alpha[n], be = beta[n];
+    const uint32_t tx =
+        (uint32_t)(kStageTiles * kTile + 2 * kTc * kK * 2 + kTc * kV * 2 + kTc * kV * 4);
+    const float2 wr = *reinterpret_cast<const float2*>(w_r + (size_t)n * kV + 2 * lane);
+    auto arm = [&](int p) {
+      const int st = p & 1, t0 = (nchunks - 1 - p) * kTc;
+      if (lane < kTc) {
+        const int t = t0 + lane;
+        const float x = (t < T ? bf16_bits_to_float(a[((size_t)b * T + t) * N + n]) : 0.f) + be;
+        const float ex = expf(-fabsf(x));
+        const float sp = fmaxf(x, 0.f) + log1pf(ex);
+        const float sg = x >= 0.f ? 1.f / (1.f + ex) : ex / (1.f + ex);
+        gates[st * kTc + lane] = make_float4(expf(-al * sp), -expm1f(-al * sp), sg, sp);
+      }
+      __syncwarp();
+      if (lane != 0) {
+        mbar_arrive(&Bs.full[st]);
+      } else {
+        uint8_t* in = smem + L.in + st * L.in_stage;
+        mbar_arrive_expect_tx(&Bs.full[st], tx);
+        // states t0 - 1 .. t0 + Tc - 1 (t0 - 1 = -1 is zero-filled and not used)
+        tma_load_4d(smem + L.hs + st * kStageTiles * kTile, &tm_h, &Bs.full[st], 0, 0, t0 - 1,
+                    pair);
+        tma_load_4d(in + L.qs, &tm_q, &Bs.full[st], 0, nq, t0, b);
+        tma_load_4d(in + L.ks, &tm_k, &Bs.full[st], 0, nq, t0, b);
+        tma_load_4d(in + L.vs, &tm_v, &Bs.full[st], 0, n, t0, b);
+        tma_load_4d(in + L.dys, &tm_dy, &Bs.full[st], 0, n, t0, b);
+      }
+    };
+    if (lane == 0) {
+      prefetch_tensormap(&tm_h);
+      prefetch_tensormap(&tm_q);
+      prefetch_tensormap(&tm_k);
+      prefetch_tensormap(&tm_v);
+      prefetch_tensormap(&tm_dy);
+    }
+    int issued = 0;
+    for (; issued < 2 && issued < nchunks; ++issued) arm(issued);
+    float2 dwr = make_float2(0.f, 0.f);
+    float dal = 0.f, dbe = 0.f;
+    bool ok = true;
+    for (int p = 0; p < nchunks; ++p) {
+      const int st = p & 1, t0 = (nchunks - 1 - p) * kTc;
+      const int steps = min(kTc, T - t0);
+      const uint32_t par = (uint32_t)(p >> 1) & 1u;
+      ok = wait_or_abort(&Bs.done[st], par, limit, Bs.abort_flag);
+      ok = ok && wait_or_abort(&Bs.mmadone[st], par, limit, Bs.abort_flag);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      const uint8_t* in = smem + L.in + st * L.in_stage;
+      const float* dys = reinterpret_cast<const float*>(in + L.dys);
+      const uint16_t* vs = reinterpret_cast<const uint16_t*>(in + L.vs);
+      for (int s = 0; s < steps; ++s) {
+        const size_t row = ((size_t)b * T + t0 + s) * N + n;
+        const float2 u = *reinterpret_cast<const float2*>(dys + s * kV + 2 * lane);
+        float2 acc = make_float2(wr.x * u.x, wr.y * u.y);
+#pragma unroll
+        for (int w = 0; w < kNW; ++w) {
+          const float2 pw =
+              *reinterpret_cast<const float2*>(dvp + ((st * kNW + w) * kTc + s) * kV + 2 * lane);
+          acc.x += pw.x;
+          acc.y += pw.y;
+        }
+        *reinterpret_cast<float2*>(dv + row * kV + 2 * lane) = acc;
+        const uint32_t vv = *reinterpret_cast<const uint32_t*>(vs + s * kV + 2 * lane);
+        dwr.x = fmaf(u.x, bf16_lo(vv), dwr.x);
+        dwr.y = fmaf(u.y, bf16_hi(vv), dwr.y);
+      }
+      if (lane < steps) {
+        float df = 0.f;
+#pragma unroll
+        for (int w = 0; w < kNW; ++w) df += dfp[(st * kNW + w) * kTc + lane];
+        const float4 gt = gates[st * kTc + lane];
+        const float d_a = df * (-al * gt.x * gt.z);
+        da[((size_t)b * T + t0 + lane) * N + n] = d_a;
+        dal = fmaf(df, -gt.x * gt.w, dal);
+        dbe += d_a;
+      }
+      __syncwarp();
+      if (issued < nchunks) arm(issued++);
+    }
+    if (!ok) {
+      if (lane == 0) {
+        *Bs.abort_flag = 1;
+        atomicExch(status, kStatusTimeout);
+        for (int i = 0; i < 2; ++i)  // let copies in flight land
+          for (int ph = 0; ph < 2; ++ph)
+            mbar_wait_bounded(&Bs.full[i], (uint32_t)ph, kDebugWaitLimitCycles);
+      }
+    } else {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        dal += __shfl_xor_sync(0xffffffffu, dal, o);
+        dbe += __shfl_xor_sync(0xffffffffu, dbe, o);
+      }
+      *reinterpret_cast<float2*>(dwr_p + 2 * lane) = dwr;
+      if (lane == 0) {
+        ab_p[0] = dal;
+        ab_p[1] = dbe;
+      }
+    }
+  } else if (warp == kIssuer) {
+    // ======================================================= tensor-core issuer
+    if (lane == 0) {
+      const uint32_t idesc_p = umma_idesc_bf16(kK, kV, false);  // A = H (K-major), B = W^T
+      const uint32_t idesc_w = umma_idesc_bf16(kV, kV, true);   // A = H^T (M-major view)
+      const uint64_t d_wt = umma_desc(sbase + L.wt, 16, 1024, 2);
+      Cursor cp{0, chunk_steps(0, nchunks, T) - 1, chunk_steps(0, nchunks, T), 0};
+      Cursor cw = cp;
+      bool ok = true;
+      int full_seen = -1;  // chunks whose TMA completion was waited for
+      auto need_stage = [&](int p) {
+        if (p > full_seen) {
+          ok = ok && wait_or_abort(&Bs.full[p & 1], (uint32_t)(p >> 1) & 1u, limit, Bs.abort_flag);
+          full_seen = p;
+        }
+      };
+      while (ok && cw.u < T) {
+        while (ok && cp.u < T && cp.u < cw.u + kS) {  // P_t = H_{t-1} W into slot u % kS
+          need_stage(cp.p);
+          const int slot = cp.u % kS;
+          if (cp.u >= kS)
+            ok = ok && wait_or_abort(&Bs.pfree[slot], (uint32_t)((cp.u / kS) - 1) & 1u, limit,
+                                     Bs.abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          const uint64_t d_h = umma_desc(hprev_tile(cp.p & 1, cp.s, cp.p), 16, 1024, 2);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            umma_bf16(tmem + (uint32_t)(64 * slot), d_h + (uint64_t)((kk * 32) >> 4),
+                      d_wt + (uint64_t)((kk * 32) >> 4), idesc_p, kk);
+          umma_commit(&Bs.pready[slot]);
+          cursor_next(cp, nchunks, T);
+        }
+        if (!ok) break;
+        // dW += H_{t-1}^T D_t once the compute warps have written D_t^T.
+        ok = wait_or_abort(&Bs.dtready[cw.u & 1], (uint32_t)(cw.u >> 1) & 1u, limit,
+                           Bs.abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+        const uint64_t d_ht = umma_desc(hprev_tile(cw.p & 1, cw.s, cw.p), kTile, 1024, 2);
+        const uint64_t d_dt = umma_desc(sbase + L.dt + (cw.u & 1) * kTile, 16, 1024, 2);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          umma_bf16(tmem + kDwCol, d_ht + (uint64_t)((kk * 2048) >> 4),
+                    d_dt + (uint64_t)((kk * 32) >> 4), idesc_w, (cw.u > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&Bs.dtfree[cw.u & 1]);
+        if (cw.s == 0) umma_commit(&Bs.mmadone[cw.p & 1]);  // the chunk's stage may be reused
+        cursor_next(cw, nchunks, T);
+      }
+      if (!ok) {
+        *Bs.abort_flag = 1;
+        atomicExch(status, kStatusTimeout);
+      }
+      // Before the tensor memory is released every issued MMA must have finished: a
+      // commit completes when all earlier MMAs of this thread have, so wait for the last
+      // commit of each kind (bounded).
+      if (cp.u > 0)
+        mbar_wait_bounded(&Bs.pready[(cp.u - 1) % kS], (uint32_t)((cp.u - 1) / kS) & 1u, limit);
+      if (cw.u > 0)
+        mbar_wait_bounded(&Bs.dtfree[(cw.u - 1) & 1], (uint32_t)((cw.u - 1) >> 1) & 1u, limit);
+    }
+  } else {
+    // ======================================================= compute warps
+    const int g = lane >> 2, c = lane & 3;
+    const int r0 = 16 * warp + g, r1 = r0 + 8;
+    const int lr = lane & 7, lq = lane >> 3;
+    const uint32_t t_rows = tmem + ((uint32_t)(32 * warp) << 16);
+
+    uint32_t wtb[kVT][kNT][2];  // W^T as B fragments of C += D W^T
+#pragma unroll
+    for (int kj = 0; kj < kVT; ++kj)
+#pragma unroll
+      for (int nl = 0; nl < kNT; ++nl) {
+        const uint16_t* wrow = Wn + (8 * nl + g) * kV + 16 * kj + 2 * c;
+        wtb[kj][nl][0] = *reinterpret_cast<const uint32_t*>(wrow);
+        wtb[kj][nl][1] = *reinterpret_cast<const uint32_t*>(wrow + 8);
+      }
+    float2 C[kNT][2];
+    const float* dhp = dH_T ? dH_T + (size_t)pair * kK * kV : nullptr;
+#pragma unroll
+    for (int nt = 0; nt < kNT; ++nt) {
+      C[nt][0] = dhp ? *reinterpret_cast<const float2*>(dhp + r0 * kV + 8 * nt + 2 * c)
+                     : make_float2(0.f, 0.f);
+      C[nt][1] = dhp ? *reinterpret_cast<const float2*>(dhp + r1 * kV + 8 * nt + 2 * c)
+                     : make_float2(0.f, 0.f);
+    }
+    bool ok = true;
+    if (debug & kDebugForceTimeout) ok = mbar_wait_bounded(Bs.never, 0u, kDebugWaitLimitCycles);
+    int u = 0;
+    for (int p = 0; p < nchunks && ok; ++p) {
+      const int st = p & 1, t0 = (nchunks - 1 - p) * kTc;
+      const int steps = min(kTc, T - t0);
+      ok = wait_or_abort(&Bs.full[st], (uint32_t)(p >> 1) & 1u, limit, Bs.abort_flag);
+      const uint8_t* in = smem + L.in + st * L.in_stage;
+      const uint16_t* qs = reinterpret_cast<const uint16_t*>(in + L.qs);
+      const uint16_t* ks = reinterpret_cast<const uint16_t*>(in + L.ks);
+      const uint16_t* vs = reinterpret_cast<const uint16_t*>(in + L.vs);
+      const float* dys = reinterpret_cast<const float*>(in + L.dys);
+      for (int s = steps - 1; s >= 0 && ok; --s, ++u) {
+        const int t = t0 + s;
+        const uint32_t hprev = hprev_tile(st, s, p);
+        const uint32_t hcur = sbase + L.hs + (st * kStageTiles + s + 1) * kTile;
+        const float4 gt = gates[st * kTc + s];
+        const float2 ff = make_float2(gt.x, gt.x), gg = make_float2(gt.y, gt.y);
+
+        // ---- P_t from tensor memory (H_{t-1} W), then + k_t v_t^T
+        const int slot = u % kS;
+        ok = wait_or_abort(&Bs.pready[slot], (uint32_t)(u / kS) & 1u, limit, Bs.abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t pr[32];
+        tmem_ld_16x256b_x8(t_rows + (uint32_t)(64 * slot), pr);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&Bs.pfree[slot]);
+        float2 P[kNT][2];
+        {
+          const float kv0 = bf16_bits_to_float(ks[s * kK + r0]);
+          const float kv1 = bf16_bits_to_float(ks[s * kK + r1]);
+          const float2 k0 = make_float2(kv0, kv0), k1 = make_float2(kv1, kv1);
+#pragma unroll
+          for (int nt = 0; nt < kNT; ++nt) {
+            const float2 vv =
+                bf16x2_to_float2(*reinterpret_cast<const uint32_t*>(vs + s * kV + 8 * nt + 2 * c));
+            P[nt][0] = fma2(k0, vv, make_float2(__uint_as_float(pr[4 * nt]),
+                                                __uint_as_float(pr[4 * nt + 1])));
+            P[nt][1] = fma2(k1, vv, make_float2(__uint_as_float(pr[4 * nt + 2]),
+                                                __uint_as_float(pr[4 * nt + 3])));
+          }
+        }
+        // ---- Z, R, D (in place of P), dL/df partial, C <- f R
+        uint32_t ah[kVT][4];
+#pragma unroll
+        for (int kt = 0; kt < kVT; ++kt)
+          ldsm_x4(ah[kt], sw128_addr(hprev, 16 * warp + lr + 8 * (lq & 1), 2 * kt + (lq >> 1)));
+        const float qv0 = bf16_bits_to_float(qs[s * kK + r0]);
+        const float qv1 = bf16_bits_to_float(qs[s * kK + r1]);
+        const float2 q0 = make_float2(qv0, qv0), q1 = make_float2(qv1, qv1);
+        float2 dfl2 = make_float2(0.f, 0.f);
+        const float2 one = make_float2(1.f, 1.f);
+#pragma unroll
+        for (int nt = 0; nt < kNT; ++nt) {
+          const float2 uu = *reinterpret_cast<const float2*>(dys + s * kV + 8 * nt + 2 * c);
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            const float2 h = bf16x2_to_float2(ah[nt >> 1][2 * (nt & 1) + r]);
+            const float2 z = make_float2(tanh_mufu(P[nt][r].x), tanh_mufu(P[nt][r].y));
+            const float2 R = fma2(r ? q1 : q0, uu, C[nt][r]);
+            const float2 omz = fma2(make_float2(-z.x, -z.y), z, one);
+            P[nt][r] = mul2(mul2(gg, R), omz);                         // D_t
+            dfl2 = fma2(R, make_float2(h.x - z.x, h.y - z.y), dfl2);
+            C[nt][r] = mul2(ff, R);
+          }
+        }
+        // ---- dk_t, dv partial
+        float pdv[2 * kNT];
+        float2 sk0 = make_float2(0.f, 0.f), sk1 = make_float2(0.f, 0.f);
+        {
+          const float kv0 = bf16_bits_to_float(ks[s * kK + r0]);
+          const float kv1 = bf16_bits_to_float(ks[s * kK + r1]);
+          const float2 k0 = make_float2(kv0, kv0), k1 = make_float2(kv1, kv1);
+#pragma unroll
+          for (int nt = 0; nt < kNT; ++nt) {
+            const float2 vv =
+                bf16x2_to_float2(*reinterpret_cast<const uint32_t*>(vs + s * kV + 8 * nt + 2 * c));
+            sk0 = fma2(P[nt][0], vv, sk0);
+            sk1 = fma2(P[nt][1], vv, sk1);
+            const float2 pv = fma2(k1, P[nt][1], mul2(k0, P[nt][0]));
+            pdv[2 * nt] = pv.x;
+            pdv[2 * nt + 1] = pv.y;
+          }
+        }
+        // ---- D_t as bf16 A fragments: C += D W^T (the chain); D_t^T to shared memory
+        uint32_t ad[kVT][4];
+#pragma unroll
+        for (int kj = 0; kj < kVT; ++kj) {
+          ad[kj][0] = pack_bf16x2(P[2 * kj][0].x, P[2 * kj][0].y);
+          ad[kj][1] = pack_bf16x2(P[2 * kj][1].x, P[2 * kj][1].y);
+          ad[kj][2] = pack_bf16x2(P[2 * kj + 1][0].x, P[2 * kj + 1][0].y);
+          ad[kj][3] = pack_bf16x2(P[2 * kj + 1][1].x, P[2 * kj + 1][1].y);
+        }
+#pragma unroll
+        for (int kj = 0; kj < kVT; ++kj)
+#pragma unroll
+          for (int nl = 0; nl < kNT; ++nl) mma2(C[nl], ad[kj], wtb[kj][nl][0], wtb[kj][nl][1]);
+        if (u >= 2) {  // the dW product of step u - 2 has finished reading this slot
+          ok = wait_or_abort(&Bs.dtfree[u & 1], (uint32_t)((u >> 1) - 1) & 1u, limit,
+                             Bs.abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+        }
+        const uint32_t dts = sbase + L.dt + (u & 1) * kTile;
+#pragma unroll
+        for (int kj = 0; kj < kVT; ++kj)  // D^T rows j = 16 kj .., columns i = 16 warp ..
+          stsm_x4_trans(sw128_addr(dts, 16 * kj + lr + 8 * (lq >> 1), 2 * warp + (lq & 1)), ad[kj]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&Bs.dtready[u & 1]);
+
+        // ---- reductions: dk, dv partials, dL/df, dq = H_t u_t
+        float k0s = sk0.x + sk0.y, k1s = sk1.x + sk1.y;
+#pragma unroll
+        for (int o = 1; o <= 2; o <<= 1) {
+          k0s += __shfl_xor_sync(0xffffffffu, k0s, o);
+          k1s += __shfl_xor_sync(0xffffffffu, k1s, o);
+        }
+#pragma unroll
+        for (int stg = 0; stg < 3; ++stg) {
+          const int mask = 16 >> stg, half = kNT >> stg;
+          const bool up = (lane & mask) != 0;
+#pragma unroll
+          for (int i = 0; i < half; ++i) {
+            const float send = up ? pdv[i] : pdv[i + half];
+            const float keep = up ? pdv[i + half] : pdv[i];
+            pdv[i] = keep + __shfl_xor_sync(0xffffffffu, send, mask);
+          }
+        }
+        *reinterpret_cast<float2*>(dvp + ((st * kNW + warp) * kTc + s) * kV + 8 * g + 2 * c) =
+            make_float2(pdv[0], pdv[1]);
+        float dfl = dfl2.x + dfl2.y;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) dfl += __shfl_xor_sync(0xffffffffu, dfl, o);
+        if (lane == 0) dfp[(st * kNW + warp) * kTc + s] = dfl;
+        float2 sq0 = make_float2(0.f, 0.f), sq1 = make_float2(0.f, 0.f);
+        {
+          uint32_t hc[kVT][4];
+#pragma unroll
+          for (int kt = 0; kt < kVT; ++kt)
+            ldsm_x4(hc[kt], sw128_addr(hcur, 16 * warp + lr + 8 * (lq & 1), 2 * kt + (lq >> 1)));
+#pragma unroll
+          for (int nt = 0; nt < kNT; ++nt) {
+            const float2 uu = *reinterpret_cast<const float2*>(dys + s * kV + 8 * nt + 2 * c);
+            sq0 = fma2(bf16x2_to_float2(hc[nt >> 1][2 * (nt & 1)]), uu, sq0);
+            sq1 = fma2(bf16x2_to_float2(hc[nt >> 1][2 * (nt & 1) + 1]), uu, sq1);
+          }
+        }
+        float q0s = sq0.x + sq0.y, q1s = sq1.x + sq1.y;
+#pragma unroll
+        for (int o = 1; o <= 2; o <<= 1) {
+          q0s += __shfl_xor_sync(0xffffffffu, q0s, o);
+          q1s += __shfl_xor_sync(0xffffffffu, q1s, o);
+        }
+        if (c == 0) {
+          const size_t qrow = ((size_t)b * T + t) * (shared_qk ? N : Nqk) + (shared_qk ? n : nq);
+          float* dqo = shared_qk ? dqk_heads : dq;
+          float* dko = shared_qk ? dqk_heads + (size_t)gridDim.x * T * kK : dk;
+          dqo[qrow * kK + r0] = q0s;
+          dqo[qrow * kK + r1] = q1s;
+          dko[qrow * kK + r0] = k0s;
+          dko[qrow * kK + r1] = k1s;
+        }
+      }
+      if (!ok) break;
+      mbar_arrive(&Bs.done[st]);
+    }
+    if (ok) {  // the last dW product has finished: read this warp's 16 rows of dW
+      ok = wait_or_abort(&Bs.dtfree[(T - 1) & 1], (uint32_t)((T - 1) >> 1) & 1u, limit,
+                         Bs.abort_flag);
+      if (ok) {
+        tc_fence_after();
+        uint32_t wr[32];
+        tmem_ld_16x256b_x8(t_rows + kDwCol, wr);
+        tmem_wait_ld();
+#pragma unroll
+        for (int nt = 0; nt < kNT; ++nt) {
+          *reinterpret_cast<float2*>(dWp + r0 * kV + 8 * nt + 2 * c) =
+              make_float2(__uint_as_float(wr[4 * nt]), __uint_as_float(wr[4 * nt + 1]));
+          *reinterpret_cast<float2*>(dWp + r1 * kV + 8 * nt + 2 * c) =
+              make_float2(__uint_as_float(wr[4 * nt + 2]), __uint_as_float(wr[4 * nt + 3]));
+        }
+        if (dH0) {
+          float* hp = dH0 + (size_t)pair * kK * kV;
+#pragma unroll
+          for (int nt = 0; nt < kNT; ++nt) {
+            *reinterpret_cast<float2*>(hp + r0 * kV + 8 * nt + 2 * c) = C[nt][0];
+            *reinterpret_cast<float2*>(hp + r1 * kV + 8 * nt + 2 * c) = C[nt][1];
+          }
+        }
+      }
+    }
+    if (!ok) {
+      *Bs.abort_flag = 1;
+      if (lane == 0) atomicExch(status, kStatusTimeout);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+}
+
+bool make_map(EncodeTiledFn enc, CUtensorMap* map, CUtensorMapDataType dt, const void* base,
+              int esize, const cuuint64_t (&dims)[4], const cuuint32_t (&box)[4],
+              CUtensorMapSwizzle swz) {
+  const cuuint64_t strides[3] = {dims[0] * esize, dims[0] * dims[1] * esize,
+                                 dims[0] * dims[1] * dims[2] * esize};
+  const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  return enc(map, dt, 4, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_bf16_tc(const BackwardProblem& p, EncodeTiledFn enc, int debug, int* status,
+                               cudaStream_t stream) {
+  const TcLayout L = tc_layout();
+  const cuuint64_t B = (cuuint64_t)p.B, T = (cuuint64_t)p.T, N = (cuuint64_t)p.N;
+  CUtensorMap mh, mq, mk, mv, mdy;
+  const cuuint64_t dh[4] = {kV, kK, T, B * N};
+  const cuuint32_t bh[4] = {kV, kK, kStageTiles, 1};
+  const cuuint64_t dqk[4] = {kK, (cuuint64_t)p.Nqk, T, B};
+  const cuuint32_t bqk[4] = {kK, 1, kTc, 1};
+  const cuuint64_t dvv[4] = {kV, N, T, B};
+  const cuuint32_t bvv[4] = {kV, 1, kTc, 1};
+  if (!make_map(enc, &mh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.Hs, 2, dh, bh,
+                CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map(enc, &mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.q, 2, dqk, bqk,
+                CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !make_map(enc, &mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.k, 2, dqk, bqk,
+                CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !make_map(enc, &mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.v, 2, dvv, bvv,
+                CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !make_map(enc, &mdy, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.dy, 4, dvv, bvv,
+                CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
+  cudaError_t err =
+      cudaFuncSetAttribute(bwd_bf16_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
+  if (err != cudaSuccess) return err;
+  float* heads = p.ws + (size_t)p.B * p.N * backward_pair_floats(kK, kV);
+  bwd_bf16_tc<<<(unsigned)(p.B * p.N), kThreads, L.total, stream>>>(
+      mh, mq, mk, mv, mdy, (const uint16_t*)p.a, p.alpha, p.beta, (const uint16_t*)p.W, p.w_r,
+      p.H0, p.dH_T, p.dq, p.dk, p.dv, p.da, p.dH0, p.ws, heads, p.T, p.N, p.Nqk, debug, status);
+  err = cudaGetLastError();
+  return err == cudaSuccess ? launch_bwd_reduce(p, stream) : err;
+}
+
+}  // namespace m2rnn

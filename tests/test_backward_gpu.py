@@ -122,8 +122,8 @@ BF16_SHAPES = [(1, 1, 1, 16, 16), (2, 65, 3, 64, 64), (1, 130, 2, 32, 32), (2, 4
 
 
 def bwd_variants(K, V):
-    # 1: SIMT (any shape); 2: tensor-core kernel (K = V = 64)
-    return [1, 2] if (K, V) == (64, 64) else [1]
+    # 1: SIMT (any shape); 2: warp-MMA kernel, 3: tcgen05 kernel (K = V = 64)
+    return [1, 2, 3] if (K, V) == (64, 64) else [1]
 
 
 @pytest.mark.parametrize("shape", BF16_SHAPES)
@@ -134,40 +134,43 @@ def test_backward_bf16_matches_oracle(shape, h0):
         assert max(errs.values()) <= TOL["bf16"], (variant, errs)
 
 
-@pytest.mark.parametrize("variant", [1, 2])
+@pytest.mark.parametrize("variant", [1, 2, 3])
 def test_backward_bf16_shared_qk(variant):
     _, _, g, errs = run_case("bf16", 2, 50, 4, 64, 64, shared=True, variant=variant)
     assert g["dq"].shape[2] == 1
     assert max(errs.values()) <= TOL["bf16"], errs
 
 
-def test_backward_mma_without_dHT():
-    _, _, _, errs = run_case("bf16", 2, 37, 2, 64, 64, with_dHT=False, variant=2)
+@pytest.mark.parametrize("variant", [2, 3])
+def test_backward_mma_without_dHT(variant):
+    _, _, _, errs = run_case("bf16", 2, 37, 2, 64, 64, with_dHT=False, variant=variant)
     assert max(errs.values()) <= TOL["bf16"], errs
 
 
-def test_backward_mma_close_to_simt():
-    """Both kernels differentiate the same kept states; they differ only by rounding
+@pytest.mark.parametrize("variant", [2, 3])
+def test_backward_mma_close_to_simt(variant):
+    """The kernels differentiate the same kept states; they differ only by rounding
     (bf16 D in the MMA products vs fp32 SIMT sums)."""
     wl = Workload("cmp", 2, 90, 3, 64, 64, h0="uniform")
     inp = make_inputs(wl, DEV, 8)
     _, _, Hs = pkg.m2rnn_forward_train(inp)
     dy, dHT = upstream(2, 90, 3, 64, 64, 9)
     g1 = pkg.m2rnn_backward(inp, Hs, dy, dHT, variant=1)
-    g2 = pkg.m2rnn_backward(inp, Hs, dy, dHT, variant=2)
+    g2 = pkg.m2rnn_backward(inp, Hs, dy, dHT, variant=variant)
     for n in GRADS:
         assert rel_err(g2[n], g1[n].double().cpu().numpy()) <= 1e-2, n
 
 
-def test_backward_mma_forced_timeout_is_reported():
+@pytest.mark.parametrize("variant", [2, 3])
+def test_backward_mma_forced_timeout_is_reported(variant):
     wl = Workload("to", 2, 20, 2, 64, 64, h0="uniform")
     inp = make_inputs(wl, DEV, 3)
     _, _, Hs = pkg.m2rnn_forward_train(inp)
     dy, dHT = upstream(2, 20, 2, 64, 64, 4)
-    pkg.m2rnn_backward(inp, Hs, dy, dHT, variant=2 | (1 << 8))
+    pkg.m2rnn_backward(inp, Hs, dy, dHT, variant=variant | (1 << 8))
     assert pkg.stream_status() == binding.ERR_TIMEOUT
     assert pkg.stream_status() == binding.OK
-    g = pkg.m2rnn_backward(inp, Hs, dy, dHT, variant=2)     # the context still works
+    g = pkg.m2rnn_backward(inp, Hs, dy, dHT, variant=variant)   # the context still works
     ref = m2rnn_backward_inputs(all_f64(inp), dy.double().cpu().numpy(),
                                 dHT.double().cpu().numpy())
     assert max(rel_err(g[n], ref[n]) for n in GRADS) <= TOL["bf16"]
