@@ -29,26 +29,27 @@ namespace m2rnn {
 namespace {
 
 constexpr int kK = 64, kV = 64;
-constexpr int kNW = 4;                   // compute warps
+constexpr int kNW = 4;                   // row blocks of 16 rows
 constexpr int kNT = kV / 8, kVT = kV / 16;
-constexpr int kTc = 4;                   // steps per chunk
+constexpr int kTc = 8;                   // steps per chunk
+constexpr int kStages = 2;               // chunk stages in flight (TMA ring)
 constexpr int kS = 4;                    // P slots in tensor memory (issue up to kS - 1 ahead)
-constexpr int kThreads = 32 * (kNW + 2);
-constexpr int kProducer = kNW, kIssuer = kNW + 1;
 constexpr int kTile = kK * kV * 2;       // one bf16 64 x 64 tile (64 rows of 128 bytes)
 constexpr int kStageTiles = kTc + 1;     // states t0 - 1 .. t0 + Tc - 1
 constexpr uint32_t kTmemCols = 512;      // P slots: columns 0 .. 255; dW: 256 .. 319
 constexpr uint32_t kDwCol = 256;
 
 struct TcLayout {
-  int hs, h0t, wt, dt, in, in_stage, qs, ks, vs, dys, gates, dfp, dvp, bar, total;
+  int hs, h0t, wt, dt, in, in_stage, qs, ks, vs, dys, gates, dfp, dvp, dkqp, bar, total;
 };
 
+// kCW compute warps: 4 (one per 16-row block) or 8 (two per row block, one per 32-column half).
+template <int kCW>
 __host__ __device__ inline TcLayout tc_layout() {
   TcLayout L;
   int o = 0;
   L.hs = o;
-  o += 2 * kStageTiles * kTile;
+  o += kStages * kStageTiles * kTile;
   L.h0t = o;
   o += kTile;
   L.wt = o;
@@ -61,20 +62,22 @@ __host__ __device__ inline TcLayout tc_layout() {
   L.dys = L.vs + kTc * kV * 2;
   L.in_stage = (L.dys + kTc * kV * 4 + 127) & ~127;
   L.in = o;
-  o += 2 * L.in_stage;
+  o += kStages * L.in_stage;
   L.gates = o;
-  o += 2 * kTc * 16;
+  o += kStages * kTc * 16;
   L.dfp = o;
-  o += 2 * kNW * kTc * 4;
+  o += kStages * kCW * kTc * 4;
   L.dvp = o;
-  o += 2 * kNW * kTc * kV * 4;
+  o += kStages * kNW * kTc * kV * 4;
+  L.dkqp = o;                      // float [kStages][2 halves][dk, dq][kTc][kK] (kCW == 8)
+  o += kCW == 8 ? kStages * 2 * 2 * kTc * kK * 4 : 0;
   L.bar = o;
   o += 256;
   L.total = o + 1024;
   return L;
 }
 
-// Barrier block: full[2] done[2] mmadone[2] pready[kS] pfree[kS] dtready[2] dtfree[2] never
+// Barrier block: full, done, mmadone [kStages]; pready, pfree [kS]; dtready, dtfree [2]; never
 struct Bars {
   uint64_t* full;
   uint64_t* done;
@@ -92,17 +95,20 @@ __device__ inline Bars bars_at(uint8_t* p) {
   Bars B;
   uint64_t* b = reinterpret_cast<uint64_t*>(p);
   B.full = b;
-  B.done = b + 2;
-  B.mmadone = b + 4;
-  B.pready = b + 6;
-  B.pfree = b + 6 + kS;
-  B.dtready = b + 6 + 2 * kS;
-  B.dtfree = b + 8 + 2 * kS;
-  B.never = b + 10 + 2 * kS;
-  B.abort_flag = reinterpret_cast<volatile int*>(b + 11 + 2 * kS);
-  B.tmem_slot = reinterpret_cast<uint32_t*>(b + 12 + 2 * kS);
+  B.done = b + kStages;
+  B.mmadone = b + 2 * kStages;
+  B.pready = b + 3 * kStages;
+  B.pfree = B.pready + kS;
+  B.dtready = B.pfree + kS;
+  B.dtfree = B.dtready + 2;
+  B.never = B.dtfree + 2;
+  B.abort_flag = reinterpret_cast<volatile int*>(B.never + 1);
+  B.tmem_slot = reinterpret_cast<uint32_t*>(B.never + 2);
   return B;
 }
+
+__host__ __device__ constexpr int stage_of(int p) { return p % kStages; }
+__host__ __device__ constexpr uint32_t phase_of(int p) { return (uint32_t)(p / kStages) & 1u; }
 
 // Walks the steps in processing order: chunks from last to first, steps within a chunk
 // from last to first.
@@ -126,7 +132,8 @@ __device__ inline void cursor_next(Cursor& c, int nchunks, int T) {
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+template <int kCW>
+__global__ void __launch_bounds__(32 * (kCW + 2), 1)
     bwd_bf16_tc(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_q,
                 const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                 const __grid_constant__ CUtensorMap tm_dy, const uint16_t* __restrict__ a,
@@ -136,8 +143,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float* __restrict__ dq, float* __restrict__ dk, float* __restrict__ dv,
                 float* __restrict__ da, float* __restrict__ dH0, float* __restrict__ ws,
                 float* __restrict__ dqk_heads, int T, int N, int Nqk, int debug, int* status) {
+  constexpr int kThreads = 32 * (kCW + 2);
+  constexpr int kProducer = kCW, kIssuer = kCW + 1;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  const TcLayout L = tc_layout();
+  const TcLayout L = tc_layout<kCW>();
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -149,6 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   float4* gates = reinterpret_cast<float4*>(smem + L.gates);
   float* dfp = reinterpret_cast<float*>(smem + L.dfp);
   float* dvp = reinterpret_cast<float*>(smem + L.dvp);
+  float* dkqp = reinterpret_cast<float*>(smem + L.dkqp);
   float* wsp = ws + (size_t)pair * backward_pair_floats(kK, kV);
   float* dWp = wsp + kK * kV;
   float* dwr_p = dWp + kV * kV;
@@ -156,16 +166,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const long long limit = kWaitLimitCycles;
 
   if (tid == 0) {
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kStages; ++i) {
       mbar_init(&Bs.full[i], 32);
-      mbar_init(&Bs.done[i], 32 * kNW);
+      mbar_init(&Bs.done[i], 32 * kCW);
       mbar_init(&Bs.mmadone[i], 1);
-      mbar_init(&Bs.dtready[i], kNW);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&Bs.dtready[i], kCW);
       mbar_init(&Bs.dtfree[i], 1);
     }
     for (int i = 0; i < kS; ++i) {
       mbar_init(&Bs.pready[i], 1);
-      mbar_init(&Bs.pfree[i], kNW);
+      mbar_init(&Bs.pfree[i], kCW);
     }
     mbar_init(Bs.never, 1);
     *Bs.abort_flag = 0;
@@ -212,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         (uint32_t)(kStageTiles * kTile + 2 * kTc * kK * 2 + kTc * kV * 2 + kTc * kV * 4);
     const float2 wr = *reinterpret_cast<const float2*>(w_r + (size_t)n * kV + 2 * lane);
     auto arm = [&](int p) {
-      const int st = p & 1, t0 = (nchunks - 1 - p) * kTc;
+      const int st = stage_of(p), t0 = (nchunks - 1 - p) * kTc;
       if (lane < kTc) {
         const int t = t0 + lane;
         const float x = (t < T ? bf16_bits_to_float(a[((size_t)b * T + t) * N + n]) : 0.f) + be;
@@ -244,14 +256,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tensormap(&tm_dy);
     }
     int issued = 0;
-    for (; issued < 2 && issued < nchunks; ++issued) arm(issued);
+    for (; issued < kStages && issued < nchunks; ++issued) arm(issued);
     float2 dwr = make_float2(0.f, 0.f);
     float dal = 0.f, dbe = 0.f;
     bool ok = true;
     for (int p = 0; p < nchunks; ++p) {
-      const int st = p & 1, t0 = (nchunks - 1 - p) * kTc;
+      const int st = stage_of(p), t0 = (nchunks - 1 - p) * kTc;
       const int steps = min(kTc, T - t0);
-      const uint32_t par = (uint32_t)(p >> 1) & 1u;
+      const uint32_t par = phase_of(p);
       ok = wait_or_abort(&Bs.done[st], par, limit, Bs.abort_flag);
       ok = ok && wait_or_abort(&Bs.mmadone[st], par, limit, Bs.abort_flag);
       if (!__all_sync(0xffffffffu, ok)) {
@@ -277,10 +289,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         dwr.x = fmaf(u.x, bf16_lo(vv), dwr.x);
         dwr.y = fmaf(u.y, bf16_hi(vv), dwr.y);
       }
+      if constexpr (kCW == 8) {  // dk, dq: the two column halves' partial sums
+        for (int s = 0; s < steps; ++s) {
+          const size_t qrow = ((size_t)b * T + t0 + s) * (shared_qk ? N : Nqk) + (shared_qk ? n : nq);
+          float* dqo = shared_qk ? dqk_heads : dq;
+          float* dko = shared_qk ? dqk_heads + (size_t)gridDim.x * T * kK : dk;
+          const float* pk0 = dkqp + ((st * 2 + 0) * 2 * kTc + s) * kK;
+          const float* pk1 = dkqp + ((st * 2 + 1) * 2 * kTc + s) * kK;
+          const float* pq0 = pk0 + kTc * kK;
+          const float* pq1 = pk1 + kTc * kK;
+          const float2 k0v = *reinterpret_cast<const float2*>(pk0 + 2 * lane);
+          const float2 k1v = *reinterpret_cast<const float2*>(pk1 + 2 * lane);
+          const float2 q0v = *reinterpret_cast<const float2*>(pq0 + 2 * lane);
+          const float2 q1v = *reinterpret_cast<const float2*>(pq1 + 2 * lane);
+          *reinterpret_cast<float2*>(dko + qrow * kK + 2 * lane) =
+              make_float2(k0v.x + k1v.x, k0v.y + k1v.y);
+          *reinterpret_cast<float2*>(dqo + qrow * kK + 2 * lane) =
+              make_float2(q0v.x + q1v.x, q0v.y + q1v.y);
+        }
+      }
       if (lane < steps) {
         float df = 0.f;
 #pragma unroll
-        for (int w = 0; w < kNW; ++w) df += dfp[(st * kNW + w) * kTc + lane];
+        for (int w = 0; w < kCW; ++w) df += dfp[(st * kCW + w) * kTc + lane];
         const float4 gt = gates[st * kTc + lane];
         const float d_a = df * (-al * gt.x * gt.z);
         da[((size_t)b * T + t0 + lane) * N + n] = d_a;
@@ -294,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         *Bs.abort_flag = 1;
         atomicExch(status, kStatusTimeout);
-        for (int i = 0; i < 2; ++i)  // let copies in flight land
+        for (int i = 0; i < kStages; ++i)  // let copies in flight land
           for (int ph = 0; ph < 2; ++ph)
             mbar_wait_bounded(&Bs.full[i], (uint32_t)ph, kDebugWaitLimitCycles);
       }
@@ -322,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int full_seen = -1;  // chunks whose TMA completion was waited for
       auto need_stage = [&](int p) {
         if (p > full_seen) {
-          ok = ok && wait_or_abort(&Bs.full[p & 1], (uint32_t)(p >> 1) & 1u, limit, Bs.abort_flag);
+          ok = ok && wait_or_abort(&Bs.full[stage_of(p)], phase_of(p), limit, Bs.abort_flag);
           full_seen = p;
         }
       };
@@ -335,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                      Bs.abort_flag);
           if (!ok) break;
           tc_fence_after();
-          const uint64_t d_h = umma_desc(hprev_tile(cp.p & 1, cp.s, cp.p), 16, 1024, 2);
+          const uint64_t d_h = umma_desc(hprev_tile(stage_of(cp.p), cp.s, cp.p), 16, 1024, 2);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             umma_bf16(tmem + (uint32_t)(64 * slot), d_h + (uint64_t)((kk * 32) >> 4),
@@ -349,14 +380,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                            Bs.abort_flag);
         if (!ok) break;
         tc_fence_after();
-        const uint64_t d_ht = umma_desc(hprev_tile(cw.p & 1, cw.s, cw.p), kTile, 1024, 2);
+        const uint64_t d_ht = umma_desc(hprev_tile(stage_of(cw.p), cw.s, cw.p), kTile, 1024, 2);
         const uint64_t d_dt = umma_desc(sbase + L.dt + (cw.u & 1) * kTile, 16, 1024, 2);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
           umma_bf16(tmem + kDwCol, d_ht + (uint64_t)((kk * 2048) >> 4),
                     d_dt + (uint64_t)((kk * 32) >> 4), idesc_w, (cw.u > 0 || kk > 0) ? 1u : 0u);
         umma_commit(&Bs.dtfree[cw.u & 1]);
-        if (cw.s == 0) umma_commit(&Bs.mmadone[cw.p & 1]);  // the chunk's stage may be reused
+        if (cw.s == 0) umma_commit(&Bs.mmadone[stage_of(cw.p)]);  // the chunk's stage may be reused
         cursor_next(cw, nchunks, T);
       }
       if (!ok) {
@@ -371,8 +402,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (cw.u > 0)
         mbar_wait_bounded(&Bs.dtfree[(cw.u - 1) & 1], (uint32_t)((cw.u - 1) >> 1) & 1u, limit);
     }
-  } else {
-    // ======================================================= compute warps
+  } else if constexpr (kCW == 4) {
+    // ======================================================= compute warps (one per row block)
     const int g = lane >> 2, c = lane & 3;
     const int r0 = 16 * warp + g, r1 = r0 + 8;
     const int lr = lane & 7, lq = lane >> 3;
@@ -400,9 +431,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (debug & kDebugForceTimeout) ok = mbar_wait_bounded(Bs.never, 0u, kDebugWaitLimitCycles);
     int u = 0;
     for (int p = 0; p < nchunks && ok; ++p) {
-      const int st = p & 1, t0 = (nchunks - 1 - p) * kTc;
+      const int st = stage_of(p), t0 = (nchunks - 1 - p) * kTc;
       const int steps = min(kTc, T - t0);
-      ok = wait_or_abort(&Bs.full[st], (uint32_t)(p >> 1) & 1u, limit, Bs.abort_flag);
+      ok = wait_or_abort(&Bs.full[st], phase_of(p), limit, Bs.abort_flag);
       const uint8_t* in = smem + L.in + st * L.in_stage;
       const uint16_t* qs = reinterpret_cast<const uint16_t*>(in + L.qs);
       const uint16_t* ks = reinterpret_cast<const uint16_t*>(in + L.ks);
@@ -533,7 +564,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float dfl = dfl2.x + dfl2.y;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) dfl += __shfl_xor_sync(0xffffffffu, dfl, o);
-        if (lane == 0) dfp[(st * kNW + warp) * kTc + s] = dfl;
+        if (lane == 0) dfp[(st * kCW + warp) * kTc + s] = dfl;
         float2 sq0 = make_float2(0.f, 0.f), sq1 = make_float2(0.f, 0.f);
         {
           uint32_t hc[kVT][4];
@@ -595,6 +626,246 @@ __global__ void __launch_bounds__(kThreads, 1)
       *Bs.abort_flag = 1;
       if (lane == 0) atomicExch(status, kStatusTimeout);
     }
+  } else {
+    // ================================================ compute warps (two per row block)
+    // Warp w: row block rb = w % 4 (rows 16 rb .. 16 rb + 15, the tensor-memory lanes of its
+    // sub-partition), column half ch = w / 4 (columns 32 ch .. 32 ch + 31).  The chain
+    // product C += D W^T needs all of D's columns: each warp writes its half of D_t^T to
+    // the swizzled tile, meets its partner at a named barrier, and reads the partner's
+    // half back as A fragments.
+    const int rb = warp & 3, ch = warp >> 2;
+    const int g = lane >> 2, c = lane & 3;
+    const int r0 = 16 * rb + g, r1 = r0 + 8;
+    const int c0 = 32 * ch;
+    const int lr = lane & 7, lq = lane >> 3;
+    const uint32_t t_rows = tmem + ((uint32_t)(32 * rb) << 16);
+
+    // W^T B fragments for this half's 4 n-tiles: k-tiles of D's own half (2 ch + q) in
+    // wown, those of the partner's half (2 (1 - ch) + q) in woth; static indices only.
+    uint32_t wown[2][4][2], woth[2][4][2];
+#pragma unroll
+    for (int q2 = 0; q2 < 2; ++q2)
+#pragma unroll
+      for (int nl = 0; nl < 4; ++nl) {
+        const uint16_t* wo = Wn + (c0 + 8 * nl + g) * kV + 16 * (2 * ch + q2) + 2 * c;
+        const uint16_t* wx = Wn + (c0 + 8 * nl + g) * kV + 16 * (2 * (1 - ch) + q2) + 2 * c;
+        wown[q2][nl][0] = *reinterpret_cast<const uint32_t*>(wo);
+        wown[q2][nl][1] = *reinterpret_cast<const uint32_t*>(wo + 8);
+        woth[q2][nl][0] = *reinterpret_cast<const uint32_t*>(wx);
+        woth[q2][nl][1] = *reinterpret_cast<const uint32_t*>(wx + 8);
+      }
+    float2 C[4][2];
+    const float* dhp = dH_T ? dH_T + (size_t)pair * kK * kV : nullptr;
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+      C[nt][0] = dhp ? *reinterpret_cast<const float2*>(dhp + r0 * kV + c0 + 8 * nt + 2 * c)
+                     : make_float2(0.f, 0.f);
+      C[nt][1] = dhp ? *reinterpret_cast<const float2*>(dhp + r1 * kV + c0 + 8 * nt + 2 * c)
+                     : make_float2(0.f, 0.f);
+    }
+    bool ok = true;
+    if (debug & kDebugForceTimeout) ok = mbar_wait_bounded(Bs.never, 0u, kDebugWaitLimitCycles);
+    ok = !named_bar_or(1 + rb, 64, !ok);
+    int u = 0;
+    for (int p = 0; p < nchunks && ok; ++p) {
+      const int st = stage_of(p), t0 = (nchunks - 1 - p) * kTc;
+      const int steps = min(kTc, T - t0);
+      ok = !named_bar_or(1 + rb, 64,
+                         !wait_or_abort(&Bs.full[st], phase_of(p), limit, Bs.abort_flag));
+      const uint8_t* in = smem + L.in + st * L.in_stage;
+      const uint16_t* qs = reinterpret_cast<const uint16_t*>(in + L.qs);
+      const uint16_t* ks = reinterpret_cast<const uint16_t*>(in + L.ks);
+      const uint16_t* vs = reinterpret_cast<const uint16_t*>(in + L.vs);
+      const float* dys = reinterpret_cast<const float*>(in + L.dys);
+      for (int s = steps - 1; s >= 0 && ok; --s, ++u) {
+        const uint32_t hprev = hprev_tile(st, s, p);
+        const uint32_t hcur = sbase + L.hs + (st * kStageTiles + s + 1) * kTile;
+        const float4 gt = gates[st * kTc + s];
+        const float2 ff = make_float2(gt.x, gt.x), gg = make_float2(gt.y, gt.y);
+
+        // ---- P_t (this half's 32 columns) from tensor memory, + k_t v_t^T
+        const int slot = u % kS;
+        bool w_ok = wait_or_abort(&Bs.pready[slot], (uint32_t)(u / kS) & 1u, limit, Bs.abort_flag);
+        if (u >= 2) {  // the dW product of step u - 2 has finished reading the D^T slot
+          w_ok = w_ok && wait_or_abort(&Bs.dtfree[u & 1], (uint32_t)((u >> 1) - 1) & 1u, limit,
+                                       Bs.abort_flag);
+        }
+        if (named_bar_or(1 + rb, 64, !w_ok)) {  // one decision for both halves
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t pr[16];
+        tmem_ld_16x256b_x4(t_rows + (uint32_t)(64 * slot + c0), pr);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&Bs.pfree[slot]);
+        const float kv0 = bf16_bits_to_float(ks[s * kK + r0]);
+        const float kv1 = bf16_bits_to_float(ks[s * kK + r1]);
+        const float2 k0 = make_float2(kv0, kv0), k1 = make_float2(kv1, kv1);
+        float2 vv[4], uu[4];
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+          vv[nt] = bf16x2_to_float2(
+              *reinterpret_cast<const uint32_t*>(vs + s * kV + c0 + 8 * nt + 2 * c));
+          uu[nt] = *reinterpret_cast<const float2*>(dys + s * kV + c0 + 8 * nt + 2 * c);
+        }
+        float2 P[4][2];
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+          P[nt][0] = fma2(k0, vv[nt], make_float2(__uint_as_float(pr[4 * nt]),
+                                                  __uint_as_float(pr[4 * nt + 1])));
+          P[nt][1] = fma2(k1, vv[nt], make_float2(__uint_as_float(pr[4 * nt + 2]),
+                                                  __uint_as_float(pr[4 * nt + 3])));
+        }
+        // ---- Z, R, D, dL/df partial, C <- f R (this half)
+        uint32_t ah[2][4];  // H_{t-1}, this half's two k-tiles
+#pragma unroll
+        for (int q2 = 0; q2 < 2; ++q2)
+          ldsm_x4(ah[q2], sw128_addr(hprev, 16 * rb + lr + 8 * (lq & 1), 4 * ch + 2 * q2 + (lq >> 1)));
+        const float qv0 = bf16_bits_to_float(qs[s * kK + r0]);
+        const float qv1 = bf16_bits_to_float(qs[s * kK + r1]);
+        const float2 q0 = make_float2(qv0, qv0), q1 = make_float2(qv1, qv1);
+        float2 dfl2 = make_float2(0.f, 0.f);
+        const float2 one = make_float2(1.f, 1.f);
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            const float2 h = bf16x2_to_float2(ah[nt >> 1][2 * (nt & 1) + r]);
+            const float2 z = make_float2(tanh_mufu(P[nt][r].x), tanh_mufu(P[nt][r].y));
+            const float2 R = fma2(r ? q1 : q0, uu[nt], C[nt][r]);
+            const float2 omz = fma2(make_float2(-z.x, -z.y), z, one);
+            P[nt][r] = mul2(mul2(gg, R), omz);                         // D_t
+            dfl2 = fma2(R, make_float2(h.x - z.x, h.y - z.y), dfl2);
+            C[nt][r] = mul2(ff, R);
+          }
+        // ---- this half of D_t: bf16 A fragments; D_t^T to the shared tile
+        uint32_t aown[2][4], aoth[2][4];
+#pragma unroll
+        for (int q2 = 0; q2 < 2; ++q2) {
+          aown[q2][0] = pack_bf16x2(P[2 * q2][0].x, P[2 * q2][0].y);
+          aown[q2][1] = pack_bf16x2(P[2 * q2][1].x, P[2 * q2][1].y);
+          aown[q2][2] = pack_bf16x2(P[2 * q2 + 1][0].x, P[2 * q2 + 1][0].y);
+          aown[q2][3] = pack_bf16x2(P[2 * q2 + 1][1].x, P[2 * q2 + 1][1].y);
+        }
+        const uint32_t dts = sbase + L.dt + (u & 1) * kTile;
+#pragma unroll
+        for (int q2 = 0; q2 < 2; ++q2) {
+          const int kj = 2 * ch + q2;  // D^T rows j = 16 kj .., columns i = 16 rb ..
+          stsm_x4_trans(sw128_addr(dts, 16 * kj + lr + 8 * (lq >> 1), 2 * rb + (lq & 1)), aown[q2]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&Bs.dtready[u & 1]);
+        named_bar_sync(1 + rb, 64);  // the partner's half of this row block is written
+#pragma unroll
+        for (int q2 = 0; q2 < 2; ++q2) {
+          const int kj = 2 * (1 - ch) + q2;
+          ldsm_x4_trans(aoth[q2], sw128_addr(dts, 16 * kj + lr + 8 * (lq >> 1), 2 * rb + (lq & 1)));
+        }
+        // ---- the chain: C += D_t W^T (this half's columns, all 64 of D's): own k-tiles first
+#pragma unroll
+        for (int q2 = 0; q2 < 2; ++q2)
+#pragma unroll
+          for (int nl = 0; nl < 4; ++nl) mma2(C[nl], aown[q2], wown[q2][nl][0], wown[q2][nl][1]);
+#pragma unroll
+        for (int q2 = 0; q2 < 2; ++q2)
+#pragma unroll
+          for (int nl = 0; nl < 4; ++nl) mma2(C[nl], aoth[q2], woth[q2][nl][0], woth[q2][nl][1]);
+
+        // ---- partial sums of this half: dk (D v), dv (D^T k), dL/df, dq (H_t u)
+        float2 sk0 = make_float2(0.f, 0.f), sk1 = make_float2(0.f, 0.f);
+        float pdv[8];
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+          sk0 = fma2(P[nt][0], vv[nt], sk0);
+          sk1 = fma2(P[nt][1], vv[nt], sk1);
+          const float2 pv = fma2(k1, P[nt][1], mul2(k0, P[nt][0]));
+          pdv[2 * nt] = pv.x;
+          pdv[2 * nt + 1] = pv.y;
+        }
+#pragma unroll
+        for (int stg = 0; stg < 3; ++stg) {  // reduce-scatter over the 8 row groups
+          const int mask = 16 >> stg, half = 4 >> stg;
+          const bool up = (lane & mask) != 0;
+#pragma unroll
+          for (int i = 0; i < half; ++i) {
+            const float send = up ? pdv[i] : pdv[i + half];
+            const float keep = up ? pdv[i + half] : pdv[i];
+            pdv[i] = keep + __shfl_xor_sync(0xffffffffu, send, mask);
+          }
+        }
+        // Lane (g, c) holds column c0 + 8 (g >> 1) + 2c + (g & 1).
+        dvp[((st * kNW + rb) * kTc + s) * kV + c0 + 8 * (g >> 1) + 2 * c + (g & 1)] = pdv[0];
+        float dfl = dfl2.x + dfl2.y;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) dfl += __shfl_xor_sync(0xffffffffu, dfl, o);
+        if (lane == 0) dfp[(st * kCW + warp) * kTc + s] = dfl;
+        float2 sq0 = make_float2(0.f, 0.f), sq1 = make_float2(0.f, 0.f);
+        {
+          uint32_t hc[2][4];
+#pragma unroll
+          for (int q2 = 0; q2 < 2; ++q2)
+            ldsm_x4(hc[q2], sw128_addr(hcur, 16 * rb + lr + 8 * (lq & 1), 4 * ch + 2 * q2 + (lq >> 1)));
+#pragma unroll
+          for (int nt = 0; nt < 4; ++nt) {
+            sq0 = fma2(bf16x2_to_float2(hc[nt >> 1][2 * (nt & 1)]), uu[nt], sq0);
+            sq1 = fma2(bf16x2_to_float2(hc[nt >> 1][2 * (nt & 1) + 1]), uu[nt], sq1);
+          }
+        }
+        float k0s = sk0.x + sk0.y, k1s = sk1.x + sk1.y;
+        float q0s = sq0.x + sq0.y, q1s = sq1.x + sq1.y;
+#pragma unroll
+        for (int o = 1; o <= 2; o <<= 1) {
+          k0s += __shfl_xor_sync(0xffffffffu, k0s, o);
+          k1s += __shfl_xor_sync(0xffffffffu, k1s, o);
+          q0s += __shfl_xor_sync(0xffffffffu, q0s, o);
+          q1s += __shfl_xor_sync(0xffffffffu, q1s, o);
+        }
+        if (c == 0) {
+          float* pk = dkqp + ((st * 2 + ch) * 2 * kTc + s) * kK;
+          float* pq = pk + kTc * kK;
+          pk[r0] = k0s;
+          pk[r1] = k1s;
+          pq[r0] = q0s;
+          pq[r1] = q1s;
+        }
+      }
+      if (!ok) break;
+      mbar_arrive(&Bs.done[st]);
+    }
+    if (ok) {  // the last dW product has finished: this warp's 16 rows x 32 columns of dW
+      ok = !named_bar_or(1 + rb, 64,
+                         !wait_or_abort(&Bs.dtfree[(T - 1) & 1], (uint32_t)((T - 1) >> 1) & 1u,
+                                        limit, Bs.abort_flag));
+      if (ok) {
+        tc_fence_after();
+        uint32_t wr[16];
+        tmem_ld_16x256b_x4(t_rows + kDwCol + c0, wr);
+        tmem_wait_ld();
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+          *reinterpret_cast<float2*>(dWp + r0 * kV + c0 + 8 * nt + 2 * c) =
+              make_float2(__uint_as_float(wr[4 * nt]), __uint_as_float(wr[4 * nt + 1]));
+          *reinterpret_cast<float2*>(dWp + r1 * kV + c0 + 8 * nt + 2 * c) =
+              make_float2(__uint_as_float(wr[4 * nt + 2]), __uint_as_float(wr[4 * nt + 3]));
+        }
+        if (dH0) {
+          float* hp = dH0 + (size_t)pair * kK * kV;
+#pragma unroll
+          for (int nt = 0; nt < 4; ++nt) {
+            *reinterpret_cast<float2*>(hp + r0 * kV + c0 + 8 * nt + 2 * c) = C[nt][0];
+            *reinterpret_cast<float2*>(hp + r1 * kV + c0 + 8 * nt + 2 * c) = C[nt][1];
+          }
+        }
+      }
+    }
+    if (!ok) {
+      *Bs.abort_flag = 1;
+      if (lane == 0) atomicExch(status, kStatusTimeout);
+    }
   }
 
   tc_fence_before();
@@ -616,9 +887,10 @@ bool make_map(EncodeTiledFn enc, CUtensorMap* map, CUtensorMapDataType dt, const
 
 }  // namespace
 
-cudaError_t launch_bwd_bf16_tc(const BackwardProblem& p, EncodeTiledFn enc, int debug, int* status,
-                               cudaStream_t stream) {
-  const TcLayout L = tc_layout();
+template <int kCW>
+cudaError_t launch_tc(const BackwardProblem& p, EncodeTiledFn enc, int debug, int* status,
+                      cudaStream_t stream) {
+  const TcLayout L = tc_layout<kCW>();
   const cuuint64_t B = (cuuint64_t)p.B, T = (cuuint64_t)p.T, N = (cuuint64_t)p.N;
   CUtensorMap mh, mq, mk, mv, mdy;
   const cuuint64_t dh[4] = {kV, kK, T, B * N};
@@ -638,15 +910,21 @@ cudaError_t launch_bwd_bf16_tc(const BackwardProblem& p, EncodeTiledFn enc, int 
       !make_map(enc, &mdy, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.dy, 4, dvv, bvv,
                 CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
-  cudaError_t err =
-      cudaFuncSetAttribute(bwd_bf16_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
+  cudaError_t err = cudaFuncSetAttribute(bwd_bf16_tc<kCW>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
   if (err != cudaSuccess) return err;
   float* heads = p.ws + (size_t)p.B * p.N * backward_pair_floats(kK, kV);
-  bwd_bf16_tc<<<(unsigned)(p.B * p.N), kThreads, L.total, stream>>>(
+  bwd_bf16_tc<kCW><<<(unsigned)(p.B * p.N), 32 * (kCW + 2), L.total, stream>>>(
       mh, mq, mk, mv, mdy, (const uint16_t*)p.a, p.alpha, p.beta, (const uint16_t*)p.W, p.w_r,
       p.H0, p.dH_T, p.dq, p.dk, p.dv, p.da, p.dH0, p.ws, heads, p.T, p.N, p.Nqk, debug, status);
   err = cudaGetLastError();
   return err == cudaSuccess ? launch_bwd_reduce(p, stream) : err;
+}
+
+cudaError_t launch_bwd_bf16_tc(const BackwardProblem& p, EncodeTiledFn enc, int debug, int* status,
+                               int compute_warps, cudaStream_t stream) {
+  return compute_warps == 8 ? launch_tc<8>(p, enc, debug, status, stream)
+                            : launch_tc<4>(p, enc, debug, status, stream);
 }
 
 }  // namespace m2rnn

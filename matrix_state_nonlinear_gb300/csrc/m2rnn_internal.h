@@ -119,9 +119,10 @@ cudaError_t launch_fwd_bf16_mma_cluster(const Problem& p, EncodeTiledFn enc, cud
 bool bwd_mma_supports(int K, int V);
 cudaError_t launch_bwd_bf16_mma(const BackwardProblem& p, EncodeTiledFn enc, int debug,
                                 int* status, cudaStream_t stream);
-// The same backward with H_{t-1} W and the dW sum on tcgen05 (tensor memory), K = V = 64.
+// The same backward with H_{t-1} W and the dW sum on tcgen05 (tensor memory), K = V = 64,
+// with 4 compute warps (one per 16-row block) or 8 (two per row block, column halves).
 cudaError_t launch_bwd_bf16_tc(const BackwardProblem& p, EncodeTiledFn enc, int debug, int* status,
-                               cudaStream_t stream);
+                               int compute_warps, cudaStream_t stream);
 
 // One decode step (T = 1) on the warp MMA, no TMA: K % 16 == 0, K <= 128,
 // V in {16, 32, 64}.  Uses q, k, v, a, alpha, beta, W, w_r, H0 (state in, may be
