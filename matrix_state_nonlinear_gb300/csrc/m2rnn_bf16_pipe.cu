@@ -32,6 +32,8 @@
 // issue slot); tanh is the MUFU tanh.approx.f32.
 #include <cuda_bf16.h>
 
+#include <cstring>
+
 #include "m2rnn_internal.h"
 #include "ptx_util.cuh"
 
@@ -45,12 +47,14 @@ struct PipeLayout {
                                 //                          target of the empty first pending readout)
   int wr;                       // float  [V]
   int bar;                      // uint64 full[2], done[2], never-armed[1]; int abort
+  int hring;                    // state-keeping forward, V = 64: [nw][4 slots][16 rows][64] bf16,
+                                //   128-byte swizzled, staged for TMA stores (+1024 to align)
   int total;
 };
 
 __host__ __device__ inline int al128(int x) { return (x + 127) & ~127; }
 
-__host__ __device__ inline PipeLayout pipe_layout(int K, int V, int Tc) {
+__host__ __device__ inline PipeLayout pipe_layout(int K, int V, int Tc, bool ring = false) {
   PipeLayout L;
   const int nw = K / 16;
   L.qs = 0;
@@ -66,6 +70,8 @@ __host__ __device__ inline PipeLayout pipe_layout(int K, int V, int Tc) {
   o += al128(V * 4);
   L.bar = o;
   o += 128;
+  L.hring = o;
+  if (ring) o += nw * 4 * 16 * V * 2 + 1024;
   L.total = o;
   return L;
 }
@@ -74,7 +80,8 @@ template <int VT, bool kCache>
 __global__ void __launch_bounds__(160, 1)
     fwd_bf16_mma_pipe(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
-                      const __grid_constant__ CUtensorMap tm_v, const uint16_t* __restrict__ a,
+                      const __grid_constant__ CUtensorMap tm_v,
+                      const __grid_constant__ CUtensorMap tm_hs, const uint16_t* __restrict__ a,
                       const float* __restrict__ alpha, const float* __restrict__ beta,
                       const uint16_t* __restrict__ W, const float* __restrict__ w_r,
                       const float* H0, float* __restrict__ y, float* H_T, uint16_t* __restrict__ Hs,
@@ -85,7 +92,9 @@ __global__ void __launch_bounds__(160, 1)
 
   extern __shared__ __align__(128) uint8_t smem[];
   const int nw = K / 16;  // compute warps; warp nw is the producer
-  const PipeLayout L = pipe_layout(K, V, Tc);
+  // V = 64 keeps the states through a shared-memory ring and TMA tensor stores.
+  constexpr bool kRing = kCache && VT == 4;
+  const PipeLayout L = pipe_layout(K, V, Tc, kRing);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int pair = blockIdx.x, b = pair / N, n = pair - (pair / N) * N;
   const int nchunks = (T + Tc - 1) / Tc;
@@ -379,7 +388,29 @@ __global__ void __launch_bounds__(160, 1)
     // This step's partial sums are reduced during the next step (or at chunk end).
 #pragma unroll
     for (int i = 0; i < M; ++i) pout[i] = p[i];
-    if constexpr (kCache) {
+    if constexpr (kRing) {
+      // Keep H_t for the backward pass as the bf16 A fragments just packed from it
+      // (exactly the tensor-core operand step t+1 uses): stmatrix into this warp's slot of
+      // a 4-slot swizzled ring, then one TMA store of the warp's 16 rows.  A slot is
+      // rewritten only after the store issued from it four steps earlier has read it.
+      const int t = cc * Tc + s;
+      const uint32_t rbase = (smem_u32(smem) + L.hring + 1023u) & ~1023u;
+      const uint32_t sb = rbase + (uint32_t)((warp * 4 + (t & 3)) * 16 * V * 2);
+      if (t >= 4) {
+        if (lane == 0) bulk_wait_group_read<3>();
+        __syncwarp();
+      }
+      const int lr = lane & 7, lq = lane >> 3;
+#pragma unroll
+      for (int kt = 0; kt < VT; ++kt)
+        stsm_x4(sw128_addr(sb, lr + 8 * (lq & 1), 2 * kt + (lq >> 1)), af[kt]);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_4d(&tm_hs, sb, 0, 16 * warp, t, pair);
+        bulk_commit_group();
+      }
+    } else if constexpr (kCache) {
       // Keep H_t for the backward pass as the bf16 A fragments just packed from it:
       // exactly the tensor-core operand step t+1 uses (streaming stores).
       uint16_t* hp = Hs + ((size_t)pair * T + (size_t)cc * Tc + s) * K * V;
@@ -426,6 +457,9 @@ __global__ void __launch_bounds__(160, 1)
     if (aborted) {
       *abort_flag = 1;
       if (lane == 0) atomicExch(status, kStatusTimeout);
+      if constexpr (kRing) {
+        if (lane == 0) bulk_wait_group<0>();  // stores still reading the ring
+      }
       return;
     }
     {  // flush the chunk's last pending readout
@@ -447,6 +481,9 @@ __global__ void __launch_bounds__(160, 1)
       *reinterpret_cast<float2*>(hp + (size_t)r1 * V + 8 * nt + 2 * c) = h[nt][1];
     }
   }
+  if constexpr (kRing) {
+    if (lane == 0) bulk_wait_group<0>();  // every state store complete before the block ends
+  }
 }
 
 bool make_map_pipe(EncodeTiledFn enc, CUtensorMap* map, const void* base, int inner, int N, int T,
@@ -464,23 +501,37 @@ bool make_map_pipe(EncodeTiledFn enc, CUtensorMap* map, const void* base, int in
 template <int VT>
 cudaError_t launch_pipe_vt(const Problem& p, EncodeTiledFn enc, cudaStream_t stream) {
   const int V = 16 * VT;
+  const bool ring = p.Hs && VT == 4;
   int Tc = 64;
-  PipeLayout L = pipe_layout(p.K, V, Tc);
+  PipeLayout L = pipe_layout(p.K, V, Tc, ring);
   while (L.total > 227 * 1024 && Tc > 8) {
     Tc /= 2;
-    L = pipe_layout(p.K, V, Tc);
+    L = pipe_layout(p.K, V, Tc, ring);
   }
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mh;
   if (!make_map_pipe(enc, &mq, p.q, p.K, p.Nqk, p.T, p.B, Tc) ||
       !make_map_pipe(enc, &mk, p.k, p.K, p.Nqk, p.T, p.B, Tc) ||
       !make_map_pipe(enc, &mv, p.v, V, p.N, p.T, p.B, Tc))
     return cudaErrorInvalidValue;
+  memset(&mh, 0, sizeof(mh));
+  if (ring) {  // kept states [B N, T, K, V] bf16, stored 16 rows at a time, 128-byte swizzle
+    const cuuint64_t dims[4] = {(cuuint64_t)V, (cuuint64_t)p.K, (cuuint64_t)p.T,
+                                (cuuint64_t)p.B * p.N};
+    const cuuint64_t strides[3] = {(cuuint64_t)V * 2, (cuuint64_t)V * 2 * p.K,
+                                   (cuuint64_t)V * 2 * p.K * p.T};
+    const cuuint32_t box[4] = {(cuuint32_t)V, 16u, 1u, 1u};
+    const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    if (enc(&mh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, p.Hs, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
   auto kern = p.Hs ? fwd_bf16_mma_pipe<VT, true> : fwd_bf16_mma_pipe<VT, false>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
   if (err != cudaSuccess) return err;
   const unsigned grid = (unsigned)p.B * (unsigned)p.N;
   const int threads = 32 * (p.K / 16 + 1);
-  kern<<<grid, threads, L.total, stream>>>(mq, mk, mv, (const uint16_t*)p.a, p.alpha, p.beta,
+  kern<<<grid, threads, L.total, stream>>>(mq, mk, mv, mh, (const uint16_t*)p.a, p.alpha, p.beta,
                                            (const uint16_t*)p.W, p.w_r, p.H0, p.y, p.H_T,
                                            static_cast<uint16_t*>(p.Hs), p.T,
                                            p.N, p.K, Tc, p.Nqk == 1 ? 0 : 1, p.debug, p.status);
