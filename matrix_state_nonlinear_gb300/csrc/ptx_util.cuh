@@ -78,6 +78,18 @@ __device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, uint32_t sm
 __device__ __forceinline__ void bulk_commit_group() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
+// tma_store_4d issued only where `pred` holds, as a predicated instruction rather than a
+// branch (a warp can call it converged, keeping the caller's code one basic block).
+__device__ __forceinline__ void tma_store_4d_if(bool pred, const CUtensorMap* map,
+                                                uint32_t smem_src, int c0, int c1, int c2, int c3) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+      "@p cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5}], [%1];\n\t}"
+      ::"l"(reinterpret_cast<uint64_t>(map)), "r"(smem_src), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+      "r"((int)pred)
+      : "memory");
+}
+
 // Waits until at most N of this thread's bulk groups still read shared memory.
 template <int N>
 __device__ __forceinline__ void bulk_wait_group_read() {
