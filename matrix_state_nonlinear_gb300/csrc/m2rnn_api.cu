@@ -302,9 +302,9 @@ m2rnn_status m2rnn_backward_bf16(const uint16_t* q, const uint16_t* k, const uin
   if (st != M2RNN_OK) return st;
   const int debug = variant >> 8;
   int base = variant & 0xff;
-  if (base < 0 || base > 4) return M2RNN_ERR_INVALID_ARG;
+  if (base < 0 || base > 5) return M2RNN_ERR_INVALID_ARG;
   const bool mma_ok = bwd_mma_supports(K, V) && T > 0;
-  if (base == 0) base = mma_ok ? 3 : 1;
+  if (base == 0) base = mma_ok ? 5 : 1;
   if (base >= 2 && !mma_ok) return M2RNN_ERR_UNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (base == 1) return launch_bwd_simt_bf16(p, s) == cudaSuccess ? M2RNN_OK : M2RNN_ERR_CUDA;
@@ -317,8 +317,10 @@ m2rnn_status m2rnn_backward_bf16(const uint16_t* q, const uint16_t* k, const uin
   int* status = status_address(dev);
   EncodeTiledFn enc = encode_fn();
   if (!status || !enc) return M2RNN_ERR_CUDA;
-  const cudaError_t err = base >= 3 ? launch_bwd_bf16_tc(p, enc, debug, status, base == 4 ? 8 : 4, s)
-                                    : launch_bwd_bf16_mma(p, enc, debug, status, s);
+  const cudaError_t err =
+      base == 5   ? launch_bwd_bf16_tcc(p, enc, debug, status, s)
+      : base >= 3 ? launch_bwd_bf16_tc(p, enc, debug, status, base == 4 ? 8 : 4, s)
+                  : launch_bwd_bf16_mma(p, enc, debug, status, s);
   return err == cudaSuccess ? M2RNN_OK : M2RNN_ERR_CUDA;
 }
 

@@ -123,6 +123,9 @@ cudaError_t launch_bwd_bf16_mma(const BackwardProblem& p, EncodeTiledFn enc, int
 // with 4 compute warps (one per 16-row block) or 8 (two per row block, column halves).
 cudaError_t launch_bwd_bf16_tc(const BackwardProblem& p, EncodeTiledFn enc, int debug, int* status,
                                int compute_warps, cudaStream_t stream);
+// The same backward with the chain product D_t W^T on tcgen05 as well (eight compute warps).
+cudaError_t launch_bwd_bf16_tcc(const BackwardProblem& p, EncodeTiledFn enc, int debug,
+                                int* status, cudaStream_t stream);
 
 // One decode step (T = 1) on the warp MMA, no TMA: K % 16 == 0, K <= 128,
 // V in {16, 32, 64}.  Uses q, k, v, a, alpha, beta, W, w_r, H0 (state in, may be

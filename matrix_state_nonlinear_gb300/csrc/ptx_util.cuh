@@ -183,6 +183,11 @@ __device__ __forceinline__ float2 mul2(float2 a, float2 b) {
   asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2_as_u64(a)), "l"(f2_as_u64(b)));
   return u64_as_f2(d);
 }
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2_as_u64(a)), "l"(f2_as_u64(b)));
+  return u64_as_f2(d);
+}
 __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t u) {
   return make_float2(bf16_lo(u), bf16_hi(u));
 }
@@ -316,6 +321,13 @@ __host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N, bool a_mn_m
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// The same with the major-ness of both operands chosen: b_mn_major stores B N-contiguous
+// (bit 16 of the descriptor), as a_mn_major does for A (bit 15).
+__host__ __device__ constexpr uint32_t umma_idesc_bf16_ab(int M, int N, bool a_mn_major,
+                                                         bool b_mn_major) {
+  return umma_idesc_bf16(M, N, a_mn_major) | ((b_mn_major ? 1u : 0u) << 16);
+}
+
 // D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                           uint32_t idesc, uint32_t accumulate) {
@@ -326,11 +338,38 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint
       : "memory");
 }
 
+// umma_bf16 issued only where `pred` holds, predicated rather than branched: a whole warp
+// can run the issuing loop (descriptors stay warp-uniform) while one lane issues.
+__device__ __forceinline__ void umma_bf16_if(bool pred, uint32_t d_tmem, uint64_t a_desc,
+                                             uint64_t b_desc, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 q, %5, 0;\n\t"
+      "@q tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+      ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"((int)pred)
+      : "memory");
+}
+
+// One lane of the (converged) warp: true there, false elsewhere.
+__device__ __forceinline__ bool elect_one_sync() {
+  uint32_t pred = 0;
+  asm volatile("{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.u32 %0, 1, 0, P;\n\t}"
+               : "=r"(pred));
+  return pred != 0;
+}
+
 // The mbarrier completes when every tcgen05.mma issued so far by this thread is done.
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
                ::"r"(smem_u32(bar))
                : "memory");
+}
+
+__device__ __forceinline__ void umma_commit_if(bool pred, uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %1, 0;\n\t"
+      "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}"
+      ::"r"(smem_u32(bar)), "r"((int)pred)
+      : "memory");
 }
 
 __device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {  // one full warp

@@ -123,8 +123,8 @@ BF16_SHAPES = [(1, 1, 1, 16, 16), (2, 65, 3, 64, 64), (1, 130, 2, 32, 32), (2, 4
 
 def bwd_variants(K, V):
     # 1: SIMT (any shape); 2: warp-MMA kernel; 3, 4: tcgen05 kernels with 4 or 8 compute
-    # warps (K = V = 64)
-    return [1, 2, 3, 4] if (K, V) == (64, 64) else [1]
+    # warps; 5: every product on tcgen05, the chain included (K = V = 64)
+    return [1, 2, 3, 4, 5] if (K, V) == (64, 64) else [1]
 
 
 @pytest.mark.parametrize("shape", BF16_SHAPES)
@@ -135,20 +135,20 @@ def test_backward_bf16_matches_oracle(shape, h0):
         assert max(errs.values()) <= TOL["bf16"], (variant, errs)
 
 
-@pytest.mark.parametrize("variant", [1, 2, 3, 4])
+@pytest.mark.parametrize("variant", [1, 2, 3, 4, 5])
 def test_backward_bf16_shared_qk(variant):
     _, _, g, errs = run_case("bf16", 2, 50, 4, 64, 64, shared=True, variant=variant)
     assert g["dq"].shape[2] == 1
     assert max(errs.values()) <= TOL["bf16"], errs
 
 
-@pytest.mark.parametrize("variant", [2, 3, 4])
+@pytest.mark.parametrize("variant", [2, 3, 4, 5])
 def test_backward_mma_without_dHT(variant):
     _, _, _, errs = run_case("bf16", 2, 37, 2, 64, 64, with_dHT=False, variant=variant)
     assert max(errs.values()) <= TOL["bf16"], errs
 
 
-@pytest.mark.parametrize("variant", [2, 3, 4])
+@pytest.mark.parametrize("variant", [2, 3, 4, 5])
 def test_backward_mma_close_to_simt(variant):
     """The kernels differentiate the same kept states; they differ only by rounding
     (bf16 D in the MMA products vs fp32 SIMT sums)."""
@@ -162,7 +162,7 @@ def test_backward_mma_close_to_simt(variant):
         assert rel_err(g2[n], g1[n].double().cpu().numpy()) <= 1e-2, n
 
 
-@pytest.mark.parametrize("variant", [2, 3, 4])
+@pytest.mark.parametrize("variant", [2, 3, 4, 5])
 def test_backward_mma_forced_timeout_is_reported(variant):
     wl = Workload("to", 2, 20, 2, 64, 64, h0="uniform")
     inp = make_inputs(wl, DEV, 3)
