@@ -126,7 +126,8 @@ m2rnn_status m2rnn_forward_bf16_qk(const uint16_t* q, const uint16_t* k, const u
  *                           rounding of H_t, i.e. exactly the tensor-core operand
  *                           the next step multiplies by W (B·N·T·K·V·2 bytes).
  *   Hs is required when T > 0 (16-byte aligned on the bf16 entry).  The bf16 entry takes the pipelined warp-MMA
- *   kernel, so it supports K a multiple of 16 with K <= 64 and V in {16, 32, 64}
+ *   kernel for K a multiple of 16 with K <= 64 and V in {16, 32, 64}, and the row-warp
+ *   kernel (W in shared memory) for K a multiple of 16 up to 128 with V = 128
  *   (UNSUPPORTED otherwise); the fp32 entry supports 1 <= K, V <= 128.
  */
 m2rnn_status m2rnn_forward_train_f32(const float* q, const float* k, const float* v,
@@ -230,9 +231,11 @@ m2rnn_status m2rnn_backward_bf16_noalloc(const uint16_t* q, const uint16_t* k, c
  *          the state in place)
  *   y      [B, N, V] float32
  * The arithmetic is exactly one step of m2rnn_forward_bf16 (K <= 64, V <= 64 path),
- * so T successive calls reproduce a T-step forward bit for bit.  No TMA and no
- * pipelining: the launch is a single small kernel, suitable for CUDA-graph capture.
- * Supports K a multiple of 16 with K <= 128 and V in {16, 32, 64} (UNSUPPORTED
+ * so T successive calls reproduce a T-step forward bit for bit.  For V = 128 the
+ * forward uses other kernels (other summation orders): the results agree within the
+ * bf16 path's tolerance, not bit for bit.  No TMA and no pipelining: the launch is a
+ * single small kernel, suitable for CUDA-graph capture.
+ * Supports K a multiple of 16 with K <= 128 and V in {16, 32, 64, 128} (UNSUPPORTED
  * otherwise).  Same pointer and size errors as m2rnn_forward_bf16 (INVALID_ARG for a
  * null H_out, or W not 16-byte aligned).
  */

@@ -73,15 +73,18 @@ __device__ __forceinline__ float2 gate_pair(float a, float al, float be) {
   return make_float2(expf(e), -expm1f(e));
 }
 
-template <int VT, bool WREG>
+// kCache: also keep every state H_t, as the bf16 A fragments the next step's MMAs use
+// (Hs [B N, T, K, V]), for the backward pass.
+template <int VT, bool WREG, bool kCache>
 __global__ void __launch_bounds__(256, 1)
     fwd_bf16_mma_rowwarp(const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, const uint16_t* __restrict__ a,
                          const float* __restrict__ alpha, const float* __restrict__ beta,
                          const uint16_t* __restrict__ W, const float* __restrict__ w_r,
-                         const float* H0, float* __restrict__ y, float* H_T, int T, int N, int K,
-                         int Tc, int qk_hs, int debug, int* status) {
+                         const float* H0, float* __restrict__ y, float* H_T,
+                         uint16_t* __restrict__ Hs, int T, int N, int K, int Tc, int qk_hs,
+                         int debug, int* status) {
   constexpr int V = 16 * VT;
   constexpr int NT = 2 * VT;  // n-tiles of 8 columns
   constexpr int M = 4 * VT;   // readout partial sums per thread
@@ -268,6 +271,16 @@ __global__ void __launch_bounds__(256, 1)
         af[kt][2] = pack_bf16x2(h[2 * kt + 1][0], h[2 * kt + 1][1]);
         af[kt][3] = pack_bf16x2(h[2 * kt + 1][2], h[2 * kt + 1][3]);
       }
+      if constexpr (kCache) {  // H_t in bf16, streaming stores
+        uint16_t* hp = Hs + ((size_t)pair * T + t0 + s) * K * V;
+#pragma unroll
+        for (int kt = 0; kt < VT; ++kt) {
+          __stcs(reinterpret_cast<unsigned int*>(hp + (size_t)r0 * V + 16 * kt + 2 * c), af[kt][0]);
+          __stcs(reinterpret_cast<unsigned int*>(hp + (size_t)r1 * V + 16 * kt + 2 * c), af[kt][1]);
+          __stcs(reinterpret_cast<unsigned int*>(hp + (size_t)r0 * V + 16 * kt + 8 + 2 * c), af[kt][2]);
+          __stcs(reinterpret_cast<unsigned int*>(hp + (size_t)r1 * V + 16 * kt + 8 + 2 * c), af[kt][3]);
+        }
+      }
       // Readout (Eq. (12)): this thread's two rows, weighted by q, per column.
       float p[M];
 #pragma unroll
@@ -362,8 +375,8 @@ bool make_map(EncodeTiledFn enc, CUtensorMap* map, const void* base, int inner, 
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int VT, bool WREG>
-cudaError_t launch_vt(const Problem& p, EncodeTiledFn enc, cudaStream_t stream) {
+template <int VT, bool WREG, bool kCache>
+cudaError_t launch_vt_cache(const Problem& p, EncodeTiledFn enc, cudaStream_t stream) {
   const int V = 16 * VT;
   // Tc <= threads (one gate logit per thread and chunk), and the shared memory fits.
   int Tc = min(V <= 64 ? 64 : 32, 2 * p.K);
@@ -377,15 +390,21 @@ cudaError_t launch_vt(const Problem& p, EncodeTiledFn enc, cudaStream_t stream) 
       !make_map(enc, &mk, p.k, p.K, p.Nqk, p.T, p.B, Tc) ||
       !make_map(enc, &mv, p.v, V, p.N, p.T, p.B, Tc))
     return cudaErrorInvalidValue;
-  auto kern = fwd_bf16_mma_rowwarp<VT, WREG>;
+  auto kern = fwd_bf16_mma_rowwarp<VT, WREG, kCache>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
   if (err != cudaSuccess) return err;
   const unsigned grid = (unsigned)p.B * (unsigned)p.N;
   kern<<<grid, 2 * p.K, L.total, stream>>>(mq, mk, mv, (const uint16_t*)p.a, p.alpha, p.beta,
-                                           (const uint16_t*)p.W, p.w_r, p.H0, p.y, p.H_T, p.T,
-                                           p.N, p.K, Tc, p.Nqk == 1 ? 0 : 1, p.debug,
-                                           p.status);
+                                           (const uint16_t*)p.W, p.w_r, p.H0, p.y, p.H_T,
+                                           static_cast<uint16_t*>(p.Hs), p.T, p.N, p.K, Tc,
+                                           p.Nqk == 1 ? 0 : 1, p.debug, p.status);
   return cudaGetLastError();
+}
+
+template <int VT, bool WREG>
+cudaError_t launch_vt(const Problem& p, EncodeTiledFn enc, cudaStream_t stream) {
+  if (p.Hs) return launch_vt_cache<VT, WREG, true>(p, enc, stream);
+  return launch_vt_cache<VT, WREG, false>(p, enc, stream);
 }
 
 }  // namespace

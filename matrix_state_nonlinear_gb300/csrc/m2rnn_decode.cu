@@ -28,10 +28,11 @@ namespace {
 
 constexpr int kMaxWarps = 8;  // K <= 128
 
-// MAXW: the most warps a launch uses (K / 16 <= MAXW).  Four-warp launches (K <= 64)
-// are register-capped so that six blocks fit on an SM: more state loads in flight.
+// MAXW: the most warps a launch uses (K / 16 <= MAXW).  Four-warp launches (K <= 64) with
+// V <= 64 are register-capped so that six blocks fit on an SM: more state loads in flight.
+// V = 128 keeps twice the state and accumulator per thread and is not capped.
 template <int VT, int MAXW>
-__global__ void __launch_bounds__(32 * MAXW, MAXW <= 4 ? 6 : 1)
+__global__ void __launch_bounds__(32 * MAXW, (MAXW <= 4 && VT <= 4) ? 6 : 1)
     decode_bf16_mma(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
                     const uint16_t* __restrict__ v, const uint16_t* __restrict__ a,
                     const float* __restrict__ alpha, const float* __restrict__ beta,
@@ -170,7 +171,8 @@ __global__ void __launch_bounds__(32 * MAXW, MAXW <= 4 ? 6 : 1)
 }  // namespace
 
 bool decode_supports(int K, int V) {
-  return K >= 16 && K <= 16 * kMaxWarps && K % 16 == 0 && (V == 16 || V == 32 || V == 64);
+  return K >= 16 && K <= 16 * kMaxWarps && K % 16 == 0 &&
+         (V == 16 || V == 32 || V == 64 || V == 128);
 }
 
 cudaError_t launch_decode_bf16(const Problem& p, cudaStream_t stream) {
@@ -187,6 +189,7 @@ cudaError_t launch_decode_bf16(const Problem& p, cudaStream_t stream) {
     case 16: small ? args(decode_bf16_mma<1, 4>) : args(decode_bf16_mma<1, kMaxWarps>); break;
     case 32: small ? args(decode_bf16_mma<2, 4>) : args(decode_bf16_mma<2, kMaxWarps>); break;
     case 64: small ? args(decode_bf16_mma<4, 4>) : args(decode_bf16_mma<4, kMaxWarps>); break;
+    case 128: small ? args(decode_bf16_mma<8, 4>) : args(decode_bf16_mma<8, kMaxWarps>); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();

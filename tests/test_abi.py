@@ -177,7 +177,8 @@ def test_forward_train_argument_checks(lib):
     p[11] = None                                   # Hs missing with T > 0
     assert lib.m2rnn_forward_train_f32(*p, 1, 4, 1, 1, 8, 8, None) == binding.ERR_INVALID_ARG
     p = fake_ptrs(12)
-    assert lib.m2rnn_forward_train_bf16(*p, 1, 4, 1, 1, 128, 128, None) == binding.ERR_UNSUPPORTED
+    assert lib.m2rnn_forward_train_bf16(*p, 1, 4, 1, 1, 24, 64, None) == binding.ERR_UNSUPPORTED
+    assert lib.m2rnn_forward_train_bf16(*p, 1, 4, 1, 1, 64, 96, None) == binding.ERR_UNSUPPORTED
 
 
 def test_decode_argument_checks(lib):
@@ -186,7 +187,8 @@ def test_decode_argument_checks(lib):
     pp[9] = None                                   # H_out
     assert lib.m2rnn_decode_step_bf16(*pp, 2, 3, 3, 64, 64, None) == binding.ERR_INVALID_ARG
     assert lib.m2rnn_decode_step_bf16(*p, 2, 3, 3, 24, 64, None) == binding.ERR_UNSUPPORTED
-    assert lib.m2rnn_decode_step_bf16(*p, 2, 3, 3, 64, 128, None) == binding.ERR_UNSUPPORTED
+    assert lib.m2rnn_decode_step_bf16(*p, 2, 3, 3, 64, 96, None) == binding.ERR_UNSUPPORTED
+    assert lib.m2rnn_decode_step_bf16(*p, 2, 3, 3, 144, 128, None) == binding.ERR_UNSUPPORTED
     assert lib.m2rnn_decode_step_bf16(*p, 2, 3, 2, 64, 64, None) == binding.ERR_INVALID_ARG
 
 

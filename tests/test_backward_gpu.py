@@ -102,13 +102,16 @@ def test_backward_without_dHT_and_without_dH0():
 
 
 def test_forward_train_keeps_states_and_matches_plain_forward():
-    for dtype, shape in [("f32", (2, 37, 3, 8, 24)), ("bf16", (2, 150, 3, 64, 64)),
-                         ("bf16", (1, 70, 2, 32, 16))]:
+    # bf16 with V = 128 keeps the states through the row-warp kernel (forward variant 1)
+    for dtype, shape, fwd_variant in [("f32", (2, 37, 3, 8, 24), 0), ("bf16", (2, 150, 3, 64, 64), 0),
+                                      ("bf16", (1, 70, 2, 32, 16), 0),
+                                      ("bf16", (2, 45, 2, 64, 128), 1),
+                                      ("bf16", (1, 33, 2, 128, 128), 1)]:
         B, T, N, K, V = shape
         wl = Workload("tr", B, T, N, K, V, dtype=dtype, h0="uniform", rescale_w=dtype == "bf16")
         inp = make_inputs(wl, DEV, 7)
         y, HT, Hs = pkg.m2rnn_forward_train(inp)
-        y2, HT2 = pkg.m2rnn_forward(inp)
+        y2, HT2 = pkg.m2rnn_forward(inp, variant=fwd_variant)
         assert torch.equal(y, y2) and torch.equal(HT, HT2)     # same arithmetic, bit for bit
         assert torch.equal(Hs[:, :, T - 1], HT.to(Hs.dtype))    # bf16: round to nearest even
         _, _, states = m2rnn_forward_inputs(all_f64(inp), return_states=True)
@@ -118,7 +121,7 @@ def test_forward_train_keeps_states_and_matches_plain_forward():
 
 BF16_SHAPES = [(1, 1, 1, 16, 16), (2, 65, 3, 64, 64), (1, 130, 2, 32, 32), (2, 40, 2, 48, 16),
                (1, 1, 1, 64, 64), (1, 4, 2, 64, 64), (1, 5, 1, 64, 64), (2, 131, 2, 64, 64),
-               (1, 7, 2, 64, 64)]
+               (1, 7, 2, 64, 64), (1, 24, 2, 64, 128), (1, 12, 1, 128, 128), (1, 10, 2, 96, 128)]
 
 
 def bwd_variants(K, V):

@@ -48,7 +48,8 @@ def test_decode_steps_reproduce_the_forward_bitwise(shape, shared):
     assert torch.equal(H, H_ref)
 
 
-@pytest.mark.parametrize("shape", [(2, 5, 3, 128, 64), (4, 3, 2, 112, 16)])
+@pytest.mark.parametrize("shape", [(2, 5, 3, 128, 64), (4, 3, 2, 112, 16), (2, 6, 3, 64, 128),
+                                   (2, 4, 2, 128, 128), (1, 3, 1, 32, 128)])
 def test_decode_large_K_matches_oracle(shape):
     B, T, N, K, V = shape
     inp = make_inputs(Workload("decK", B, T, N, K, V, h0="uniform"), DEV, 6)
