@@ -15,10 +15,12 @@
 //   * P_t = H_{t-1} W, up to three steps ahead of the scan (kept state tile, W^T tile).
 // Eight compute warps each own a 16-row block (the tensor-memory lane quarter of their
 // sub-partition) and a 32-column half.  The halves never exchange data: the chain product
-// reads all of D_t from shared memory.  Within a step a warp first does the work that only
-// needs P_t (rank-1 term, tanh, 1 - Z^2, H_{t-1} - Z, dq), then waits for G_{t+1}, forms
-// R_t, D_t and f_t R_t, writes D_t^T and signals, and reduces dk, dv and dL/df while the
-// tensor core computes the next chain product.
+// reads all of D_t from shared memory.  Within a step a warp first loads the step's shared
+// operands and forms dq (neither waits for the tensor core), then does the work that only
+// needs P_t (rank-1 term, tanh, 1 - Z^2, H_{t-1} - Z), then waits for G_{t+1}, forms R_t,
+// D_t and f_t R_t, writes D_t^T and signals, and reduces dk, dv and dL/df while the tensor
+// core computes the next chain product.  Arrives and duplicated stores are predicated or
+// done by every lane rather than branched, so the step's code stays in few basic blocks.
 //
 // Roles: warps 0-7 compute, warp 8 producer (TMA, gates, per-chunk dv, dk, dq, da, dalpha,
 // dbeta, dw_r), warp 9 tensor-core issuer (one thread).  mbarriers: full (TMA), done
@@ -450,6 +452,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float4 gt = gates[st * kTc + s];
         const float2 ff = make_float2(gt.x, gt.x), gg = make_float2(gt.y, gt.y);
 
+        // ---- shared-memory operands of the step (the stage is resident), and dq_t
+        const float kv0 = bf16_bits_to_float(ks[s * kK + r0]);
+        const float kv1 = bf16_bits_to_float(ks[s * kK + r1]);
+        const float2 k0 = make_float2(kv0, kv0), k1 = make_float2(kv1, kv1);
+        const float qv0 = bf16_bits_to_float(qs[s * kK + r0]);
+        const float qv1 = bf16_bits_to_float(qs[s * kK + r1]);
+        const float2 q0 = make_float2(qv0, qv0), q1 = make_float2(qv1, qv1);
+        float2 vv[4], uu[4];
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+          vv[nt] = bf16x2_to_float2(
+              *reinterpret_cast<const uint32_t*>(vs + s * kV + c0 + 8 * nt + 2 * c));
+          uu[nt] = *reinterpret_cast<const float2*>(dys + s * kV + c0 + 8 * nt + 2 * c);
+        }
+        uint32_t ah[2][4];  // H_{t-1}, this half's two k-tiles
+#pragma unroll
+        for (int q2 = 0; q2 < 2; ++q2)
+          ldsm_x4(ah[q2], sw128_addr(hprev, 16 * rb + lr + 8 * (lq & 1), 4 * ch + 2 * q2 + (lq >> 1)));
+        float2 sq0 = make_float2(0.f, 0.f), sq1 = make_float2(0.f, 0.f);
+        {
+          uint32_t hc[2][4];
+#pragma unroll
+          for (int q2 = 0; q2 < 2; ++q2)
+            ldsm_x4(hc[q2], sw128_addr(hcur, 16 * rb + lr + 8 * (lq & 1), 4 * ch + 2 * q2 + (lq >> 1)));
+#pragma unroll
+          for (int nt = 0; nt < 4; ++nt) {
+            sq0 = fma2(bf16x2_to_float2(hc[nt >> 1][2 * (nt & 1)]), uu[nt], sq0);
+            sq1 = fma2(bf16x2_to_float2(hc[nt >> 1][2 * (nt & 1) + 1]), uu[nt], sq1);
+          }
+        }
         // ---- P_t (this half's 32 columns) from tensor memory, + k_t v_t^T
         const int slot = u % kS;
         ok = wait_or_abort(&Bs.pready[slot], (uint32_t)(u / kS) & 1u, limit, Bs.abort_flag);
@@ -460,22 +492,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&Bs.pfree[slot]);
-        const float kv0 = bf16_bits_to_float(ks[s * kK + r0]);
-        const float kv1 = bf16_bits_to_float(ks[s * kK + r1]);
-        const float2 k0 = make_float2(kv0, kv0), k1 = make_float2(kv1, kv1);
-        float2 vv[4], uu[4];
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt) {
-          vv[nt] = bf16x2_to_float2(
-              *reinterpret_cast<const uint32_t*>(vs + s * kV + c0 + 8 * nt + 2 * c));
-          uu[nt] = *reinterpret_cast<const float2*>(dys + s * kV + c0 + 8 * nt + 2 * c);
-        }
-        // ---- what needs only P_t: 1 - Z^2 and H_{t-1} - Z
-        uint32_t ah[2][4];  // H_{t-1}, this half's two k-tiles
-#pragma unroll
-        for (int q2 = 0; q2 < 2; ++q2)
-          ldsm_x4(ah[q2], sw128_addr(hprev, 16 * rb + lr + 8 * (lq & 1), 4 * ch + 2 * q2 + (lq >> 1)));
+        mbar_arrive_if(lane == 0, &Bs.pfree[slot]);
         float2 omz[4][2], hmz[4][2];
         const float2 one = make_float2(1.f, 1.f);
 #pragma unroll
@@ -490,26 +507,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             omz[nt][r] = fma2(make_float2(-z.x, -z.y), z, one);
             hmz[nt][r] = make_float2(h.x - z.x, h.y - z.y);
           }
-        // ---- dq_t = H_t u_t (this half's columns)
-        float2 sq0 = make_float2(0.f, 0.f), sq1 = make_float2(0.f, 0.f);
-        {
-          uint32_t hc[2][4];
-#pragma unroll
-          for (int q2 = 0; q2 < 2; ++q2)
-            ldsm_x4(hc[q2], sw128_addr(hcur, 16 * rb + lr + 8 * (lq & 1), 4 * ch + 2 * q2 + (lq >> 1)));
-#pragma unroll
-          for (int nt = 0; nt < 4; ++nt) {
-            sq0 = fma2(bf16x2_to_float2(hc[nt >> 1][2 * (nt & 1)]), uu[nt], sq0);
-            sq1 = fma2(bf16x2_to_float2(hc[nt >> 1][2 * (nt & 1) + 1]), uu[nt], sq1);
-          }
-        }
-        if (u >= 2) {  // the products of step u - 2 have finished reading this D^T slot
-          ok = wait_or_abort(&Bs.dtfree[u & 1], (uint32_t)((u >> 1) - 1) & 1u, limit,
-                             Bs.abort_flag);
-          if (!ok) break;
-          tc_fence_after();
-        }
-        // ---- the chain: C_t = f_{t+1} R_{t+1} + G_{t+1}
+        // ---- the chain: C_t = f_{t+1} R_{t+1} + G_{t+1}.  G_{t+1} was committed after the
+        // dW product of step u - 2 was issued, and a commit completes only when every earlier
+        // product has: so it also guarantees that this step's D^T slot has been read.
         if (u >= 1) {
           ok = wait_or_abort(&Bs.gready[(u - 1) & 1], (uint32_t)((u - 1) >> 1) & 1u, limit,
                              Bs.abort_flag);
@@ -526,9 +526,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                   __uint_as_float(gr[4 * nt + 3])));
           }
         }
-        const float qv0 = bf16_bits_to_float(qs[s * kK + r0]);
-        const float qv1 = bf16_bits_to_float(qs[s * kK + r1]);
-        const float2 q0 = make_float2(qv0, qv0), q1 = make_float2(qv1, qv1);
         float2 Dm[4][2];
         float2 dfl2 = make_float2(0.f, 0.f);
 #pragma unroll
@@ -558,7 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&Bs.dtready[u & 1]);
+        mbar_arrive_if(lane == 0, &Bs.dtready[u & 1]);
 
         // ---- off the chain: dk_t = D_t v_t, dv partial D_t^T k_t, dL/df_t, dq_t
         float2 sk0 = make_float2(0.f, 0.f), sk1 = make_float2(0.f, 0.f);
@@ -587,7 +584,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float dfl = dfl2.x + dfl2.y;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) dfl += __shfl_xor_sync(0xffffffffu, dfl, o);
-        if (lane == 0) dfp[(st * kCW + warp) * kTc + s] = dfl;
+        dfp[(st * kCW + warp) * kTc + s] = dfl;  // the same value on every lane
         float k0s = sk0.x + sk0.y, k1s = sk1.x + sk1.y;
         float q0s = sq0.x + sq0.y, q1s = sq1.x + sq1.y;
 #pragma unroll
@@ -597,7 +594,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           q0s += __shfl_xor_sync(0xffffffffu, q0s, o);
           q1s += __shfl_xor_sync(0xffffffffu, q1s, o);
         }
-        if (c == 0) {
+        {  // the four lanes of a row hold the same sums
           float* pk = dkqp + ((st * 2 + ch) * 2 * kTc + s) * kK;
           float* pq = pk + kTc * kK;
           pk[r0] = k0s;

@@ -206,6 +206,14 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// mbarrier arrive issued only where `pred` holds, predicated rather than branched.
+__device__ __forceinline__ void mbar_arrive_if(bool pred, uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %1, 0;\n\t"
+      "@p mbarrier.arrive.shared::cta.b64 _, [%0];\n\t}" ::"r"(smem_u32(bar)), "r"((int)pred)
+      : "memory");
+}
+
 // Bounded wait that also gives up early once another warp has raised `abort`.
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, long long limit,
                                               volatile int* abort) {
