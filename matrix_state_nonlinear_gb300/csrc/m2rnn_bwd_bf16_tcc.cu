@@ -482,11 +482,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             sq1 = fma2(bf16x2_to_float2(hc[nt >> 1][2 * (nt & 1) + 1]), uu[nt], sq1);
           }
         }
-        // ---- P_t (this half's 32 columns) from tensor memory, + k_t v_t^T
+        // ---- P_t (this half's 32 columns) from tensor memory, + k_t v_t^T.  From step 2 on
+        // P_t is complete already: it was issued before the chain product of step u - 2,
+        // whose commit the previous step waited for.
         const int slot = u % kS;
-        ok = wait_or_abort(&Bs.pready[slot], (uint32_t)(u / kS) & 1u, limit, Bs.abort_flag);
-        if (!ok) break;
-        tc_fence_after();
+        if (u < 2) {
+          ok = wait_or_abort(&Bs.pready[slot], (uint32_t)(u / kS) & 1u, limit, Bs.abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+        }
         uint32_t pr[16];
         tmem_ld_16x256b_x4(t_lanes + (uint32_t)(64 * slot + c0), pr);
         tmem_wait_ld();
