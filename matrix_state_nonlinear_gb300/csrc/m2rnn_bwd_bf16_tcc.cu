@@ -450,7 +450,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t hprev = hprev_tile(st, s, p);
         const uint32_t hcur = sbase + L.hs + (st * kStageTiles + s + 1) * kTile;
         const float4 gt = gates[st * kTc + s];
-        const float2 ff = make_float2(gt.x, gt.x), gg = make_float2(gt.y, gt.y);
+        // ff = f_t; ngg = -(1 - f_t), paired with Z^2 - 1 below (one fma, no negation)
+        const float2 ff = make_float2(gt.x, gt.x), ngg = make_float2(-gt.y, -gt.y);
 
         // ---- shared-memory operands of the step (the stage is resident), and dq_t
         const float kv0 = bf16_bits_to_float(ks[s * kK + r0]);
@@ -497,8 +498,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         mbar_arrive_if(lane == 0, &Bs.pfree[slot]);
-        float2 omz[4][2], hmz[4][2];
-        const float2 one = make_float2(1.f, 1.f);
+        float2 zz1[4][2], hmz[4][2];  // Z^2 - 1 and H_{t-1} - Z
+        const float2 mone = make_float2(-1.f, -1.f);
 #pragma unroll
         for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
@@ -508,8 +509,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                __uint_as_float(pr[4 * nt + 2 * r + 1])));
             const float2 z = make_float2(tanh_mufu(pv.x), tanh_mufu(pv.y));
             const float2 h = bf16x2_to_float2(ah[nt >> 1][2 * (nt & 1) + r]);
-            omz[nt][r] = fma2(make_float2(-z.x, -z.y), z, one);
-            hmz[nt][r] = make_float2(h.x - z.x, h.y - z.y);
+            zz1[nt][r] = fma2(z, z, mone);
+            hmz[nt][r] = sub2(h, z);
           }
         // ---- the chain: C_t = f_{t+1} R_{t+1} + G_{t+1}.  G_{t+1} was committed after the
         // dW product of step u - 2 was issued, and a commit completes only when every earlier
@@ -537,7 +538,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int r = 0; r < 2; ++r) {
             const float2 R = fma2(r ? q1 : q0, uu[nt], C[nt][r]);
-            Dm[nt][r] = mul2(mul2(gg, R), omz[nt][r]);
+            Dm[nt][r] = mul2(mul2(ngg, R), zz1[nt][r]);  // (1 - f) R (1 - Z^2)
             dfl2 = fma2(R, hmz[nt][r], dfl2);
             C[nt][r] = mul2(ff, R);
           }

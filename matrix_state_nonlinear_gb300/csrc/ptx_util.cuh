@@ -188,6 +188,11 @@ __device__ __forceinline__ float2 add2(float2 a, float2 b) {
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2_as_u64(a)), "l"(f2_as_u64(b)));
   return u64_as_f2(d);
 }
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2_as_u64(a)), "l"(f2_as_u64(b)));
+  return u64_as_f2(d);
+}
 __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t u) {
   return make_float2(bf16_lo(u), bf16_hi(u));
 }
