@@ -498,7 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         mbar_arrive_if(lane == 0, &Bs.pfree[slot]);
-        float2 zz1[4][2], hmz[4][2];  // Z^2 - 1 and H_{t-1} - Z
+        float2 zz1[4][2], hmz[4][2], R[4][2];
         const float2 mone = make_float2(-1.f, -1.f);
 #pragma unroll
         for (int nt = 0; nt < 4; ++nt)
@@ -509,12 +509,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                __uint_as_float(pr[4 * nt + 2 * r + 1])));
             const float2 z = make_float2(tanh_mufu(pv.x), tanh_mufu(pv.y));
             const float2 h = bf16x2_to_float2(ah[nt >> 1][2 * (nt & 1) + r]);
-            zz1[nt][r] = fma2(z, z, mone);
+            zz1[nt][r] = mul2(ngg, fma2(z, z, mone));  // (1 - f_t) (1 - Z^2)
             hmz[nt][r] = sub2(h, z);
+            R[nt][r] = fma2(r ? q1 : q0, uu[nt], C[nt][r]);  // q_t u_t^T + f_{t+1} R_{t+1}
           }
-        // ---- the chain: C_t = f_{t+1} R_{t+1} + G_{t+1}.  G_{t+1} was committed after the
-        // dW product of step u - 2 was issued, and a commit completes only when every earlier
-        // product has: so it also guarantees that this step's D^T slot has been read.
+        // ---- the chain: R_t = q_t u_t^T + C_t, with C_t = f_{t+1} R_{t+1} + G_{t+1} (the part
+        // without G is formed above).  G_{t+1} was committed after the dW product of step u - 2
+        // was issued, and a commit completes only when every earlier product has: so it also
+        // guarantees that this step's D^T slot has been read.
         if (u >= 1) {
           ok = wait_or_abort(&Bs.gready[(u - 1) & 1], (uint32_t)((u - 1) >> 1) & 1u, limit,
                              Bs.abort_flag);
@@ -525,23 +527,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_wait_ld();
 #pragma unroll
           for (int nt = 0; nt < 4; ++nt) {
-            C[nt][0] = add2(C[nt][0], make_float2(__uint_as_float(gr[4 * nt]),
+            R[nt][0] = add2(R[nt][0], make_float2(__uint_as_float(gr[4 * nt]),
                                                   __uint_as_float(gr[4 * nt + 1])));
-            C[nt][1] = add2(C[nt][1], make_float2(__uint_as_float(gr[4 * nt + 2]),
+            R[nt][1] = add2(R[nt][1], make_float2(__uint_as_float(gr[4 * nt + 2]),
                                                   __uint_as_float(gr[4 * nt + 3])));
           }
         }
         float2 Dm[4][2];
-        float2 dfl2 = make_float2(0.f, 0.f);
 #pragma unroll
         for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-          for (int r = 0; r < 2; ++r) {
-            const float2 R = fma2(r ? q1 : q0, uu[nt], C[nt][r]);
-            Dm[nt][r] = mul2(mul2(ngg, R), zz1[nt][r]);  // (1 - f) R (1 - Z^2)
-            dfl2 = fma2(R, hmz[nt][r], dfl2);
-            C[nt][r] = mul2(ff, R);
-          }
+          for (int r = 0; r < 2; ++r) Dm[nt][r] = mul2(R[nt][r], zz1[nt][r]);  // D_t
         // ---- D_t^T (this warp's 16 rows x 32 columns) to the shared tile, then signal
         uint32_t ad[2][4];
 #pragma unroll
@@ -562,7 +558,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         mbar_arrive_if(lane == 0, &Bs.dtready[u & 1]);
 
-        // ---- off the chain: dk_t = D_t v_t, dv partial D_t^T k_t, dL/df_t, dq_t
+        // ---- off the chain: f_t R_t (the next C without G), dL/df_t, dk_t = D_t v_t, dv partial
+        float2 dfl2 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            dfl2 = fma2(R[nt][r], hmz[nt][r], dfl2);
+            C[nt][r] = mul2(ff, R[nt][r]);
+          }
         float2 sk0 = make_float2(0.f, 0.f), sk1 = make_float2(0.f, 0.f);
         float pdv[8];
 #pragma unroll
