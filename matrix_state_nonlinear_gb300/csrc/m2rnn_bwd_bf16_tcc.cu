@@ -594,22 +594,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) dfl += __shfl_xor_sync(0xffffffffu, dfl, o);
         dfp[(st * kCW + warp) * kTc + s] = dfl;  // the same value on every lane
-        float k0s = sk0.x + sk0.y, k1s = sk1.x + sk1.y;
-        float q0s = sq0.x + sq0.y, q1s = sq1.x + sq1.y;
-#pragma unroll
-        for (int o = 1; o <= 2; o <<= 1) {
-          k0s += __shfl_xor_sync(0xffffffffu, k0s, o);
-          k1s += __shfl_xor_sync(0xffffffffu, k1s, o);
-          q0s += __shfl_xor_sync(0xffffffffu, q0s, o);
-          q1s += __shfl_xor_sync(0xffffffffu, q1s, o);
-        }
-        {  // the four lanes of a row hold the same sums
+        // dk (rows r0, r1) and dq (rows r0, r1): reduce-scatter the four sums over the lane
+        // quad, so that lane c ends with dk r0, dk r1, dq r0, dq r1 for c = 0 .. 3.
+        {
+          const float k0s = sk0.x + sk0.y, k1s = sk1.x + sk1.y;
+          const float q0s = sq0.x + sq0.y, q1s = sq1.x + sq1.y;
+          const bool hi2 = (c & 2) != 0, hi1 = (c & 1) != 0;
+          float a0 = hi2 ? q0s : k0s, a1 = hi2 ? q1s : k1s;
+          a0 += __shfl_xor_sync(0xffffffffu, hi2 ? k0s : q0s, 2);
+          a1 += __shfl_xor_sync(0xffffffffu, hi2 ? k1s : q1s, 2);
+          float bsum = hi1 ? a1 : a0;
+          bsum += __shfl_xor_sync(0xffffffffu, hi1 ? a0 : a1, 1);
           float* pk = dkqp + ((st * 2 + ch) * 2 * kTc + s) * kK;
-          float* pq = pk + kTc * kK;
-          pk[r0] = k0s;
-          pk[r1] = k1s;
-          pq[r0] = q0s;
-          pq[r1] = q1s;
+          (hi2 ? pk + kTc * kK : pk)[hi1 ? r1 : r0] = bsum;
         }
       }
       if (!ok) break;
