@@ -35,7 +35,9 @@ def step_args(inp, t):
 
 
 @pytest.mark.parametrize("shape,shared", [((2, 37, 3, 64, 64), False), ((3, 20, 2, 32, 16), False),
-                                          ((2, 9, 4, 48, 32), True), ((1, 70, 2, 16, 64), False)])
+                                          ((2, 9, 4, 48, 32), True), ((1, 70, 2, 16, 64), False),
+                                          ((96, 3, 8, 64, 64), False), ((40, 2, 16, 32, 16), True),
+                                          ((70, 2, 9, 48, 32), False)])
 def test_decode_steps_reproduce_the_forward_bitwise(shape, shared):
     B, T, N, K, V = shape
     inp = make_inputs(Workload("dec", B, T, N, K, V, h0="uniform", shared_qk=shared), DEV, 5)
