@@ -72,8 +72,8 @@ __host__ __device__ inline Layout layout_tcc() {
   o += kStages * L.in_stage;
   L.gates = o;                     // float4 [kStages][kTc]: f, 1 - f, sigmoid(a + beta), softplus
   o += kStages * kTc * 16;
-  L.dfp = o;                       // float [kStages][kCW][kTc]: dL/df partials
-  o += kStages * kCW * kTc * 4;
+  L.dfp = o;                       // float [kStages][kCW][kTc][8]: dL/df partials (per lane & 7)
+  o += kStages * kCW * kTc * 8 * 4;
   L.dvp = o;                       // float [kStages][kNW][kTc][kV]: dv partials per row block
   o += kStages * kNW * kTc * kV * 4;
   L.dkqp = o;                      // float [kStages][2 halves][dk, dq][kTc][kK]
@@ -309,10 +309,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         *reinterpret_cast<float2*>(dqo + qrow * kK + 2 * lane) =
             make_float2(q0v.x + q1v.x, q0v.y + q1v.y);
       }
-      if (lane < steps) {  // da_t, and the sums for dalpha, dbeta
-        float df = 0.f;
+      // dL/df_t: the 8 warps' 8 partials of each step, summed by the whole warp; lane s keeps
+      // step s's total.
+      float df = 0.f;
+      for (int s = 0; s < steps; ++s) {
+        const int w = lane >> 2, j = 2 * (lane & 3);
+        const float2 pp = *reinterpret_cast<const float2*>(dfp + ((st * kCW + w) * kTc + s) * 8 + j);
+        float sum = pp.x + pp.y;
 #pragma unroll
-        for (int w = 0; w < kCW; ++w) df += dfp[(st * kCW + w) * kTc + lane];
+        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        if (lane == s) df = sum;
+      }
+      if (lane < steps) {  // da_t, and the sums for dalpha, dbeta
         const float4 gt = gates[st * kTc + lane];
         const float d_a = df * (-al * gt.x * gt.z);
         da[((size_t)b * T + t0 + lane) * N + n] = d_a;
@@ -590,10 +598,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // Lane (g, c) holds column c0 + 8 (g >> 1) + 2c + (g & 1).
         dvp[((st * kNW + rb) * kTc + s) * kV + c0 + 8 * (g >> 1) + 2 * c + (g & 1)] = pdv[0];
+        // dL/df_t partial: summed over lane bits 4 and 3 only; lanes that agree in bits 0-2
+        // hold the same value and store it together (the producer adds the rest).
         float dfl = dfl2.x + dfl2.y;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) dfl += __shfl_xor_sync(0xffffffffu, dfl, o);
-        dfp[(st * kCW + warp) * kTc + s] = dfl;  // the same value on every lane
+        dfl += __shfl_xor_sync(0xffffffffu, dfl, 16);
+        dfl += __shfl_xor_sync(0xffffffffu, dfl, 8);
+        dfp[((st * kCW + warp) * kTc + s) * 8 + (lane & 7)] = dfl;
         // dk (rows r0, r1) and dq (rows r0, r1): reduce-scatter the four sums over the lane
         // quad, so that lane c ends with dk r0, dk r1, dq r0, dq r1 for c = 0 .. 3.
         {
