@@ -7,8 +7,10 @@
 //   R_t = C_t + q_t u_t^T,  D_t = ((1 - f_t) R_t) ⊙ (1 - Z_t^2),
 //   C_{t-1} = f_t R_t + D_t W^T,  dW += H_{t-1}^T D_t,
 //   dk_t = D_t v_t,  dv_t = D_t^T k_t + w_r ⊙ u_t,  dq_t = H_t u_t,  dL/df_t = <R_t, H_{t-1} - Z_t>.
-// One thread issues three tcgen05.mma products per step (M = N = 64, four K = 16 steps,
-// fp32 accumulators in tensor memory):
+// The issuer warp puts three tcgen05.mma products per step on the tensor core (M = N = 64,
+// four K = 16 steps, fp32 accumulators in tensor memory).  The whole warp runs the issuing
+// loop, so the descriptors stay warp-uniform, and one elected lane issues each MMA and
+// commit (an issuer in a one-lane branch issued ~1.6x slower):
 //   * G_t = D_t W^T, the chain product, as soon as every compute warp has written its part
 //     of D_t^T (A = the D_t^T tile read M-major, B = the W^T tile read N-major);
 //   * dW += H_{t-1}^T D_t into one accumulator over the whole sequence (same D_t^T tile);
@@ -21,9 +23,11 @@
 // D_t and f_t R_t, writes D_t^T and signals, and reduces dk, dv and dL/df while the tensor
 // core computes the next chain product.  Arrives and duplicated stores are predicated or
 // done by every lane rather than branched, so the step's code stays in few basic blocks.
+// Waits that a commit already implies are skipped: a commit completes only when every
+// earlier product of the issuing thread has.
 //
-// Roles: warps 0-7 compute, warp 8 producer (TMA, gates, per-chunk dv, dk, dq, da, dalpha,
-// dbeta, dw_r), warp 9 tensor-core issuer (one thread).  mbarriers: full (TMA), done
+// Roles: warps 0-7 compute, warp 8 producer (TMA, gates, per-chunk dv, dk, dq, da, dL/df
+// sums, dalpha, dbeta, dw_r), warp 9 tensor-core issuer.  mbarriers: full (TMA), done
 // (compute warps finished a chunk), mmadone (the chunk's products finished), pready /
 // pfree (P slots), dtready / dtfree (D^T slots), gready (G slots).  Every wait is bounded.
 #include <cuda_bf16.h>

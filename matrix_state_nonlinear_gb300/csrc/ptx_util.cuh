@@ -66,20 +66,12 @@ __device__ __forceinline__ void tma_load_4d(void* smem_dst, const CUtensorMap* m
       : "memory");
 }
 
-// Stores one box of a 4-D tensor map from shared memory (bulk async-group completion).
-__device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, uint32_t smem_src, int c0,
-                                             int c1, int c2, int c3) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
-          reinterpret_cast<uint64_t>(map)),
-      "r"(smem_src), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
-      : "memory");
-}
 __device__ __forceinline__ void bulk_commit_group() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
-// tma_store_4d issued only where `pred` holds, as a predicated instruction rather than a
-// branch (a warp can call it converged, keeping the caller's code one basic block).
+// Stores one box of a 4-D tensor map from shared memory (bulk async-group completion), issued
+// only where `pred` holds: a predicated instruction rather than a branch, so a converged warp
+// can call it and keep the caller's code one basic block.
 __device__ __forceinline__ void tma_store_4d_if(bool pred, const CUtensorMap* map,
                                                 uint32_t smem_src, int c0, int c1, int c2, int c3) {
   asm volatile(
