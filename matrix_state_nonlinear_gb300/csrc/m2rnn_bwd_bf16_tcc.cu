@@ -7,29 +7,34 @@
 //   R_t = C_t + q_t u_t^T,  D_t = ((1 - f_t) R_t) ⊙ (1 - Z_t^2),
 //   C_{t-1} = f_t R_t + D_t W^T,  dW += H_{t-1}^T D_t,
 //   dk_t = D_t v_t,  dv_t = D_t^T k_t + w_r ⊙ u_t,  dq_t = H_t u_t,  dL/df_t = <R_t, H_{t-1} - Z_t>.
-// The issuer warp puts three tcgen05.mma products per step on the tensor core (M = N = 64,
+// The issuer warp puts three tcgen05.mma products per step on the tensor core (M = 64,
 // four K = 16 steps, fp32 accumulators in tensor memory).  The whole warp runs the issuing
 // loop, so the descriptors stay warp-uniform, and one elected lane issues each MMA and
 // commit (an issuer in a one-lane branch issued ~1.6x slower):
 //   * G_t = D_t W^T, the chain product, as soon as every compute warp has written its part
 //     of D_t^T (A = the D_t^T tile read M-major, B = the W^T tile read N-major);
 //   * dW += H_{t-1}^T D_t into one accumulator over the whole sequence (same D_t^T tile);
-//   * P_t = H_{t-1} W, up to three steps ahead of the scan (kept state tile, W^T tile).
+//   * P_t = H_{t-1} [W | u], up to two steps ahead of the scan (kept state tile; B = the W^T
+//     tile followed by 16 rows that hold u_{t-1} split into bf16 high and low parts, written
+//     by the issuer just before the product).  Columns 64 .. 79 of the result give
+//     dq_{t-1} = H_{t-1} u_{t-1} with fp32 accuracy in u; dq_{T-1} comes from one extra
+//     N = 16 product on H_{T-1} at the start.
 // Eight compute warps each own a 16-row block (the tensor-memory lane quarter of their
 // sub-partition) and a 32-column half.  The halves never exchange data: the chain product
 // reads all of D_t from shared memory.  Within a step a warp first loads the step's shared
-// operands and forms dq (neither waits for the tensor core), then does the work that only
-// needs P_t (rank-1 term, tanh, 1 - Z^2, H_{t-1} - Z), then waits for G_{t+1}, forms R_t,
-// D_t and f_t R_t, writes D_t^T and signals, and reduces dk, dv and dL/df while the tensor
-// core computes the next chain product.  Arrives and duplicated stores are predicated or
-// done by every lane rather than branched, so the step's code stays in few basic blocks.
-// Waits that a commit already implies are skipped: a commit completes only when every
-// earlier product of the issuing thread has.
+// operands (no wait for the tensor core), then does the work that only needs P_t (rank-1
+// term, tanh, 1 - Z^2, H_{t-1} - Z; dq_{t-1} read from the same slot), then waits for
+// G_{t+1}, forms R_t, D_t and f_t R_t, writes D_t^T and signals, and reduces dk, dv and
+// dL/df while the tensor core computes the next chain product.  Arrives and duplicated
+// stores are predicated or done by every lane rather than branched, so the step's code
+// stays in few basic blocks.  Waits that a commit already implies are skipped: a commit
+// completes only when every earlier product of the issuing thread has.
 //
 // Roles: warps 0-7 compute, warp 8 producer (TMA, gates, per-chunk dv, dk, dq, da, dL/df
 // sums, dalpha, dbeta, dw_r), warp 9 tensor-core issuer.  mbarriers: full (TMA), done
 // (compute warps finished a chunk), mmadone (the chunk's products finished), pready /
-// pfree (P slots), dtready / dtfree (D^T slots), gready (G slots).  Every wait is bounded.
+// pfree (P slots), dtready / dtfree (D^T slots), gready (G slots), qdone (the dq_{T-1}
+// product).  Every wait is bounded.
 #include <cuda_bf16.h>
 
 #include "m2rnn_internal.h"
@@ -43,17 +48,20 @@ constexpr int kNW = 4;                   // 16-row blocks
 constexpr int kCW = 8;                   // compute warps: row block w % 4, column half w / 4
 constexpr int kProducer = kCW, kIssuer = kCW + 1;
 constexpr int kThreads = 32 * (kCW + 2);
-constexpr int kTc = 8;                   // steps per chunk
+constexpr int kTc = 8;                   // steps per chunk (= the 8 u rows: t0 % 8 == 0)
+static_assert(kTc == 8, "the u rows of the P product are indexed by t % 8");
 constexpr int kStages = 2;               // chunk stages in flight (TMA ring)
-constexpr int kS = 4;                    // P slots in tensor memory (issue up to kS - 1 ahead)
+constexpr int kS = 3;                    // P slots in tensor memory (issue up to kS - 1 ahead)
 constexpr int kTile = kK * kV * 2;       // one bf16 64 x 64 tile (64 rows of 128 bytes)
 constexpr int kStageTiles = kTc + 1;     // states t0 - 1 .. t0 + Tc - 1
+constexpr int kPN = kV + 16;             // P product width: W's 64 columns + 16 columns of u
+constexpr uint32_t kPCols = 96;          // tensor-memory columns per P slot
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kDwCol = 256;         // P slots: columns 0 .. 255; dW: 256 .. 319
-constexpr uint32_t kGCol = 320;          // G slots: 320 .. 447
+constexpr uint32_t kDwCol = kS * kPCols; // P slots: columns 0 .. 287; dW: 288 .. 351
+constexpr uint32_t kGCol = kDwCol + 64;  // G slots: 352 .. 479
 
 struct Layout {
-  int hs, h0t, wt, dt, in, in_stage, qs, ks, vs, dys, gates, dfp, dvp, dkqp, bar, total;
+  int hs, h0t, wt, dt, in, in_stage, qs, ks, vs, dys, gates, dfp, dvp, dkp, dqp, bar, total;
 };
 
 __host__ __device__ inline Layout layout_tcc() {
@@ -63,8 +71,8 @@ __host__ __device__ inline Layout layout_tcc() {
   o += kStages * kStageTiles * kTile;
   L.h0t = o;                       // bf16(H_0): the state before step 0
   o += kTile;
-  L.wt = o;                        // W^T: row j holds W[0..63][j]
-  o += kTile;
+  L.wt = o;                        // W^T: row j holds W[0..63][j]; rows 64 .. 79 follow it:
+  o += kTile + 2 * 1024;           // u_tau split as bf16 hi (row 64 + tau % 8) + lo (row 72 + ...)
   L.dt = o;                        // D_t^T, two slots: row j holds D_t[0..63][j]
   o += 2 * kTile;
   L.qs = 0;                        // per-stage inputs: q, k, v (bf16), dy (fp32)
@@ -80,8 +88,10 @@ __host__ __device__ inline Layout layout_tcc() {
   o += kStages * kCW * kTc * 8 * 4;
   L.dvp = o;                       // float [kStages][kNW][kTc][kV]: dv partials per row block
   o += kStages * kNW * kTc * kV * 4;
-  L.dkqp = o;                      // float [kStages][2 halves][dk, dq][kTc][kK]
-  o += kStages * 2 * 2 * kTc * kK * 4;
+  L.dkp = o;                       // float [kStages][2 halves][kTc][kK]: dk partials
+  o += kStages * 2 * kTc * kK * 4;
+  L.dqp = o;                       // float [kStages][kTc][kK]: dq_t
+  o += kStages * kTc * kK * 4;
   L.bar = o;
   o += 256;
   L.total = o + 1024;              // slack for aligning the base to 1024 bytes
@@ -97,6 +107,7 @@ struct Bars {
   uint64_t* dtready;  // [2]
   uint64_t* dtfree;   // [2]
   uint64_t* gready;   // [2]
+  uint64_t* qdone;    // the dq_{T-1} product
   uint64_t* never;
   volatile int* abort_flag;
   uint32_t* tmem_slot;
@@ -113,7 +124,8 @@ __device__ inline Bars bars_at(uint8_t* p) {
   B.dtready = B.pfree + kS;
   B.dtfree = B.dtready + 2;
   B.gready = B.dtfree + 2;
-  B.never = B.gready + 2;
+  B.qdone = B.gready + 2;
+  B.never = B.qdone + 1;
   B.abort_flag = reinterpret_cast<volatile int*>(B.never + 1);
   B.tmem_slot = reinterpret_cast<uint32_t*>(B.never + 2);
   return B;
@@ -165,7 +177,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   float4* gates = reinterpret_cast<float4*>(smem + L.gates);
   float* dfp = reinterpret_cast<float*>(smem + L.dfp);
   float* dvp = reinterpret_cast<float*>(smem + L.dvp);
-  float* dkqp = reinterpret_cast<float*>(smem + L.dkqp);
+  float* dkp = reinterpret_cast<float*>(smem + L.dkp);
+  float* dqp = reinterpret_cast<float*>(smem + L.dqp);
   float* wsp = ws + (size_t)pair * backward_pair_floats(kK, kV);
   float* dWp = wsp + kK * kV;
   float* dwr_p = dWp + kV * kV;
@@ -187,6 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&Bs.pready[i], 1);
       mbar_init(&Bs.pfree[i], kCW);
     }
+    mbar_init(Bs.qdone, 1);
     mbar_init(Bs.never, 1);
     *Bs.abort_flag = 0;
     fence_mbar_init();
@@ -213,6 +227,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     *reinterpret_cast<uint4*>(smem + (sw128_addr(sbase + L.h0t, row, ch) - sbase)) = hv;
   }
+  for (int e = tid; e < 16 * 8; e += kThreads)  // u rows: zero until first written
+    *reinterpret_cast<uint4*>(smem + L.wt + kTile + 16 * e) = make_uint4(0u, 0u, 0u, 0u);
   fence_proxy_async_smem();  // the tiles are read by the tensor cores
   tc_fence_before();
   __syncthreads();
@@ -297,21 +313,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t vv = *reinterpret_cast<const uint32_t*>(vs + s * kV + 2 * lane);
         dwr.x = fmaf(u.x, bf16_lo(vv), dwr.x);
         dwr.y = fmaf(u.y, bf16_hi(vv), dwr.y);
-        // dk_t, dq_t: the two column halves' partial sums; lane: rows 2 lane, +1
+        // dk_t (the two column halves' partial sums) and dq_t; lane: rows 2 lane, +1
         const size_t qrow =
             ((size_t)b * T + t0 + s) * (shared_qk ? N : Nqk) + (shared_qk ? n : nq);
         float* dqo = shared_qk ? dqk_heads : dq;
         float* dko = shared_qk ? dqk_heads + (size_t)gridDim.x * T * kK : dk;
-        const float* pk0 = dkqp + ((st * 2 + 0) * 2 * kTc + s) * kK;
-        const float* pk1 = dkqp + ((st * 2 + 1) * 2 * kTc + s) * kK;
+        const float* pk0 = dkp + ((st * 2 + 0) * kTc + s) * kK;
+        const float* pk1 = dkp + ((st * 2 + 1) * kTc + s) * kK;
         const float2 k0v = *reinterpret_cast<const float2*>(pk0 + 2 * lane);
         const float2 k1v = *reinterpret_cast<const float2*>(pk1 + 2 * lane);
-        const float2 q0v = *reinterpret_cast<const float2*>(pk0 + kTc * kK + 2 * lane);
-        const float2 q1v = *reinterpret_cast<const float2*>(pk1 + kTc * kK + 2 * lane);
         *reinterpret_cast<float2*>(dko + qrow * kK + 2 * lane) =
             make_float2(k0v.x + k1v.x, k0v.y + k1v.y);
         *reinterpret_cast<float2*>(dqo + qrow * kK + 2 * lane) =
-            make_float2(q0v.x + q1v.x, q0v.y + q1v.y);
+            *reinterpret_cast<const float2*>(dqp + (st * kTc + s) * kK + 2 * lane);
       }
       // dL/df_t: the 8 warps' 8 partials of each step, summed by the whole warp; lane s keeps
       // step s's total.
@@ -359,33 +373,79 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The whole warp runs the loop (the descriptors stay warp-uniform); one elected lane
     // issues each MMA and commit.  Wait outcomes are made warp-uniform with __all_sync.
     const bool leader = elect_one_sync();
-    const uint32_t idesc_p = umma_idesc_bf16(kK, kV, false);          // A = H (K-major), B = W^T
+    const uint32_t idesc_p = umma_idesc_bf16(kK, kPN, false);         // A = H, B = [W^T; u rows]
+    const uint32_t idesc_q = umma_idesc_bf16(kK, 16, false);          // A = H, B = the u rows
     const uint32_t idesc_w = umma_idesc_bf16(kV, kV, true);           // A = H^T (M-major view)
     const uint32_t idesc_g = umma_idesc_bf16_ab(kK, kV, true, true);  // A = D, B = W^T N-major
     const uint64_t d_wt = umma_desc(sbase + L.wt, 16, 1024, 2);       // W^T, K-major
     const uint64_t d_wn = umma_desc(sbase + L.wt, kTile, 1024, 2);    // the same tile, N-major
+    const uint64_t d_u = umma_desc(sbase + L.wt + kTile, 16, 1024, 2);  // the u rows alone
+    // u_tau (fp32, step s_u of the dy block of stage st_u) into rows 64 + tau % 8 (bf16 of u)
+    // and 72 + tau % 8 (bf16 of the remainder) of the B operand [W^T; u rows], so that the
+    // product H_{t-1} [W | u] also yields H_{t-1} u_{t-1} = dq_{t-1} to fp32 accuracy in u.
+    auto put_u = [&](int st_u, int s_u, int row) {
+      const float2 x = *reinterpret_cast<const float2*>(smem + L.in + st_u * L.in_stage + L.dys +
+                                                        (s_u * kV + 2 * lane) * 4);
+      const uint32_t hi = pack_bf16x2(x.x, x.y);
+      const float2 hf = bf16x2_to_float2(hi);
+      const uint32_t lo = pack_bf16x2(x.x - hf.x, x.y - hf.y);
+      const uint32_t off = (uint32_t)(lane & 3) * 4u - sbase;
+      *reinterpret_cast<uint32_t*>(smem + (sw128_addr(sbase + L.wt, 64 + row, lane >> 2) + off)) = hi;
+      *reinterpret_cast<uint32_t*>(smem + (sw128_addr(sbase + L.wt, 72 + row, lane >> 2) + off)) = lo;
+      fence_proxy_async_smem();
+    };
     Cursor cp{0, chunk_steps(0, nchunks, T) - 1, chunk_steps(0, nchunks, T), 0};
     Cursor cw = cp;
     bool ok = true;
     int full_seen = -1;  // chunks whose TMA completion was waited for
+    // dq_{T-1} = H_{T-1} u_{T-1}: no P product has H_{T-1} as its A operand.  Into the second
+    // G slot, which is first written by the chain product of step 1.
+    {
+      const int steps0 = chunk_steps(0, nchunks, T);
+      ok = __all_sync(0xffffffffu, wait_or_abort(&Bs.full[0], 0u, limit, Bs.abort_flag));
+      if (ok) {
+        full_seen = 0;
+        put_u(0, steps0 - 1, (T - 1) & 7);
+        __syncwarp();
+        tc_fence_after();
+        const uint64_t d_hl = umma_desc(sbase + L.hs + steps0 * kTile, 16, 1024, 2);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          umma_bf16_if(leader, tmem + kGCol + 64, d_hl + (uint64_t)((kk * 32) >> 4),
+                       d_u + (uint64_t)((kk * 32) >> 4), idesc_q, kk);
+        umma_commit_if(leader, Bs.qdone);
+      }
+    }
+    const bool q_issued = ok;
     while (ok && cw.u < T) {
       // P_t = H_{t-1} W for the steps ahead, into slot u % kS.
       while (ok && cp.u < T && cp.u < cw.u + kS) {
         const int slot = cp.u % kS;
+        // u_{t-1} sits in the next processed chunk when t is the first step of its chunk.
+        const bool cross = cp.s == 0 && cp.p + 1 < nchunks;
         bool w = true;
         if (cp.p > full_seen)
           w = wait_or_abort(&Bs.full[stage_of(cp.p)], phase_of(cp.p), limit, Bs.abort_flag);
+        if (cross && cp.p + 1 > full_seen)
+          w = w && wait_or_abort(&Bs.full[stage_of(cp.p + 1)], phase_of(cp.p + 1), limit,
+                                 Bs.abort_flag);
+        // The slot, and (as its product completed before) the u rows the product of step
+        // u - 8 read: both are free once the warps have read P of step u - kS.
         if (cp.u >= kS)
           w = w && wait_or_abort(&Bs.pfree[slot], (uint32_t)((cp.u / kS) - 1) & 1u, limit,
                                  Bs.abort_flag);
         ok = __all_sync(0xffffffffu, w);
         if (!ok) break;
-        full_seen = cp.p;
+        full_seen = cross ? cp.p + 1 : max(full_seen, cp.p);
+        if (cp.s > 0 || cross)  // t > 0: u_{t-1} into row (t - 1) % 8
+          put_u(cross ? stage_of(cp.p + 1) : stage_of(cp.p), cross ? kTc - 1 : cp.s - 1,
+                (cp.s + 7) & 7);
+        __syncwarp();
         tc_fence_after();
         const uint64_t d_h = umma_desc(hprev_tile(stage_of(cp.p), cp.s, cp.p), 16, 1024, 2);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          umma_bf16_if(leader, tmem + (uint32_t)(64 * slot), d_h + (uint64_t)((kk * 32) >> 4),
+          umma_bf16_if(leader, tmem + kPCols * (uint32_t)slot, d_h + (uint64_t)((kk * 32) >> 4),
                        d_wt + (uint64_t)((kk * 32) >> 4), idesc_p, kk);
         umma_commit_if(leader, &Bs.pready[slot]);
         cursor_next(cp, nchunks, T);
@@ -422,6 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Before the tensor memory is released every issued MMA must have finished: a commit
     // completes when all earlier MMAs of the issuing thread have, so wait for the last
     // commit of each kind (bounded).
+    if (q_issued) mbar_wait_bounded(Bs.qdone, 0u, limit);
     if (cp.u > 0)
       mbar_wait_bounded(&Bs.pready[(cp.u - 1) % kS], (uint32_t)((cp.u - 1) / kS) & 1u, limit);
     if (cw.u > 0)
@@ -448,6 +509,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     bool ok = true;
     if (debug & kDebugForceTimeout) ok = mbar_wait_bounded(Bs.never, 0u, kDebugWaitLimitCycles);
+    // dq_t of the coming step; lanes 0-15 hold rows 16 rb + lane.  First dq_{T-1}, whose
+    // product was issued before P_{T-1} (so the pready commit of step 0 covers it).
+    float dqc = 0.f;
+    if (ok) {
+      ok = wait_or_abort(&Bs.pready[0], 0u, limit, Bs.abort_flag);
+      if (ok) {
+        tc_fence_after();
+        const uint32_t col = kGCol + 64 + (uint32_t)((T - 1) & 7);
+        const uint32_t qh = tmem_ld_32x32b_x1(t_lanes + col);
+        const uint32_t ql = tmem_ld_32x32b_x1(t_lanes + col + 8);
+        tmem_wait_ld();
+        dqc = __uint_as_float(qh) + __uint_as_float(ql);
+      }
+    }
     int u = 0;
     for (int p = 0; p < nchunks && ok; ++p) {
       const int st = stage_of(p), t0 = (nchunks - 1 - p) * kTc;
@@ -460,12 +535,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float* dys = reinterpret_cast<const float*>(in + L.dys);
       for (int s = steps - 1; s >= 0 && ok; --s, ++u) {
         const uint32_t hprev = hprev_tile(st, s, p);
-        const uint32_t hcur = sbase + L.hs + (st * kStageTiles + s + 1) * kTile;
         const float4 gt = gates[st * kTc + s];
         // ff = f_t; ngg = -(1 - f_t), paired with Z^2 - 1 below (one fma, no negation)
         const float2 ff = make_float2(gt.x, gt.x), ngg = make_float2(-gt.y, -gt.y);
 
-        // ---- shared-memory operands of the step (the stage is resident), and dq_t
+        // ---- shared-memory operands of the step (the stage is resident)
         const float kv0 = bf16_bits_to_float(ks[s * kK + r0]);
         const float kv1 = bf16_bits_to_float(ks[s * kK + r1]);
         const float2 k0 = make_float2(kv0, kv0), k1 = make_float2(kv1, kv1);
@@ -483,18 +557,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int q2 = 0; q2 < 2; ++q2)
           ldsm_x4(ah[q2], sw128_addr(hprev, 16 * rb + lr + 8 * (lq & 1), 4 * ch + 2 * q2 + (lq >> 1)));
-        float2 sq0 = make_float2(0.f, 0.f), sq1 = make_float2(0.f, 0.f);
-        {
-          uint32_t hc[2][4];
-#pragma unroll
-          for (int q2 = 0; q2 < 2; ++q2)
-            ldsm_x4(hc[q2], sw128_addr(hcur, 16 * rb + lr + 8 * (lq & 1), 4 * ch + 2 * q2 + (lq >> 1)));
-#pragma unroll
-          for (int nt = 0; nt < 4; ++nt) {
-            sq0 = fma2(bf16x2_to_float2(hc[nt >> 1][2 * (nt & 1)]), uu[nt], sq0);
-            sq1 = fma2(bf16x2_to_float2(hc[nt >> 1][2 * (nt & 1) + 1]), uu[nt], sq1);
-          }
-        }
         // ---- P_t (this half's 32 columns) from tensor memory, + k_t v_t^T.  From step 2 on
         // P_t is complete already: it was issued before the chain product of step u - 2,
         // whose commit the previous step waited for.
@@ -504,9 +566,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
           tc_fence_after();
         }
+        // dq_t: the two column halves store one half of the rows each.
+        if ((lane >> 3) == ch) dqp[(st * kTc + s) * kK + 16 * rb + lane] = dqc;
         uint32_t pr[16];
-        tmem_ld_16x256b_x4(t_lanes + (uint32_t)(64 * slot + c0), pr);
+        tmem_ld_16x256b_x4(t_lanes + kPCols * (uint32_t)slot + (uint32_t)c0, pr);
+        // dq_{t-1} = H_{t-1} u_{t-1} from the u columns of the same product (hi + lo parts)
+        const uint32_t qcol = kPCols * (uint32_t)slot + kV + (uint32_t)((s + 7) & 7);
+        const uint32_t qh = tmem_ld_32x32b_x1(t_lanes + qcol);
+        const uint32_t ql = tmem_ld_32x32b_x1(t_lanes + qcol + 8);
         tmem_wait_ld();
+        dqc = __uint_as_float(qh) + __uint_as_float(ql);
         tc_fence_before();
         __syncwarp();
         mbar_arrive_if(lane == 0, &Bs.pfree[slot]);
@@ -608,19 +677,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         dfl += __shfl_xor_sync(0xffffffffu, dfl, 16);
         dfl += __shfl_xor_sync(0xffffffffu, dfl, 8);
         dfp[((st * kCW + warp) * kTc + s) * 8 + (lane & 7)] = dfl;
-        // dk (rows r0, r1) and dq (rows r0, r1): reduce-scatter the four sums over the lane
-        // quad, so that lane c ends with dk r0, dk r1, dq r0, dq r1 for c = 0 .. 3.
+        // dk (rows r0, r1): summed over the lane quad, lanes c = 0, 2 end with row r0 and
+        // c = 1, 3 with row r1 (both store: same value, same address).
         {
           const float k0s = sk0.x + sk0.y, k1s = sk1.x + sk1.y;
-          const float q0s = sq0.x + sq0.y, q1s = sq1.x + sq1.y;
-          const bool hi2 = (c & 2) != 0, hi1 = (c & 1) != 0;
-          float a0 = hi2 ? q0s : k0s, a1 = hi2 ? q1s : k1s;
-          a0 += __shfl_xor_sync(0xffffffffu, hi2 ? k0s : q0s, 2);
-          a1 += __shfl_xor_sync(0xffffffffu, hi2 ? k1s : q1s, 2);
-          float bsum = hi1 ? a1 : a0;
-          bsum += __shfl_xor_sync(0xffffffffu, hi1 ? a0 : a1, 1);
-          float* pk = dkqp + ((st * 2 + ch) * 2 * kTc + s) * kK;
-          (hi2 ? pk + kTc * kK : pk)[hi1 ? r1 : r0] = bsum;
+          const bool hi1 = (c & 1) != 0;
+          float ks2 = hi1 ? k1s : k0s;
+          ks2 += __shfl_xor_sync(0xffffffffu, hi1 ? k0s : k1s, 1);
+          ks2 += __shfl_xor_sync(0xffffffffu, ks2, 2);
+          dkp[((st * 2 + ch) * kTc + s) * kK + (hi1 ? r1 : r0)] = ks2;
         }
       }
       if (!ok) break;
