@@ -121,7 +121,10 @@ def test_forward_train_keeps_states_and_matches_plain_forward():
 
 BF16_SHAPES = [(1, 1, 1, 16, 16), (2, 65, 3, 64, 64), (1, 130, 2, 32, 32), (2, 40, 2, 48, 16),
                (1, 1, 1, 64, 64), (1, 4, 2, 64, 64), (1, 5, 1, 64, 64), (2, 131, 2, 64, 64),
-               (1, 7, 2, 64, 64), (1, 24, 2, 64, 128), (1, 12, 1, 128, 128), (1, 10, 2, 96, 128)]
+               (1, 7, 2, 64, 64), (1, 24, 2, 64, 128), (1, 12, 1, 128, 128), (1, 10, 2, 96, 128),
+               # chunk edges of the 8-step backward chunks: exactly one, one plus one step,
+               # exactly two, and a two-step sequence
+               (1, 8, 2, 64, 64), (1, 9, 1, 64, 64), (1, 16, 2, 64, 64), (2, 2, 1, 64, 64)]
 
 
 def bwd_variants(K, V):
