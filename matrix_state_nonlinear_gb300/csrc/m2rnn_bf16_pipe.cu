@@ -160,13 +160,20 @@ __global__ void __launch_bounds__(160, 1)
 
     for (int cc = 0; cc < nchunks; ++cc) {
       const int st = cc & 1;
-      if (!wait_or_abort(&done[st], (uint32_t)(cc >> 1) & 1u, limit, abort_flag)) {
+      const bool dok = kRing ? wait_or_abort(&done[st], (uint32_t)(cc >> 1) & 1u, limit, abort_flag)
+                             : wait_or_abort_sleep(&done[st], (uint32_t)(cc >> 1) & 1u, limit,
+                                                   abort_flag);
+      if (!dok) {
         if (lane == 0) {
           *abort_flag = 1;
           atomicExch(status, kStatusTimeout);
           // Let TMA copies still in flight land before the block's shared memory goes away.
           for (int ci = cc; ci < issued; ++ci)
-            mbar_wait_bounded(&full[ci & 1], (uint32_t)(ci >> 1) & 1u, kDebugWaitLimitCycles);
+            if (kRing)
+              mbar_wait_bounded(&full[ci & 1], (uint32_t)(ci >> 1) & 1u, kDebugWaitLimitCycles);
+            else
+              mbar_wait_bounded_sleep(&full[ci & 1], (uint32_t)(ci >> 1) & 1u,
+                                      kDebugWaitLimitCycles);
         }
         return;
       }
@@ -228,8 +235,11 @@ __global__ void __launch_bounds__(160, 1)
     for (int nt = 0; nt < NT; ++nt) h[nt][0] = h[nt][1] = make_float2(0.f, 0.f);
   }
 
-  bool ok = wait_or_abort(&full[0], 0u, limit, abort_flag);
-  if (debug & kDebugForceTimeout) ok = ok && mbar_wait_bounded(never, 0u, kDebugWaitLimitCycles);
+  bool ok = kRing ? wait_or_abort(&full[0], 0u, limit, abort_flag)
+                  : wait_or_abort_sleep(&full[0], 0u, limit, abort_flag);
+  if (debug & kDebugForceTimeout)
+    ok = ok && (kRing ? mbar_wait_bounded(never, 0u, kDebugWaitLimitCycles)
+                      : mbar_wait_bounded_sleep(never, 0u, kDebugWaitLimitCycles));
   if (!ok) {
     *abort_flag = 1;
     if (lane == 0) atomicExch(status, kStatusTimeout);
@@ -485,7 +495,10 @@ __global__ void __launch_bounds__(160, 1)
     // before the two-step trip (or the odd tail) that contains that step.
     auto wait_next = [&]() {
       if (cc + 1 < nchunks &&
-          !wait_or_abort(&full[(cc + 1) & 1], (uint32_t)((cc + 1) >> 1) & 1u, limit, abort_flag))
+          !(kRing ? wait_or_abort(&full[(cc + 1) & 1], (uint32_t)((cc + 1) >> 1) & 1u, limit,
+                                  abort_flag)
+                  : wait_or_abort_sleep(&full[(cc + 1) & 1], (uint32_t)((cc + 1) >> 1) & 1u,
+                                        limit, abort_flag)))
         aborted = true;
     };
     int s = 0;

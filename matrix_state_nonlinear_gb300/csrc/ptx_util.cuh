@@ -223,6 +223,44 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, lo
   }
 }
 
+// Bounded wait for warps that wait long and off the critical path (a producer waiting for a
+// whole chunk): try_wait with a suspend-time hint, so the warp sleeps until the phase
+// completes (or the hint expires) instead of re-polling, and leaves the issue slots of its
+// sub-partition to the compute warps that share it.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity,
+                                                    uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_bounded_sleep(uint64_t* bar, uint32_t parity,
+                                                        long long limit) {
+  constexpr uint32_t kHintNs = 20000;
+  if (mbar_try_wait_sleep(bar, parity, kHintNs)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_try_wait_sleep(bar, parity, kHintNs)) return true;
+    if (clock64() - t0 > limit) return false;
+  }
+}
+__device__ __forceinline__ bool wait_or_abort_sleep(uint64_t* bar, uint32_t parity, long long limit,
+                                                    volatile int* abort) {
+  constexpr uint32_t kHintNs = 20000;
+  if (mbar_try_wait_sleep(bar, parity, kHintNs)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_try_wait_sleep(bar, parity, kHintNs)) return true;
+    if (*abort) return false;
+    if (clock64() - t0 > limit) return false;
+  }
+}
+
 // Gate of Eq. (17) of the M²RNN notes: returns (f, 1 - f) with
 // f = exp(-alpha softplus(a + beta)); 1 - f via expm1 for accuracy.
 __device__ __forceinline__ float2 gate_fg(float a, float al, float be) {
