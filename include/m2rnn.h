@@ -233,8 +233,11 @@ m2rnn_status m2rnn_backward_bf16_noalloc(const uint16_t* q, const uint16_t* k, c
  * The arithmetic is exactly one step of m2rnn_forward_bf16 (K <= 64, V <= 64 path),
  * so T successive calls reproduce a T-step forward bit for bit.  For V = 128 the
  * forward uses other kernels (other summation orders): the results agree within the
- * bf16 path's tolerance, not bit for bit.  No TMA and no pipelining: the launch is a
- * single small kernel, suitable for CUDA-graph capture.
+ * bf16 path's tolerance, not bit for bit.  Small batches run one block per (b, n) pair;
+ * K = V = 64 with at least 2048 pairs (and every tensor 16-byte aligned) runs a
+ * persistent kernel that streams each pair's state and W through shared memory with TMA
+ * (same arithmetic, same bits; its bounded waits report timeouts through
+ * m2rnn_stream_status).  Either launch is a single kernel, suitable for CUDA-graph capture.
  * Supports K a multiple of 16 with K <= 128 and V in {16, 32, 64, 128} (UNSUPPORTED
  * otherwise).  Same pointer and size errors as m2rnn_forward_bf16 (INVALID_ARG for a
  * null H_out, or W not 16-byte aligned).

@@ -341,8 +341,11 @@ m2rnn_status m2rnn_decode_step_bf16(const uint16_t* q, const uint16_t* k, const 
   if (!aligned(v, 4) || !aligned(W, 16) || !aligned(H_in, 8) || !aligned(H_out, 8) ||
       !aligned(q, 2) || !aligned(k, 2) || !aligned(a, 2))
     return M2RNN_ERR_INVALID_ARG;
-  Problem p{q, k, v, a, alpha, beta, W, w_r, H_in, y, H_out, B, 1, N, K, V, Nqk, 0, nullptr};
-  return launch_decode_bf16(p, static_cast<cudaStream_t>(stream)) == cudaSuccess
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return M2RNN_ERR_CUDA;
+  Problem p{q, k, v, a, alpha, beta, W, w_r, H_in, y, H_out, B, 1, N, K, V, Nqk, 0,
+            status_address(dev)};
+  return launch_decode_bf16(p, encode_fn(), static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? M2RNN_OK
              : M2RNN_ERR_CUDA;
 }

@@ -127,11 +127,12 @@ cudaError_t launch_bwd_bf16_tc(const BackwardProblem& p, EncodeTiledFn enc, int 
 cudaError_t launch_bwd_bf16_tcc(const BackwardProblem& p, EncodeTiledFn enc, int debug,
                                 int* status, cudaStream_t stream);
 
-// One decode step (T = 1) on the warp MMA, no TMA: K % 16 == 0, K <= 128,
-// V in {16, 32, 64}.  Uses q, k, v, a, alpha, beta, W, w_r, H0 (state in, may be
-// null), H_T (state out, may equal H0), y, B, N, K, V, Nqk of the problem.
+// One decode step (T = 1) on the warp MMA: K % 16 == 0, K <= 128, V in {16, 32, 64, 128}.
+// Uses q, k, v, a, alpha, beta, W, w_r, H0 (state in, may be null), H_T (state out, may
+// equal H0), y, B, N, K, V, Nqk and status of the problem.  K = V = 64 with at least 2048
+// pairs takes a persistent TMA-fed kernel (same arithmetic); `enc` may be null.
 bool decode_supports(int K, int V);
-cudaError_t launch_decode_bf16(const Problem& p, cudaStream_t stream);
+cudaError_t launch_decode_bf16(const Problem& p, EncodeTiledFn enc, cudaStream_t stream);
 
 // Block prologue / epilogue (memory-bound): causal depthwise Conv1D (kernel 4) + SiLU
 // over [B, T, C] bf16 (C % 8 == 0), and the output gate + RMSNorm over rows of D

@@ -37,7 +37,9 @@ def step_args(inp, t):
 @pytest.mark.parametrize("shape,shared", [((2, 37, 3, 64, 64), False), ((3, 20, 2, 32, 16), False),
                                           ((2, 9, 4, 48, 32), True), ((1, 70, 2, 16, 64), False),
                                           ((96, 3, 8, 64, 64), False), ((40, 2, 16, 32, 16), True),
-                                          ((70, 2, 9, 48, 32), False)])
+                                          ((70, 2, 9, 48, 32), False),
+                                          # >= 2048 pairs at K = V = 64: the persistent kernel
+                                          ((160, 2, 16, 64, 64), False), ((130, 3, 16, 64, 64), True)])
 def test_decode_steps_reproduce_the_forward_bitwise(shape, shared):
     B, T, N, K, V = shape
     inp = make_inputs(Workload("dec", B, T, N, K, V, h0="uniform", shared_qk=shared), DEV, 5)
@@ -66,11 +68,13 @@ def test_decode_large_K_matches_oracle(shape):
     assert err_y <= 3e-2 and err_h <= 3e-2, (err_y, err_h)
 
 
-def test_decode_zero_state_and_separate_output():
-    inp = make_inputs(Workload("dec0", 3, 1, 2, 64, 64, h0="zero"), DEV, 7)
+@pytest.mark.parametrize("B, N", [(3, 2), (256, 8)])   # 512 and 2048 pairs
+def test_decode_zero_state_and_separate_output(B, N):
+    inp = make_inputs(Workload("dec0", B, 1, N, 64, 64, h0="zero"), DEV, 7)
     y_ref, H_ref = pkg.m2rnn_forward(inp)
-    H_out = torch.full((3, 2, 64, 64), float("nan"), device=DEV)
+    H_out = torch.full((B, N, 64, 64), float("nan"), device=DEV)
     y, _ = pkg.m2rnn_decode_step(*step_args(inp, 0), None, H_out=H_out)
+    assert pkg.stream_status() == binding.OK
     assert torch.equal(y, y_ref[:, 0]) and torch.equal(H_out, H_ref)
 
 
