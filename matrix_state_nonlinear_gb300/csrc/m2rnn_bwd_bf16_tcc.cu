@@ -377,21 +377,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t idesc_q = umma_idesc_bf16(kK, 16, false);          // A = H, B = the u rows
     const uint32_t idesc_w = umma_idesc_bf16(kV, kV, true);           // A = H^T (M-major view)
     const uint32_t idesc_g = umma_idesc_bf16_ab(kK, kV, true, true);  // A = D, B = W^T N-major
-    const uint64_t d_wt = umma_desc(sbase + L.wt, 16, 1024, 2);       // W^T, K-major
-    const uint64_t d_wn = umma_desc(sbase + L.wt, kTile, 1024, 2);    // the same tile, N-major
-    const uint64_t d_u = umma_desc(sbase + L.wt + kTile, 16, 1024, 2);  // the u rows alone
+    // Descriptors of a tile at byte offset `off` from sbase: the base's address field plus
+    // off / 16 (shared-memory offsets stay below 256 KB, so the field does not overflow).
+    const uint64_t d_k0 = umma_desc(sbase, 16, 1024, 2);     // K-major 128-byte-swizzled
+    const uint64_t d_m0 = umma_desc(sbase, kTile, 1024, 2);  // MN-major, one 64-wide atom
+    const uint64_t d_wt = d_k0 + (uint64_t)(L.wt >> 4);      // W^T, K-major
+    const uint64_t d_wn = d_m0 + (uint64_t)(L.wt >> 4);      // the same tile, N-major
+    const uint64_t d_u = d_k0 + (uint64_t)((L.wt + kTile) >> 4);  // the u rows alone
+    auto hprev_off = [&](int st, int s, int p) -> int {  // the state tile before step s
+      const int t = (nchunks - 1 - p) * kTc + s;
+      return t == 0 ? L.h0t : L.hs + (st * kStageTiles + s) * kTile;
+    };
     // u_tau (fp32, step s_u of the dy block of stage st_u) into rows 64 + tau % 8 (bf16 of u)
     // and 72 + tau % 8 (bf16 of the remainder) of the B operand [W^T; u rows], so that the
     // product H_{t-1} [W | u] also yields H_{t-1} u_{t-1} = dq_{t-1} to fp32 accuracy in u.
+    // Row r of the u groups: 128-byte-swizzled like the W^T rows above it (rows 64 + r and
+    // 72 + r, r < 8, so the swizzle term is r); this lane's 4 bytes at column 2 lane.
+    uint8_t* const urow0 = smem + L.wt + kTile + (lane & 3) * 4;
+    const float* const dys0 = reinterpret_cast<const float*>(smem + L.in + L.dys) + 2 * lane;
     auto put_u = [&](int st_u, int s_u, int row) {
-      const float2 x = *reinterpret_cast<const float2*>(smem + L.in + st_u * L.in_stage + L.dys +
-                                                        (s_u * kV + 2 * lane) * 4);
+      const float2 x = *reinterpret_cast<const float2*>(dys0 + (st_u * L.in_stage) / 4 + s_u * kV);
       const uint32_t hi = pack_bf16x2(x.x, x.y);
       const float2 hf = bf16x2_to_float2(hi);
       const uint32_t lo = pack_bf16x2(x.x - hf.x, x.y - hf.y);
-      const uint32_t off = (uint32_t)(lane & 3) * 4u - sbase;
-      *reinterpret_cast<uint32_t*>(smem + (sw128_addr(sbase + L.wt, 64 + row, lane >> 2) + off)) = hi;
-      *reinterpret_cast<uint32_t*>(smem + (sw128_addr(sbase + L.wt, 72 + row, lane >> 2) + off)) = lo;
+      uint8_t* const dst = urow0 + row * 128 + (((lane >> 2) ^ row) << 4);
+      *reinterpret_cast<uint32_t*>(dst) = hi;
+      *reinterpret_cast<uint32_t*>(dst + 8 * 128) = lo;
       fence_proxy_async_smem();
     };
     Cursor cp{0, chunk_steps(0, nchunks, T) - 1, chunk_steps(0, nchunks, T), 0};
@@ -408,19 +419,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         put_u(0, steps0 - 1, (T - 1) & 7);
         __syncwarp();
         tc_fence_after();
-        const uint64_t d_hl = umma_desc(sbase + L.hs + steps0 * kTile, 16, 1024, 2);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          umma_bf16_if(leader, tmem + kGCol + 64, d_hl + (uint64_t)((kk * 32) >> 4),
-                       d_u + (uint64_t)((kk * 32) >> 4), idesc_q, kk);
+        umma4_if<2, 2>(leader, tmem + kGCol + 64, d_k0 + (uint64_t)((L.hs + steps0 * kTile) >> 4),
+                       d_u, idesc_q, 0u);
         umma_commit_if(leader, Bs.qdone);
       }
     }
     const bool q_issued = ok;
+    int pslot = 0;        // cp.u % kS
+    uint32_t pround = 0;  // cp.u / kS
     while (ok && cw.u < T) {
       // P_t = H_{t-1} W for the steps ahead, into slot u % kS.
       while (ok && cp.u < T && cp.u < cw.u + kS) {
-        const int slot = cp.u % kS;
+        const int slot = pslot;
         // u_{t-1} sits in the next processed chunk when t is the first step of its chunk.
         const bool cross = cp.s == 0 && cp.p + 1 < nchunks;
         bool w = true;
@@ -432,8 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // The slot, and (as its product completed before) the u rows the product of step
         // u - 8 read: both are free once the warps have read P of step u - kS.
         if (cp.u >= kS)
-          w = w && wait_or_abort(&Bs.pfree[slot], (uint32_t)((cp.u / kS) - 1) & 1u, limit,
-                                 Bs.abort_flag);
+          w = w && wait_or_abort(&Bs.pfree[slot], (pround - 1u) & 1u, limit, Bs.abort_flag);
         ok = __all_sync(0xffffffffu, w);
         if (!ok) break;
         full_seen = cross ? cp.p + 1 : max(full_seen, cp.p);
@@ -442,13 +451,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 (cp.s + 7) & 7);
         __syncwarp();
         tc_fence_after();
-        const uint64_t d_h = umma_desc(hprev_tile(stage_of(cp.p), cp.s, cp.p), 16, 1024, 2);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          umma_bf16_if(leader, tmem + kPCols * (uint32_t)slot, d_h + (uint64_t)((kk * 32) >> 4),
-                       d_wt + (uint64_t)((kk * 32) >> 4), idesc_p, kk);
+        umma4_if<2, 2>(leader, tmem + kPCols * (uint32_t)slot,
+                       d_k0 + (uint64_t)(hprev_off(stage_of(cp.p), cp.s, cp.p) >> 4), d_wt,
+                       idesc_p, 0u);
         umma_commit_if(leader, &Bs.pready[slot]);
         cursor_next(cp, nchunks, T);
+        if (++pslot == kS) {
+          pslot = 0;
+          ++pround;
+        }
       }
       if (!ok) break;
       // D_t^T of step cw.u written by every compute warp: the chain product first.
@@ -456,21 +467,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                  limit, Bs.abort_flag));
       if (!ok) break;
       tc_fence_after();
-      const uint32_t dt = sbase + L.dt + (cw.u & 1) * kTile;
-      const uint64_t d_dm = umma_desc(dt, kTile, 1024, 2);  // D_t, M-major view of D_t^T
-      const uint64_t d_dt = umma_desc(dt, 16, 1024, 2);     // D_t^T, K-major
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
-        umma_bf16_if(leader, tmem + kGCol + (uint32_t)(64 * (cw.u & 1)),
-                     d_dm + (uint64_t)((kk * 2048) >> 4), d_wn + (uint64_t)((kk * 2048) >> 4),
-                     idesc_g, kk);
+      const uint64_t dto = (uint64_t)((L.dt + (cw.u & 1) * kTile) >> 4);
+      // D_t (M-major view of D_t^T) x W^T (N-major): the chain product
+      umma4_if<128, 128>(leader, tmem + kGCol + (uint32_t)(64 * (cw.u & 1)), d_m0 + dto, d_wn,
+                         idesc_g, 0u);
       umma_commit_if(leader, &Bs.gready[cw.u & 1]);
-      // dW += H_{t-1}^T D_t.
-      const uint64_t d_ht = umma_desc(hprev_tile(stage_of(cw.p), cw.s, cw.p), kTile, 1024, 2);
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
-        umma_bf16_if(leader, tmem + kDwCol, d_ht + (uint64_t)((kk * 2048) >> 4),
-                     d_dt + (uint64_t)((kk * 32) >> 4), idesc_w, (cw.u > 0 || kk > 0) ? 1u : 0u);
+      // dW += H_{t-1}^T D_t  (A = H_{t-1} M-major view, B = D_t^T K-major).
+      umma4_if<128, 2>(leader, tmem + kDwCol,
+                       d_m0 + (uint64_t)(hprev_off(stage_of(cw.p), cw.s, cw.p) >> 4), d_k0 + dto,
+                       idesc_w, cw.u > 0 ? 1u : 0u);
       umma_commit_if(leader, &Bs.dtfree[cw.u & 1]);
       umma_commit_if(leader && cw.s == 0, &Bs.mmadone[stage_of(cw.p)]);  // the stage may be reused
       cursor_next(cw, nchunks, T);

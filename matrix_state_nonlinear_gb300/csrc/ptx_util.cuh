@@ -392,6 +392,30 @@ __device__ __forceinline__ void umma_bf16_if(bool pred, uint32_t d_tmem, uint64_
       : "memory");
 }
 
+// Four K = 16 steps of one product in one asm block: the descriptors advance by kAInc and
+// kBInc (16-byte units) per step, the first step accumulates only if `accumulate_first`,
+// the others always; issued where `pred` holds.  Fewer issuing instructions than four
+// umma_bf16_if calls (one predicate set-up, descriptor increments in place).
+template <int kAInc, int kBInc>
+__device__ __forceinline__ void umma4_if(bool pred, uint32_t d_tmem, uint64_t a_desc,
+                                         uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate_first) {
+  asm volatile(
+      "{\n\t.reg .pred p, q, t;\n\t.reg .b64 a, b;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 q, %5, 0;\n\tsetp.ne.b32 t, %8, 0;\n\t"
+      "mov.b64 a, %1;\n\tmov.b64 b, %2;\n\t"
+      "@q tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, p;\n\t"
+      "add.s64 a, a, %6;\n\tadd.s64 b, b, %7;\n\t"
+      "@q tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t"
+      "add.s64 a, a, %6;\n\tadd.s64 b, b, %7;\n\t"
+      "@q tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t"
+      "add.s64 a, a, %6;\n\tadd.s64 b, b, %7;\n\t"
+      "@q tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t}"
+      ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate_first), "r"((int)pred),
+        "n"(kAInc), "n"(kBInc), "r"(1)
+      : "memory");
+}
+
 // One lane of the (converged) warp: true there, false elsewhere.
 __device__ __forceinline__ bool elect_one_sync() {
   uint32_t pred = 0;
