@@ -37,6 +37,7 @@
 #include <cuda_bf16.h>
 
 #include <cstring>
+#include <type_traits>
 
 #include "m2rnn_internal.h"
 #include "ptx_util.cuh"
@@ -51,8 +52,8 @@ struct PipeLayout {
                                 //                          target of the empty first pending readout)
   int wr;                       // float  [V]
   int bar;                      // uint64 full[2], done[2], never-armed[1]; int abort
-  int hring;                    // state-keeping forward, V = 64: [nw][4 slots][16 rows][64] bf16,
-                                //   128-byte swizzled, staged for TMA stores (+1024 to align)
+  int hring;                    // state-keeping forward, V = 64: [nw][2 slots][2 steps][16 rows][64]
+                                //   bf16, 128-byte swizzled, staged for TMA stores (+1024 to align)
   int total;
 };
 
@@ -85,7 +86,8 @@ __global__ void __launch_bounds__(160, 1)
     fwd_bf16_mma_pipe(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v,
-                      const __grid_constant__ CUtensorMap tm_hs, const uint16_t* __restrict__ a,
+                      const __grid_constant__ CUtensorMap tm_hs,
+                      const __grid_constant__ CUtensorMap tm_hs1, const uint16_t* __restrict__ a,
                       const float* __restrict__ alpha, const float* __restrict__ beta,
                       const uint16_t* __restrict__ W, const float* __restrict__ w_r,
                       const float* H0, float* __restrict__ y, float* H_T, uint16_t* __restrict__ Hs,
@@ -341,7 +343,8 @@ __global__ void __launch_bounds__(160, 1)
       in.v[nt] = *reinterpret_cast<const uint32_t*>(vs + 8 * nt + 2 * c);
   };
   auto step = [&](float2 (&cur)[NT][2], float2 (&nx)[NT][2], int cc, int s, int steps,
-                  float (&pin)[M], float (&pout)[M], StepIn& in) {
+                  float (&pin)[M], float (&pout)[M], StepIn& in, bool odd) {
+    // odd: the second step of a two-step trip (a literal at every call, folded when inlined)
     float* pin_row = yrow_of(cc, s > 0 ? s - 1 : Tc);
     const int st = cc & 1;
     const uint8_t* sbase = smem + st * L.stage_bytes;
@@ -451,25 +454,32 @@ __global__ void __launch_bounds__(160, 1)
     for (int i = 0; i < M; ++i) pout[i] = p[i];
     if constexpr (kRing) {
       // Keep H_t for the backward pass as the bf16 A fragments just packed from it
-      // (exactly the tensor-core operand step t+1 uses): stmatrix into this warp's slot of
-      // a 4-slot swizzled ring, then one TMA store of the warp's 16 rows.  A slot is
-      // rewritten only after the store issued from it four steps earlier has read it.
-      // No branch: the wait and the commit run on every lane (lanes 1-31 only ever hold
-      // empty groups) and the store is predicated on lane 0, so the step body stays one
-      // basic block (with `if (lane == 0)` blocks the step took 930 instead of 790 cycles).
+      // (exactly the tensor-core operand step t+1 uses): stmatrix into this warp's half of
+      // a two-step slot of a 2-slot swizzled ring; after the second step of the trip, one
+      // fence and one TMA store of the warp's 16 rows for both steps (the odd last step of a
+      // sequence is stored alone, after the loop's tail step).  A slot is rewritten only
+      // after the store issued from it two trips earlier has read it.  No branch on the
+      // lane: the wait and the commit run on every lane (lanes 1-31 only ever hold empty
+      // groups) and the store is predicated on lane 0, so the step body stays one basic
+      // block (with `if (lane == 0)` blocks the step took 930 instead of 790 cycles).
       const int t = cc * Tc + s;
       const uint32_t rbase = (smem_u32(smem) + L.hring + 1023u) & ~1023u;
-      const uint32_t sb = rbase + (uint32_t)((warp * 4 + (t & 3)) * 16 * V * 2);
-      bulk_wait_group_read<3>();  // every lane: only lane 0 holds groups
-      __syncwarp();
+      const uint32_t pslot = rbase + (uint32_t)((warp * 2 + ((t >> 1) & 1)) * 2 * 16 * V * 2);
+      const uint32_t sb = pslot + (odd ? 16u * V * 2u : 0u);
+      if (!odd) {
+        bulk_wait_group_read<1>();  // every lane: only lane 0 holds groups
+        __syncwarp();
+      }
       const int lr = lane & 7, lq = lane >> 3;
 #pragma unroll
       for (int kt = 0; kt < VT; ++kt)
         stsm_x4(sw128_addr(sb, lr + 8 * (lq & 1), 2 * kt + (lq >> 1)), af[kt]);
-      fence_proxy_async_smem();
-      __syncwarp();
-      tma_store_4d_if(lane == 0, &tm_hs, sb, 0, 16 * warp, t, pair);
-      bulk_commit_group();
+      if (odd) {
+        fence_proxy_async_smem();
+        __syncwarp();
+        tma_store_4d_if(lane == 0, &tm_hs, pslot, 0, 16 * warp, t - 1, pair);
+        bulk_commit_group();
+      }
     } else if constexpr (kCache) {
       // Keep H_t for the backward pass as the bf16 A fragments just packed from it:
       // exactly the tensor-core operand step t+1 uses (streaming stores).
@@ -506,13 +516,22 @@ __global__ void __launch_bounds__(160, 1)
     for (; s + 1 < steps; s += 2) {  // two steps per trip: the accumulator sets swap roles
       if (s + 2 >= steps) wait_next();
       if (aborted) break;
-      step(acc, nxt, cc, s, steps, pA, pB, in);
-      step(nxt, acc, cc, s + 1, steps, pB, pA, in);
+      step(acc, nxt, cc, s, steps, pA, pB, in, false);
+      step(nxt, acc, cc, s + 1, steps, pB, pA, in, true);
     }
     if (s < steps && !aborted) {  // odd tail of the last chunk
       wait_next();
-      step(acc, nxt, cc, s, steps, pA, pB, in);
+      step(acc, nxt, cc, s, steps, pA, pB, in, false);
       tail = true;
+      if constexpr (kRing) {  // the last state alone: a one-step store of the pair slot's first half
+        const int t = cc * Tc + s;
+        const uint32_t rbase = (smem_u32(smem) + L.hring + 1023u) & ~1023u;
+        const uint32_t pslot = rbase + (uint32_t)((warp * 2 + ((t >> 1) & 1)) * 2 * 16 * V * 2);
+        fence_proxy_async_smem();
+        __syncwarp();
+        tma_store_4d_if(lane == 0, &tm_hs1, pslot, 0, 16 * warp, t, pair);
+        bulk_commit_group();
+      }
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         acc[nt][0] = nxt[nt][0];
@@ -573,20 +592,26 @@ cudaError_t launch_pipe_vt(const Problem& p, EncodeTiledFn enc, cudaStream_t str
     Tc /= 2;
     L = pipe_layout(p.K, V, Tc, ring);
   }
-  CUtensorMap mq, mk, mv, mh;
+  CUtensorMap mq, mk, mv, mh, mh1;
   if (!make_map_pipe(enc, &mq, p.q, p.K, p.Nqk, p.T, p.B, Tc) ||
       !make_map_pipe(enc, &mk, p.k, p.K, p.Nqk, p.T, p.B, Tc) ||
       !make_map_pipe(enc, &mv, p.v, V, p.N, p.T, p.B, Tc))
     return cudaErrorInvalidValue;
   memset(&mh, 0, sizeof(mh));
+  memset(&mh1, 0, sizeof(mh1));
   if (ring) {  // kept states [B N, T, K, V] bf16, stored 16 rows at a time, 128-byte swizzle
     const cuuint64_t dims[4] = {(cuuint64_t)V, (cuuint64_t)p.K, (cuuint64_t)p.T,
                                 (cuuint64_t)p.B * p.N};
     const cuuint64_t strides[3] = {(cuuint64_t)V * 2, (cuuint64_t)V * 2 * p.K,
                                    (cuuint64_t)V * 2 * p.K * p.T};
-    const cuuint32_t box[4] = {(cuuint32_t)V, 16u, 1u, 1u};
+    // two steps per store (box of 2 time steps), and one for an odd last step
+    const cuuint32_t box[4] = {(cuuint32_t)V, 16u, 2u, 1u};
+    const cuuint32_t box1[4] = {(cuuint32_t)V, 16u, 1u, 1u};
     const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
     if (enc(&mh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, p.Hs, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
+        enc(&mh1, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, p.Hs, dims, strides, box1, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
@@ -596,7 +621,7 @@ cudaError_t launch_pipe_vt(const Problem& p, EncodeTiledFn enc, cudaStream_t str
   if (err != cudaSuccess) return err;
   const unsigned grid = (unsigned)p.B * (unsigned)p.N;
   const int threads = 32 * (p.K / 16 + 1);
-  kern<<<grid, threads, L.total, stream>>>(mq, mk, mv, mh, (const uint16_t*)p.a, p.alpha, p.beta,
+  kern<<<grid, threads, L.total, stream>>>(mq, mk, mv, mh, mh1, (const uint16_t*)p.a, p.alpha, p.beta,
                                            (const uint16_t*)p.W, p.w_r, p.H0, p.y, p.H_T,
                                            static_cast<uint16_t*>(p.Hs), p.T,
                                            p.N, p.K, Tc, p.Nqk == 1 ? 0 : 1, p.debug, p.status);
