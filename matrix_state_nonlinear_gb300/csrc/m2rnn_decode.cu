@@ -12,12 +12,16 @@
 // partials in warp order).  T decode steps therefore reproduce a T-step forward pass
 // bit for bit.
 //
-// No TMA, no producer warp, no pipelining: one block per pair, K / 16 warps; each
-// warp loads its 16 state rows straight from global memory into registers, and the
-// block stages W through shared memory for the B fragments.  The
-// state update may be in place (H_in == H_out): every element is read and written
-// by the same thread.  Large batches are bound by HBM traffic (the state is read and
-// written once); small ones by launch latency.
+// Two kernels with that arithmetic:
+//  * decode_bf16_mma: one block per pair, K / 16 warps; each warp loads its 16 state rows
+//    straight from global memory into registers, and the block stages W through shared
+//    memory for the B fragments.  Any supported shape; small batches are bound by launch
+//    latency.
+//  * decode_bf16_persist (K = V = 64, many pairs): persistent blocks stream the pairs'
+//    states and operands through a TMA-filled shared-memory ring (below); large batches are
+//    bound by HBM traffic (the state is read and written once).
+// The state update may be in place (H_in == H_out): a pair's state is read before any of
+// it is written, and no two pairs share state.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -175,8 +179,9 @@ __global__ void __launch_bounds__(32 * MAXW, (MAXW <= 4 && VT <= 4) ? 6 : 1)
 // K = V = 64 with many pairs: each block walks the pairs blockIdx.x, + gridDim.x, ... and a
 // producer warp streams every pair's state (fp32, two 128-byte-swizzled boxes of 32 columns),
 // its head's W (bf16, one swizzled 64 x 64 box) and the q, k, v rows into a ring of
-// kPS shared-memory stages with TMA, so that the state loads of later pairs are in flight
-// while four compute warps update the current one.  The per-element arithmetic and the
+// kPS shared-memory stages with TMA, and writes the pair's gate (f, 1 - f) into the stage,
+// so that the state loads of later pairs are in flight while four compute warps update the
+// current one.  The per-element arithmetic and the
 // readout order are those of decode_bf16_mma<4, 4> above (bit for bit); only the operands'
 // path differs (shared memory filled by TMA instead of per-thread global loads).
 constexpr int kPS = 2;                  // stages per block
@@ -189,8 +194,10 @@ constexpr int kPBar = kPYpart + 2 * 4 * 64 * 4;
 constexpr int kPSmem = kPBar + 2 * kPS * 8 + 1024;  // + slack to align the base to 1024
 
 __global__ void __launch_bounds__(160, kPBlocks)
-    decode_bf16_persist(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_w,
-                        const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+    decode_bf16_persist(const __grid_constant__ CUtensorMap tm_h,
+                        const __grid_constant__ CUtensorMap tm_w,
+                        const __grid_constant__ CUtensorMap tm_q,
+                        const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const uint16_t* __restrict__ a,
                         const float* __restrict__ alpha, const float* __restrict__ beta,
                         const float* __restrict__ w_r, bool has_h, float* H_out,
