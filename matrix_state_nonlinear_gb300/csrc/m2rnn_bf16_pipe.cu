@@ -362,7 +362,11 @@ __global__ void __launch_bounds__(160, 1)
       cin = in;
       fetch(in, cc, s, steps);
     }
-    const float2 fg = kRing ? fgs[st * Tc + s] : cin.fg;
+    float2 fg;
+    if constexpr (kRing)
+      fg = fgs[st * Tc + s];
+    else
+      fg = cin.fg;
     const float2 ff = make_float2(fg.x, fg.x), gg = make_float2(fg.y, fg.y);
 
     // Rank-1 k_{t+1} v_{t+1}^T initialises P_{t+1}.  (After the last step of the
@@ -439,8 +443,14 @@ __global__ void __launch_bounds__(160, 1)
 
     // Readout of H_t (Eq. (12)): q-weighted sums of this thread's two rows.
     const uint16_t* qs = reinterpret_cast<const uint16_t*>(sbase + L.qs) + s * K;
-    const float qv0 = bf16_bits_to_float(kRing ? qs[r0] : cin.q0);
-    const float qv1 = bf16_bits_to_float(kRing ? qs[r1] : cin.q1);
+    float qv0, qv1;
+    if constexpr (kRing) {
+      qv0 = bf16_bits_to_float(qs[r0]);
+      qv1 = bf16_bits_to_float(qs[r1]);
+    } else {
+      qv0 = bf16_bits_to_float(cin.q0);
+      qv1 = bf16_bits_to_float(cin.q1);
+    }
     const float2 q0 = make_float2(qv0, qv0), q1 = make_float2(qv1, qv1);
     float p[M];
 #pragma unroll
