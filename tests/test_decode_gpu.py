@@ -78,8 +78,9 @@ def test_decode_zero_state_and_separate_output(B, N):
     assert torch.equal(y, y_ref[:, 0]) and torch.equal(H_out, H_ref)
 
 
-def test_decode_cuda_graph_replay():
-    B, T, N, K, V = 4, 8, 4, 64, 64
+@pytest.mark.parametrize("B, N", [(4, 4), (128, 16)])   # 16 pairs; 2048 pairs (persistent kernel)
+def test_decode_cuda_graph_replay(B, N):
+    T, K, V = 8, 64, 64
     inp = make_inputs(Workload("decg", B, T, N, K, V, h0="uniform"), DEV, 8)
     steps = [step_args(inp, t) for t in range(T)]
     H_eager = inp["H0"].clone()
