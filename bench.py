@@ -260,37 +260,149 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- CPU oracle sample
-def oracle_sample(wl, seconds: float, T_s: int | None = None):
-    """Times the fp64 oracle on a bounded sample of the workload.
+def host_cores() -> dict:
+    """What the host offers: logical CPUs, and the ones this process may run on."""
+    aff = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return {"host_cpu_count": os.cpu_count(), "affinity_cores": aff}
+
+
+def _as_f64(x):
+    """A worker's input block as fp64: bf16 arrives as its uint16 bit pattern (exact upcast)."""
+    import numpy as np
+    if x is None:
+        return None
+    if x.dtype == np.uint16:
+        return (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return x.astype(np.float64)
+
+
+def _oracle_worker(task):
+    """One block of (batch, head) pairs through the fp64 oracle, unchanged.  Returns the
+    monotonic start and end of the oracle call (system-wide clock) and its CPU seconds."""
+    kind, blk = task
+    from oracle import m2rnn_backward, m2rnn_forward
+    a = {k: _as_f64(v) for k, v in blk.items()}
+    c0 = time.process_time()
+    t0 = time.monotonic()
+    if kind == "forward":
+        m2rnn_forward(a["q"], a["k"], a["v"], a["a"], a["alpha"], a["beta"], a["W"], a["w_r"],
+                      a["H0"])
+    else:                                   # forward keeping states + backward
+        m2rnn_backward(a["q"], a["k"], a["v"], a["a"], a["alpha"], a["beta"], a["W"], a["w_r"],
+                       a["dy"], a["H0"])
+    return t0, time.monotonic(), time.process_time() - c0
+
+
+def pair_blocks(arrs: dict, parts: int) -> list:
+    """Splits a problem's host arrays into at most `parts` blocks of whole (batch, head)
+    pairs: heads first, then batch rows.  Pairs are independent units of the recurrence,
+    so the blocks' outputs are exactly the full problem's.  Returns a list of
+    ((b0, b1, n0, n1), block arrays)."""
+    import numpy as np
+    B, _, N = arrs["v"].shape[:3]
+    gn = max(1, min(N, parts))
+    gb = max(1, min(B, parts // gn))
+    shared = arrs["q"].shape[2] == 1 and N > 1
+    out = []
+    for bs in np.array_split(np.arange(B), gb):
+        for ns in np.array_split(np.arange(N), gn):
+            b0, b1, n0, n1 = int(bs[0]), int(bs[-1]) + 1, int(ns[0]), int(ns[-1]) + 1
+            blk = {}
+            for key, val in arrs.items():
+                if val is None:
+                    blk[key] = None
+                elif key in ("q", "k"):
+                    blk[key] = val[b0:b1, :, :] if shared else val[b0:b1, :, n0:n1]
+                elif key in ("v", "a", "dy"):
+                    blk[key] = val[b0:b1, :, n0:n1]
+                elif key == "H0":
+                    blk[key] = val[b0:b1, n0:n1]
+                else:                       # alpha, beta, W, w_r: per head
+                    blk[key] = val[n0:n1]
+                if blk[key] is not None:
+                    blk[key] = np.ascontiguousarray(blk[key])
+            out.append(((b0, b1, n0, n1), blk))
+    return out
+
+
+class OraclePool:
+    """Worker processes (spawned, one BLAS thread each) that run the oracle on blocks of
+    independent (batch, head) pairs, one block per core."""
+
+    def __init__(self, procs: int | None = None):
+        import multiprocessing as mp
+        self.procs = procs or host_cores()["affinity_cores"] or 1
+        saved = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS",
+                                                 "MKL_NUM_THREADS")}
+        for k in saved:
+            os.environ[k] = "1"
+        try:
+            self.pool = mp.get_context("spawn").Pool(self.procs)
+        finally:
+            for k, v in saved.items():
+                if v is None:
+                    os.environ.pop(k, None)
+                else:
+                    os.environ[k] = v
+
+    def run(self, kind: str, arrs: dict):
+        """Wall seconds of the parallel oracle run (first start to last end) and CPU seconds."""
+        res = self.pool.map(_oracle_worker,
+                            [(kind, b) for _, b in pair_blocks(arrs, self.procs)], chunksize=1)
+        return max(r[1] for r in res) - min(r[0] for r in res), sum(r[2] for r in res)
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
+
+
+def host_arrays(inp: dict) -> dict:
+    """Host copies of the inputs for the oracle workers: bf16 as uint16 bit patterns."""
+    import torch
+    out = {}
+    for k, v in inp.items():
+        if v is None:
+            out[k] = None
+        elif v.dtype == torch.bfloat16:
+            out[k] = v.detach().cpu().view(torch.int16).numpy().view("uint16")
+        else:
+            out[k] = v.detach().cpu().numpy()
+    return out
+
+
+def oracle_sample(wl, seconds: float, T_s: int | None = None, pool: OraclePool | None = None):
+    """Times the fp64 oracle on a bounded sample of the workload, on every host core.
 
     The sample is every (batch, head) pair of the workload over its first T_s
     time steps; without a given T_s it is grown until one run takes about
-    `seconds` of wall time.  Returns (units per second, sample description,
-    cores used = process CPU time / wall time, T_s).
+    `seconds` of wall time.  The pairs are split into one block per core, each run
+    by the unchanged oracle in its own process.  Returns (units per second, sample
+    description, cores used, T_s).
     """
-    from matrix_state_nonlinear_gb300.inputs import make_inputs, to_f64_numpy
-    from oracle import m2rnn_forward
+    from matrix_state_nonlinear_gb300.inputs import make_inputs
 
-    fixed = T_s is not None
-    T_s = T_s or 8
-    while True:
-        inp = make_inputs(wl.with_(T=T_s), "cpu", 0)
-        arrs = {k: to_f64_numpy(v) for k, v in inp.items()}
-        c0 = time.process_time()
-        t0 = time.perf_counter()
-        m2rnn_forward(arrs["q"], arrs["k"], arrs["v"], arrs["a"], arrs["alpha"], arrs["beta"],
-                      arrs["W"], arrs["w_r"], arrs["H0"])
-        wall = time.perf_counter() - t0
-        cpu = time.process_time() - c0
-        if fixed or wall >= seconds or T_s >= wl.T:
-            break
-        grow = max(2.0, min(8.0, 1.1 * seconds / max(wall, 1e-3)))
-        T_s = min(wl.T, int(T_s * grow))
+    own = pool is None
+    pool = pool or OraclePool()
+    try:
+        fixed = T_s is not None
+        T_s = T_s or 8
+        while True:
+            arrs = host_arrays(make_inputs(wl.with_(T=T_s), "cpu", 0))
+            wall, cpu = pool.run("forward", arrs)
+            if fixed or wall >= seconds or T_s >= wl.T:
+                break
+            grow = max(2.0, min(8.0, 1.1 * seconds / max(wall, 1e-3)))
+            T_s = min(wl.T, int(T_s * grow))
+    finally:
+        if own:
+            pool.close()
     units = wl.B * wl.N * T_s
-    cores = max(1, round(cpu / wall)) if wall > 0 else 1
+    blocks = min(pool.procs, wl.B * wl.N)
     desc = (f"all {wl.B * wl.N} (batch, head) pairs of {wl.name} over the first {T_s} of "
-            f"{wl.T} steps (fp64 NumPy oracle, {units} token-heads, {wall:.1f} s wall)")
-    return units / wall, desc, cores, T_s
+            f"{wl.T} steps (fp64 NumPy oracle, {units} token-heads, {wall:.1f} s wall; pairs "
+            f"split into {blocks} blocks run by {pool.procs} single-threaded processes, "
+            f"{cpu / wall if wall > 0 else 0:.1f} cores busy on average)")
+    return units / wall, desc, blocks, T_s
 
 
 def reference_arm(args, wl):
@@ -299,11 +411,15 @@ def reference_arm(args, wl):
         return 0
     per = max(2.0, min(args.cpu_seconds, 120.0 / max(1, args.steps + args.warmup)))
     vals = []
-    _, desc, cores, T_s = oracle_sample(wl, per)          # sizes the sample (untimed)
-    for i in range(args.warmup + args.steps):
-        v, desc, cores, _ = oracle_sample(wl, per, T_s)
-        if i >= args.warmup:
-            vals.append(v)
+    pool = OraclePool()
+    try:
+        _, desc, cores, T_s = oracle_sample(wl, per, pool=pool)   # sizes the sample (untimed)
+        for i in range(args.warmup + args.steps):
+            v, desc, cores, _ = oracle_sample(wl, per, T_s, pool=pool)
+            if i >= args.warmup:
+                vals.append(v)
+    finally:
+        pool.close()
     value = statistics.median(vals)
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
@@ -311,7 +427,7 @@ def reference_arm(args, wl):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": workload_config(wl),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                         "sample": desc},
+                         "sample": desc, **host_cores()},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -336,31 +452,34 @@ def workload_config(wl):
 METRIC_TRAIN = "M²RNN training step (state-keeping forward + backward) tokens·heads/s"
 
 
-def oracle_train_sample(wl, seconds: float):
-    """Times the fp64 oracle's forward + backward on every pair over a bounded prefix of T."""
+def oracle_train_sample(wl, seconds: float, pool: OraclePool | None = None):
+    """Times the fp64 oracle's forward + backward on every pair over a bounded prefix of T,
+    on every host core (one block of pairs per single-threaded process)."""
     import numpy as np
-    from matrix_state_nonlinear_gb300.inputs import make_inputs, to_f64_numpy
-    from oracle import m2rnn_backward
+    from matrix_state_nonlinear_gb300.inputs import make_inputs
 
-    T_s = 4
-    while True:
-        inp = make_inputs(wl.with_(T=T_s), "cpu", 0)
-        arrs = {k: to_f64_numpy(v) for k, v in inp.items()}
-        dy = np.random.default_rng(1).normal(0, 1, (wl.B, T_s, wl.N, wl.V))
-        c0 = time.process_time()
-        t0 = time.perf_counter()
-        m2rnn_backward(arrs["q"], arrs["k"], arrs["v"], arrs["a"], arrs["alpha"], arrs["beta"],
-                       arrs["W"], arrs["w_r"], dy, arrs["H0"])   # re-runs the forward inside
-        wall = time.perf_counter() - t0
-        cpu = time.process_time() - c0
-        if wall >= seconds or T_s >= wl.T:
-            break
-        T_s = min(wl.T, int(T_s * max(2.0, min(8.0, 1.1 * seconds / max(wall, 1e-3)))))
+    own = pool is None
+    pool = pool or OraclePool()
+    try:
+        T_s = 4
+        while True:
+            arrs = host_arrays(make_inputs(wl.with_(T=T_s), "cpu", 0))
+            arrs["dy"] = np.random.default_rng(1).normal(0, 1, (wl.B, T_s, wl.N, wl.V))
+            wall, cpu = pool.run("train", arrs)
+            if wall >= seconds or T_s >= wl.T:
+                break
+            T_s = min(wl.T, int(T_s * max(2.0, min(8.0, 1.1 * seconds / max(wall, 1e-3)))))
+    finally:
+        if own:
+            pool.close()
     units = wl.B * wl.N * T_s
+    blocks = min(pool.procs, wl.B * wl.N)
     desc = (f"all {wl.B * wl.N} (batch, head) pairs of {wl.name} over the first {T_s} of "
             f"{wl.T} steps (fp64 NumPy oracle, forward keeping states + backward, {units} "
-            f"token-heads, {wall:.1f} s wall)")
-    return units / wall, desc, max(1, round(cpu / wall)) if wall > 0 else 1
+            f"token-heads, {wall:.1f} s wall; pairs split into {blocks} blocks run by "
+            f"{pool.procs} single-threaded processes, {cpu / wall if wall > 0 else 0:.1f} cores "
+            f"busy on average)")
+    return units / wall, desc, blocks
 
 
 def main_train(args, wl):
@@ -534,7 +653,8 @@ def main_train(args, wl):
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         v, desc, cores = oracle_train_sample(wl, args.cpu_seconds)
-        cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
+        cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc,
+               **host_cores()}
     launches = 2 + (1 if Nqk == 1 and N > 1 else 0) + 1    # forward, backward, reduce(s)
     if rank == 0:
         line = {"metric": METRIC_TRAIN, "value": value, "unit": UNIT, "n_gpus": world,
@@ -579,7 +699,8 @@ def decode_reference(args):
             vals.append(B * N / (time.perf_counter() - t0))
     cores = max(1, round((time.process_time() - c0) / (time.perf_counter() - t_all)))
     value = statistics.median(vals)
-    desc = f"one decode step of {name} (fp64 NumPy oracle, {B * N} token-heads per step)"
+    desc = (f"one decode step of {name} (fp64 NumPy oracle, {B * N} token-heads per step; "
+            f"one process: a decode step is too short to split across cores)")
     print(json.dumps({
         "impl": "reference", "metric": METRIC_DECODE, "value": value, "unit": UNIT,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": None,
@@ -587,7 +708,7 @@ def decode_reference(args):
         "data": "synthetic", "config": {"workload": name, "B": B, "T": 1, "N": N, "K": K, "V": V,
                                         "pass": "decode"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                         "sample": desc},
+                         "sample": desc, **host_cores()},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
     return 0
@@ -734,9 +855,10 @@ def main_decode(args):
         wall = time.perf_counter() - t0
         line["cpu_baseline"] = {
             "value": Bs * N / wall, "unit": UNIT, "kind": "oracle",
-            "cores": max(1, round((time.process_time() - c0) / wall)),
+            "cores": max(1, round((time.process_time() - c0) / wall)), **host_cores(),
             "sample": f"one decode step of the first {Bs} of {B} batch rows "
-                      f"(fp64 NumPy oracle, {Bs * N} token-heads, {wall:.2f} s wall)"}
+                      f"(fp64 NumPy oracle, {Bs * N} token-heads, {wall:.2f} s wall; one "
+                      f"process)"}
     print(json.dumps(line), flush=True)
     return 0
 
@@ -845,6 +967,48 @@ def main_block(args, wl):
 
 
 # ---------------------------------------------------------------- GPU arm
+def serial_bound(pkg, inp, wl, variant, stream, dev, ms_per_step, mhz, T_s=4096):
+    """The serial-latency bound of T dependent steps, measured with the same kernel.
+
+    One (batch, head) pair alone on the GPU (B = N = 1, its first T_s steps) runs the
+    dependent step chain with nothing else competing for its SM(s); its per-step time
+    times T is the least time any schedule of this kernel can take for T steps.  When
+    the workload has no more pairs than the GPU runs at once, the whole job is bound
+    by this chain (serial_frac near 1)."""
+    import torch
+    T_s = min(wl.T, T_s)
+    one = {}
+    for k, v in inp.items():
+        if v is None:
+            one[k] = None
+        elif k in ("q", "k", "v", "a"):
+            one[k] = v[0:1, :T_s, 0:1].contiguous()
+        elif k == "H0":
+            one[k] = v[0:1, 0:1].contiguous()
+        else:
+            one[k] = v[0:1].contiguous()
+    y1 = torch.empty((1, T_s, 1, wl.V), dtype=torch.float32, device=dev)
+    H1 = torch.empty((1, 1, wl.K, wl.V), dtype=torch.float32, device=dev)
+    for _ in range(2):
+        pkg.m2rnn_forward(one, y=y1, H_T=H1, variant=variant, stream=stream)
+    times = []
+    for _ in range(5):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        pkg.m2rnn_forward(one, y=y1, H_T=H1, variant=variant, stream=stream)
+        e1.record(stream)
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1))
+    per_step_ms = statistics.median(times) / T_s
+    t_serial = per_step_ms * wl.T
+    return {"t_serial_bound_ms": t_serial,
+            "serial_cycles_per_step": per_step_ms * 1e-3 * mhz * 1e6,
+            "serial_frac": t_serial / ms_per_step,
+            "serial_method": (f"same kernel on one (batch, head) pair alone (B = N = 1, first "
+                              f"{T_s} steps, median of 5 CUDA-event-timed launches): per-step "
+                              f"time x T; cycles at the median sampled SM clock")}
+
+
 def main():
     args = parse()
     from matrix_state_nonlinear_gb300.inputs import HEADLINE, WORKLOADS
@@ -1001,11 +1165,13 @@ def main():
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     mhz = clk.get("sm_mhz") or 1950.0
     roof["t_mufu_tanh_floor_ms"] = K * V * wl.units / (16.0 * sms * mhz * 1e6) * 1e3
+    roof.update(serial_bound(pkg, inp, wl, args.variant, stream, dev, ms_per_step, mhz))
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         v, desc, cores, _ = oracle_sample(wl, args.cpu_seconds)
-        cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
+        cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc,
+               **host_cores()}
 
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,

@@ -74,10 +74,13 @@ m2rnn_status m2rnn_forward_f32(const float* q, const float* k, const float* v, c
  * their uint16_t bit patterns); alpha, beta, w_r, H0, y and H_T are float32.
  * The state H is carried in fp32 and rounded to bf16 only as the tensor-core
  * operand of each step's H W; the rank-1 term, tanh, gate lerp and readout are
- * fp32.  Supports K a multiple of 16 with 16 <= K <= 128 and V in
- * {16, 32, 64, 128}.  q, k, v, W, y, H0 and H_T must be 16-byte aligned
- * (INVALID_ARG otherwise).  Same argument rules and errors as m2rnn_forward_f32,
- * plus UNSUPPORTED for any other K or V.
+ * fp32.  Supports any 1 <= K <= 128 and V a multiple of 16 with 16 <= V <= 128.
+ * K that is not a multiple of 16 runs with its rows padded to the next multiple
+ * of 16 inside the kernel (padding rows hold zero state, k and q, stay zero for
+ * every t and are never stored), so the results are those of the K-row problem.
+ * q, k, v, W, y, H0 and H_T must be 16-byte aligned (INVALID_ARG otherwise).
+ * Same argument rules and errors as m2rnn_forward_f32, plus UNSUPPORTED for K or
+ * V > 128 and for V not a multiple of 16.
  */
 m2rnn_status m2rnn_forward_bf16(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                                 const uint16_t* a, const float* alpha, const float* beta,
@@ -125,10 +128,11 @@ m2rnn_status m2rnn_forward_bf16_qk(const uint16_t* q, const uint16_t* k, const u
  *                           bfloat16 (uint16_t bits), the round-to-nearest-even
  *                           rounding of H_t, i.e. exactly the tensor-core operand
  *                           the next step multiplies by W (B·N·T·K·V·2 bytes).
- *   Hs is required when T > 0 (16-byte aligned on the bf16 entry).  The bf16 entry takes the pipelined warp-MMA
- *   kernel for K a multiple of 16 with K <= 64 and V in {16, 32, 64}, and the row-warp
- *   kernel (W in shared memory) for K a multiple of 16 up to 128 with V = 128
- *   (UNSUPPORTED otherwise); the fp32 entry supports 1 <= K, V <= 128.
+ *   Hs is required when T > 0 (16-byte aligned on the bf16 entry).  The bf16 entry
+ *   takes the pipelined warp-MMA kernel for K a multiple of 16 with K <= 64 and V in
+ *   {16, 32, 64}, and the row-warp kernel for every other 1 <= K <= 128 with V a
+ *   multiple of 16 up to 128 (UNSUPPORTED otherwise); the fp32 entry supports
+ *   1 <= K, V <= 128.
  */
 m2rnn_status m2rnn_forward_train_f32(const float* q, const float* k, const float* v,
                                      const float* a, const float* alpha, const float* beta,
@@ -212,6 +216,8 @@ m2rnn_status m2rnn_backward_bf16(const uint16_t* q, const uint16_t* k, const uin
  *     Order them on one stream or with events.
  *   * The first call on a device resolves the scratch address (it may load the
  *     module); make that first call before capturing a stream into a CUDA graph.
+ *     The address is cached per CUDA context: after a cudaDeviceReset the next call
+ *     resolves it again (and must, again, come before any capture).
  */
 m2rnn_status m2rnn_backward_bf16_noalloc(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                                          const uint16_t* a, const float* alpha, const float* beta,
@@ -230,23 +236,41 @@ m2rnn_status m2rnn_backward_bf16_noalloc(const uint16_t* q, const uint16_t* k, c
  *   H_out  [B, N, K, V] float32 state after the token (required; H_out == H_in updates
  *          the state in place)
  *   y      [B, N, V] float32
- * The arithmetic is exactly one step of m2rnn_forward_bf16 (K <= 64, V <= 64 path),
- * so T successive calls reproduce a T-step forward bit for bit.  For V = 128 the
- * forward uses other kernels (other summation orders): the results agree within the
- * bf16 path's tolerance, not bit for bit.  Small batches run one block per (b, n) pair;
+ * The arithmetic is exactly one step of m2rnn_forward_bf16's warp-MMA kernels
+ * (the pipelined kernel and the row-warp kernel), so T successive calls reproduce a
+ * T-step forward on those kernels bit for bit.  K = V = 128 and K = 64, V = 128 run
+ * the forward on other kernels (other summation orders): there the results agree
+ * within the bf16 path's tolerance, not bit for bit.  Small batches run one block per (b, n) pair;
  * K = V = 64 with at least 2048 pairs (and every tensor 16-byte aligned) runs a
  * persistent kernel that streams each pair's state and W through shared memory with TMA
  * (same arithmetic, same bits; its bounded waits report timeouts through
  * m2rnn_stream_status).  Either launch is a single kernel, suitable for CUDA-graph capture.
- * Supports K a multiple of 16 with K <= 128 and V in {16, 32, 64, 128} (UNSUPPORTED
- * otherwise).  Same pointer and size errors as m2rnn_forward_bf16 (INVALID_ARG for a
- * null H_out, or W not 16-byte aligned).
+ * Supports any 1 <= K <= 128 and V a multiple of 16 with 16 <= V <= 128 (UNSUPPORTED
+ * otherwise; K that is not a multiple of 16 is padded with zero rows as in
+ * m2rnn_forward_bf16).  Same pointer and size errors as m2rnn_forward_bf16 (INVALID_ARG
+ * for a null H_out, or W not 16-byte aligned).
  */
 m2rnn_status m2rnn_decode_step_bf16(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                                     const uint16_t* a, const float* alpha, const float* beta,
                                     const uint16_t* W, const float* w_r, const float* H_in,
                                     float* H_out, float* y, int B, int N, int Nqk, int K, int V,
                                     void* stream);
+
+/*
+ * As m2rnn_decode_step_bf16 with an explicit kernel: variant 0 = automatic (what
+ * m2rnn_decode_step_bf16 uses), 1 = one block per (b, n) pair, 2 = the persistent
+ * TMA-fed kernel at any pair count (K = V = 64 and every tensor 16-byte aligned, else
+ * UNSUPPORTED).  Both give the same bits.  Bits 8 and up of `variant` are test hooks
+ * (0); they act on the persistent kernel only (the per-pair kernel has no device waits).
+ * Any other low byte returns INVALID_ARG.
+ */
+m2rnn_status m2rnn_decode_step_bf16_variant(const uint16_t* q, const uint16_t* k,
+                                            const uint16_t* v, const uint16_t* a,
+                                            const float* alpha, const float* beta,
+                                            const uint16_t* W, const float* w_r,
+                                            const float* H_in, float* H_out, float* y, int B,
+                                            int N, int Nqk, int K, int V, int variant,
+                                            void* stream);
 
 /*
  * The block's elementwise stages around the recurrence (the notes' Sec. 2.3,

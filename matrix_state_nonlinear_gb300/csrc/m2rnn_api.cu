@@ -15,17 +15,24 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 
+// Device address of this device's status word, cached per CUDA context (see
+// current_context_id).
 int* status_address(int dev) {
-  static int* addr[kMaxDevices] = {};
+  struct Entry {
+    unsigned long long ctx;
+    int* addr;
+  };
+  static Entry cache[kMaxDevices] = {};
   static std::mutex mu;
   if (dev < 0 || dev >= kMaxDevices) return nullptr;
   std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
-    addr[dev] = static_cast<int*>(p);
-  }
-  return addr[dev];
+  unsigned long long id = 0;
+  const bool have_id = current_context_id(&id);
+  if (have_id && cache[dev].addr && cache[dev].ctx == id) return cache[dev].addr;
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+  if (have_id || current_context_id(&id)) cache[dev] = Entry{id, static_cast<int*>(p)};
+  return static_cast<int*>(p);
 }
 
 EncodeTiledFn encode_fn() {
@@ -105,6 +112,31 @@ bool supports(int variant, int K, int V) {
 }
 
 }  // namespace
+
+bool current_context_id(unsigned long long* id) {
+  using GetCurrentFn = CUresult (*)(CUcontext*);
+  using GetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+  static GetCurrentFn get_current = nullptr;
+  static GetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetIdFn>(p);
+  });
+  CUcontext ctx = nullptr;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx) return false;
+  return get_id(ctx, id) == CUDA_SUCCESS;
+}
+
 }  // namespace m2rnn
 
 using namespace m2rnn;
@@ -328,26 +360,42 @@ m2rnn_status m2rnn_backward_bf16(const uint16_t* q, const uint16_t* k, const uin
   return err == cudaSuccess ? M2RNN_OK : M2RNN_ERR_CUDA;
 }
 
-m2rnn_status m2rnn_decode_step_bf16(const uint16_t* q, const uint16_t* k, const uint16_t* v,
-                                    const uint16_t* a, const float* alpha, const float* beta,
-                                    const uint16_t* W, const float* w_r, const float* H_in,
-                                    float* H_out, float* y, int B, int N, int Nqk, int K, int V,
-                                    void* stream) {
+m2rnn_status m2rnn_decode_step_bf16_variant(const uint16_t* q, const uint16_t* k,
+                                            const uint16_t* v, const uint16_t* a,
+                                            const float* alpha, const float* beta,
+                                            const uint16_t* W, const float* w_r,
+                                            const float* H_in, float* H_out, float* y, int B,
+                                            int N, int Nqk, int K, int V, int variant,
+                                            void* stream) {
   m2rnn_status st = common_checks(q, k, v, a, alpha, beta, W, w_r, y, B, 1, N, K, V);
   if (st != M2RNN_OK) return st;
   if (!H_out) return M2RNN_ERR_INVALID_ARG;
   if (Nqk != 1 && Nqk != N) return M2RNN_ERR_INVALID_ARG;
+  const int debug = variant >> 8, which = variant & 0xff;
+  if (which < 0 || which > 2) return M2RNN_ERR_INVALID_ARG;
   if (!decode_supports(K, V)) return M2RNN_ERR_UNSUPPORTED;
   if (!aligned(v, 4) || !aligned(W, 16) || !aligned(H_in, 8) || !aligned(H_out, 8) ||
       !aligned(q, 2) || !aligned(k, 2) || !aligned(a, 2))
     return M2RNN_ERR_INVALID_ARG;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return M2RNN_ERR_CUDA;
-  Problem p{q, k, v, a, alpha, beta, W, w_r, H_in, y, H_out, B, 1, N, K, V, Nqk, 0,
-            status_address(dev)};
-  return launch_decode_bf16(p, encode_fn(), static_cast<cudaStream_t>(stream)) == cudaSuccess
+  int* status = status_address(dev);
+  EncodeTiledFn enc = encode_fn();
+  Problem p{q, k, v, a, alpha, beta, W, w_r, H_in, y, H_out, B, 1, N, K, V, Nqk, debug, status};
+  if (which == 2 && (!decode_persist_supports(p) || !enc || !status))
+    return M2RNN_ERR_UNSUPPORTED;
+  return launch_decode_bf16(p, enc, static_cast<cudaStream_t>(stream), which) == cudaSuccess
              ? M2RNN_OK
              : M2RNN_ERR_CUDA;
+}
+
+m2rnn_status m2rnn_decode_step_bf16(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                    const uint16_t* a, const float* alpha, const float* beta,
+                                    const uint16_t* W, const float* w_r, const float* H_in,
+                                    float* H_out, float* y, int B, int N, int Nqk, int K, int V,
+                                    void* stream) {
+  return m2rnn_decode_step_bf16_variant(q, k, v, a, alpha, beta, W, w_r, H_in, H_out, y, B, N,
+                                        Nqk, K, V, 0, stream);
 }
 
 m2rnn_status m2rnn_conv_silu_bf16(const uint16_t* x, const float* w, const float* bias,

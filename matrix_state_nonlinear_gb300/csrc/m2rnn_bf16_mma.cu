@@ -24,7 +24,17 @@
 // Inputs q, k, v arrive in chunks of Tc steps by TMA (double-buffered, mbarrier
 // completion, bounded waits); gate logits a are prefetched into registers one
 // chunk ahead and turned into (f, 1 - f) in shared memory.
+//
+// Any 1 <= K <= 128 and any V = 16, 32, ..., 128.  K rows are padded to Kp, the next
+// multiple of 16 (one warp per 16 rows).  Padded rows start at zero and get a zero k and
+// q, so their P = 0 W + 0 stays 0, tanh(0) = 0 keeps them at 0 for every t, and they add
+// nothing to the readout; they are never stored.  With K not a multiple of 16 the q and
+// k rows (K * 2 bytes, not a legal TMA stride in general) are staged by plain loads with
+// the padding written as zeros; v still comes by TMA.  V whose readout slot count 4 V / 16
+// is not a power of two pads the reduce-scatter with zero slots that are never stored.
 #include <cuda_bf16.h>
+
+#include <cstring>
 
 #include "m2rnn_internal.h"
 #include "ptx_util.cuh"
@@ -35,7 +45,7 @@ namespace {
 struct SmemLayout {
   int qs, ks, vs, stage_bytes;  // per stage (two stages, `stage_bytes` apart)
   int fg;                       // float2 [2][Tc]   (f, 1 - f)
-  int ypart;                    // float  [K/16][Tc][V] per-warp readout partials
+  int ypart;                    // float  [Kp/16][Tc][V] per-warp readout partials
   int wr;                       // float  [V]
   int Ws;                       // bf16   [V][V + 8] (only when W is not in registers)
   int bar;                      // uint64 [3]
@@ -44,17 +54,18 @@ struct SmemLayout {
 
 __host__ __device__ inline int align128(int x) { return (x + 127) & ~127; }
 
-__host__ __device__ inline SmemLayout make_layout(int K, int V, int Tc, bool wreg) {
+// Kp: rows of H including the padding of a ragged K (a multiple of 16).
+__host__ __device__ inline SmemLayout make_layout(int Kp, int V, int Tc, bool wreg) {
   SmemLayout L;
   L.qs = 0;
-  L.ks = align128(Tc * K * 2);
-  L.vs = L.ks + align128(Tc * K * 2);
+  L.ks = align128(Tc * Kp * 2);
+  L.vs = L.ks + align128(Tc * Kp * 2);
   L.stage_bytes = L.vs + align128(Tc * V * 2);
   int o = 2 * L.stage_bytes;
   L.fg = o;
   o += align128(2 * Tc * 8);
   L.ypart = o;
-  o += align128((K / 16) * Tc * V * 4);
+  o += align128((Kp / 16) * Tc * V * 4);
   L.wr = o;
   o += align128(V * 4);
   L.Ws = o;
@@ -75,11 +86,14 @@ __device__ __forceinline__ float2 gate_pair(float a, float al, float be) {
 
 // kCache: also keep every state H_t, as the bf16 A fragments the next step's MMAs use
 // (Hs [B N, T, K, V]), for the backward pass.
-template <int VT, bool WREG, bool kCache>
+// kRagged: K is not a multiple of 16; q and k are staged by plain loads (qg, kg) into
+// rows of Kp = blockDim.x / 2 with zero padding (the TMA maps tm_q, tm_k are unused).
+template <int VT, bool WREG, bool kCache, bool kRagged>
 __global__ void __launch_bounds__(256, 1)
     fwd_bf16_mma_rowwarp(const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k,
-                         const __grid_constant__ CUtensorMap tm_v, const uint16_t* __restrict__ a,
+                         const __grid_constant__ CUtensorMap tm_v, const uint16_t* __restrict__ qg,
+                         const uint16_t* __restrict__ kg, const uint16_t* __restrict__ a,
                          const float* __restrict__ alpha, const float* __restrict__ beta,
                          const uint16_t* __restrict__ W, const float* __restrict__ w_r,
                          const float* H0, float* __restrict__ y, float* H_T,
@@ -88,10 +102,13 @@ __global__ void __launch_bounds__(256, 1)
   constexpr int V = 16 * VT;
   constexpr int NT = 2 * VT;  // n-tiles of 8 columns
   constexpr int M = 4 * VT;   // readout partial sums per thread
+  // Reduce-scatter width: M rounded up to a power of two (slots M .. MP-1 stay zero).
+  constexpr int MP = M <= 4 ? M : M <= 8 ? 8 : M <= 16 ? 16 : 32;
   constexpr int WS = V + 8;   // padded shared-memory row of W (bank-conflict-free ldmatrix)
 
   extern __shared__ __align__(128) uint8_t smem[];
-  const SmemLayout L = make_layout(K, V, Tc, WREG);
+  const int Kp = kRagged ? (int)(blockDim.x >> 1) : K;  // rows incl. padding (16 per warp)
+  const SmemLayout L = make_layout(Kp, V, Tc, WREG);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nthreads = blockDim.x;
   const int g = lane >> 2, c = lane & 3;
@@ -104,20 +121,42 @@ __global__ void __launch_bounds__(256, 1)
   float* wrs = reinterpret_cast<float*>(smem + L.wr);
   __nv_bfloat16* Ws = reinterpret_cast<__nv_bfloat16*>(smem + L.Ws);
   const float al = alpha[n], be = beta[n];
-  const uint32_t stage_tx = (uint32_t)(2 * K + V) * (uint32_t)Tc * 2u;
+  const uint32_t stage_tx = (uint32_t)((kRagged ? 0 : 2 * K) + V) * (uint32_t)Tc * 2u;
 
   auto issue = [&](int cc) {  // one thread: TMA of chunk cc's q, k, v into stage cc & 1
     const int st = cc & 1;
     uint8_t* base = smem + st * L.stage_bytes;
     mbar_arrive_expect_tx(&bar[st], stage_tx);
-    tma_load_4d(base + L.qs, &tm_q, &bar[st], 0, n * qk_hs, cc * Tc, b);
-    tma_load_4d(base + L.ks, &tm_k, &bar[st], 0, n * qk_hs, cc * Tc, b);
+    if constexpr (!kRagged) {
+      tma_load_4d(base + L.qs, &tm_q, &bar[st], 0, n * qk_hs, cc * Tc, b);
+      tma_load_4d(base + L.ks, &tm_k, &bar[st], 0, n * qk_hs, cc * Tc, b);
+    }
     tma_load_4d(base + L.vs, &tm_v, &bar[st], 0, n, cc * Tc, b);
+  };
+  // Ragged K, every thread: chunk cc's q and k rows into stage cc & 1, rows K .. Kp-1 and
+  // steps past T written as zeros.
+  auto stage_qk = [&](int cc) {
+    uint16_t* qd = reinterpret_cast<uint16_t*>(smem + (cc & 1) * L.stage_bytes + L.qs);
+    uint16_t* kd = reinterpret_cast<uint16_t*>(smem + (cc & 1) * L.stage_bytes + L.ks);
+    const size_t heads = qk_hs ? (size_t)N : 1;
+    for (int idx = tid; idx < Tc * Kp; idx += nthreads) {
+      const int s = idx / Kp, r = idx - s * Kp, t = cc * Tc + s;
+      uint16_t qv = 0, kv = 0;
+      if (t < T && r < K) {
+        const size_t off = (((size_t)b * T + t) * heads + (size_t)n * qk_hs) * K + r;
+        qv = qg[off];
+        kv = kg[off];
+      }
+      qd[idx] = qv;
+      kd[idx] = kv;
+    }
   };
 
   if (tid == 0) {
-    prefetch_tensormap(&tm_q);
-    prefetch_tensormap(&tm_k);
+    if constexpr (!kRagged) {
+      prefetch_tensormap(&tm_q);
+      prefetch_tensormap(&tm_k);
+    }
     prefetch_tensormap(&tm_v);
     mbar_init(&bar[0], 1);
     mbar_init(&bar[1], 1);
@@ -128,6 +167,8 @@ __global__ void __launch_bounds__(256, 1)
   if (tid == 0) {
     for (int cc = 0; cc < 2 && cc < nchunks; ++cc) issue(cc);
   }
+  if constexpr (kRagged)
+    for (int cc = 0; cc < 2 && cc < nchunks; ++cc) stage_qk(cc);
   const size_t pair_row = (size_t)b * T;  // (b, t) row index base
   for (int cc = 0; cc < 2 && cc < nchunks; ++cc)
     for (int t = tid; t < Tc; t += nthreads) {
@@ -162,13 +203,16 @@ __global__ void __launch_bounds__(256, 1)
   // H (fp32) in the accumulator layout: rows r0 = 16 warp + g and r1 = r0 + 8,
   // columns 8 nt + 2c and 8 nt + 2c + 1.
   const int r0 = 16 * warp + g, r1 = r0 + 8;
+  const bool in0 = r0 < K, in1 = r1 < K;  // false only for the padding rows of a ragged K
   float h[NT][4];
   if (H0) {
     const float* h0p = H0 + (size_t)pair * K * V;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      const float2 u = *reinterpret_cast<const float2*>(h0p + (size_t)r0 * V + 8 * nt + 2 * c);
-      const float2 w = *reinterpret_cast<const float2*>(h0p + (size_t)r1 * V + 8 * nt + 2 * c);
+      const float2 u = in0 ? *reinterpret_cast<const float2*>(h0p + (size_t)r0 * V + 8 * nt + 2 * c)
+                           : make_float2(0.f, 0.f);
+      const float2 w = in1 ? *reinterpret_cast<const float2*>(h0p + (size_t)r1 * V + 8 * nt + 2 * c)
+                           : make_float2(0.f, 0.f);
       h[nt][0] = u.x;
       h[nt][1] = u.y;
       h[nt][2] = w.x;
@@ -224,10 +268,10 @@ __global__ void __launch_bounds__(256, 1)
 
     for (int s = 0; s < steps; ++s) {
       const float2 fg = fgc[s];
-      const float k0 = bf16_bits_to_float(ks[s * K + r0]);
-      const float k1 = bf16_bits_to_float(ks[s * K + r1]);
-      const float q0 = bf16_bits_to_float(qs[s * K + r0]);
-      const float q1 = bf16_bits_to_float(qs[s * K + r1]);
+      const float k0 = bf16_bits_to_float(ks[s * Kp + r0]);
+      const float k1 = bf16_bits_to_float(ks[s * Kp + r1]);
+      const float q0 = bf16_bits_to_float(qs[s * Kp + r0]);
+      const float q1 = bf16_bits_to_float(qs[s * Kp + r1]);
 
       // Rank-1 write k_t v_t^T as the accumulator's initial value (Eq. (10)).
       float acc[NT][4];
@@ -271,28 +315,34 @@ __global__ void __launch_bounds__(256, 1)
         af[kt][2] = pack_bf16x2(h[2 * kt + 1][0], h[2 * kt + 1][1]);
         af[kt][3] = pack_bf16x2(h[2 * kt + 1][2], h[2 * kt + 1][3]);
       }
-      if constexpr (kCache) {  // H_t in bf16, streaming stores
+      if constexpr (kCache) {  // H_t in bf16, streaming stores (real rows only)
         uint16_t* hp = Hs + ((size_t)pair * T + t0 + s) * K * V;
 #pragma unroll
         for (int kt = 0; kt < VT; ++kt) {
-          __stcs(reinterpret_cast<unsigned int*>(hp + (size_t)r0 * V + 16 * kt + 2 * c), af[kt][0]);
-          __stcs(reinterpret_cast<unsigned int*>(hp + (size_t)r1 * V + 16 * kt + 2 * c), af[kt][1]);
-          __stcs(reinterpret_cast<unsigned int*>(hp + (size_t)r0 * V + 16 * kt + 8 + 2 * c), af[kt][2]);
-          __stcs(reinterpret_cast<unsigned int*>(hp + (size_t)r1 * V + 16 * kt + 8 + 2 * c), af[kt][3]);
+          if (in0) {
+            __stcs(reinterpret_cast<unsigned int*>(hp + (size_t)r0 * V + 16 * kt + 2 * c), af[kt][0]);
+            __stcs(reinterpret_cast<unsigned int*>(hp + (size_t)r0 * V + 16 * kt + 8 + 2 * c), af[kt][2]);
+          }
+          if (in1) {
+            __stcs(reinterpret_cast<unsigned int*>(hp + (size_t)r1 * V + 16 * kt + 2 * c), af[kt][1]);
+            __stcs(reinterpret_cast<unsigned int*>(hp + (size_t)r1 * V + 16 * kt + 8 + 2 * c), af[kt][3]);
+          }
         }
       }
       // Readout (Eq. (12)): this thread's two rows, weighted by q, per column.
-      float p[M];
+      float p[MP];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         p[2 * nt] = fmaf(q1, h[nt][2], q0 * h[nt][0]);
         p[2 * nt + 1] = fmaf(q1, h[nt][3], q0 * h[nt][1]);
       }
+#pragma unroll
+      for (int i = M; i < MP; ++i) p[i] = 0.f;
       // Reduce-scatter over the 8 row groups (lane bits 4, 3, 2).
 #pragma unroll
       for (int stg = 0; stg < 3; ++stg) {
         const int mask = 16 >> stg;
-        const int half = M >> (stg + 1);
+        const int half = MP >> (stg + 1);
         if (half >= 1) {
           const bool up = (lane & mask) != 0;
 #pragma unroll
@@ -308,12 +358,12 @@ __global__ void __launch_bounds__(256, 1)
       // Lane (g, c) now holds the sums of value slots m = m0 .. m0 + cnt - 1,
       // slot m being column 8 (m >> 1) + 2c + (m & 1).
       float* yrow = yp + s * V;
-      if constexpr (M >= 8) {
-        constexpr int cnt = M / 8;
+      if constexpr (MP >= 8) {
+        constexpr int cnt = MP / 8;
 #pragma unroll
         for (int i = 0; i < cnt; ++i) {
           const int m = cnt * g + i;
-          yrow[8 * (m >> 1) + 2 * c + (m & 1)] = p[i];
+          if (m < M) yrow[8 * (m >> 1) + 2 * c + (m & 1)] = p[i];
         }
       } else {
         if ((g & 1) == 0) {
@@ -327,7 +377,7 @@ __global__ void __launch_bounds__(256, 1)
     // y_t = sum over warps of the partials + w_r ⊙ v_t, as float4 rows.
     {
       constexpr int V4 = V / 4;
-      const int nw = K / 16;
+      const int nw = Kp / 16;
       for (int idx = tid; idx < steps * V4; idx += nthreads) {
         const int s = idx / V4, j = (idx - s * V4) * 4;
         const uint2 vv = *reinterpret_cast<const uint2*>(vs + s * V + j);
@@ -349,6 +399,7 @@ __global__ void __launch_bounds__(256, 1)
     __syncthreads();
     if (has_next) {
       if (tid == 0) issue(cc + 2);
+      if constexpr (kRagged) stage_qk(cc + 2);
       if (tid < Tc) fgs[st * Tc + tid] = gate_pair(a_next, al, be);
     }
   }
@@ -357,8 +408,10 @@ __global__ void __launch_bounds__(256, 1)
     float* hp = H_T + (size_t)pair * K * V;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      *reinterpret_cast<float2*>(hp + (size_t)r0 * V + 8 * nt + 2 * c) = make_float2(h[nt][0], h[nt][1]);
-      *reinterpret_cast<float2*>(hp + (size_t)r1 * V + 8 * nt + 2 * c) = make_float2(h[nt][2], h[nt][3]);
+      if (in0)
+        *reinterpret_cast<float2*>(hp + (size_t)r0 * V + 8 * nt + 2 * c) = make_float2(h[nt][0], h[nt][1]);
+      if (in1)
+        *reinterpret_cast<float2*>(hp + (size_t)r1 * V + 8 * nt + 2 * c) = make_float2(h[nt][2], h[nt][3]);
     }
   }
 }
@@ -375,50 +428,63 @@ bool make_map(EncodeTiledFn enc, CUtensorMap* map, const void* base, int inner, 
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int VT, bool WREG, bool kCache>
+template <int VT, bool WREG, bool kCache, bool kRagged>
 cudaError_t launch_vt_cache(const Problem& p, EncodeTiledFn enc, cudaStream_t stream) {
   const int V = 16 * VT;
+  const int Kp = (p.K + 15) & ~15;
   // Tc <= threads (one gate logit per thread and chunk), and the shared memory fits.
-  int Tc = min(V <= 64 ? 64 : 32, 2 * p.K);
-  SmemLayout L = make_layout(p.K, V, Tc, WREG);
+  int Tc = min(V <= 64 ? 64 : 32, 2 * Kp);
+  SmemLayout L = make_layout(Kp, V, Tc, WREG);
   while (L.total > 227 * 1024 && Tc > 8) {
     Tc /= 2;
-    L = make_layout(p.K, V, Tc, WREG);
+    L = make_layout(Kp, V, Tc, WREG);
   }
   CUtensorMap mq, mk, mv;
-  if (!make_map(enc, &mq, p.q, p.K, p.Nqk, p.T, p.B, Tc) ||
-      !make_map(enc, &mk, p.k, p.K, p.Nqk, p.T, p.B, Tc) ||
-      !make_map(enc, &mv, p.v, V, p.N, p.T, p.B, Tc))
+  memset(&mq, 0, sizeof(mq));
+  memset(&mk, 0, sizeof(mk));
+  if (!kRagged && (!make_map(enc, &mq, p.q, p.K, p.Nqk, p.T, p.B, Tc) ||
+                   !make_map(enc, &mk, p.k, p.K, p.Nqk, p.T, p.B, Tc)))
     return cudaErrorInvalidValue;
-  auto kern = fwd_bf16_mma_rowwarp<VT, WREG, kCache>;
+  if (!make_map(enc, &mv, p.v, V, p.N, p.T, p.B, Tc)) return cudaErrorInvalidValue;
+  auto kern = fwd_bf16_mma_rowwarp<VT, WREG, kCache, kRagged>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
   if (err != cudaSuccess) return err;
   const unsigned grid = (unsigned)p.B * (unsigned)p.N;
-  kern<<<grid, 2 * p.K, L.total, stream>>>(mq, mk, mv, (const uint16_t*)p.a, p.alpha, p.beta,
-                                           (const uint16_t*)p.W, p.w_r, p.H0, p.y, p.H_T,
-                                           static_cast<uint16_t*>(p.Hs), p.T, p.N, p.K, Tc,
-                                           p.Nqk == 1 ? 0 : 1, p.debug, p.status);
+  kern<<<grid, 2 * Kp, L.total, stream>>>(mq, mk, mv, (const uint16_t*)p.q, (const uint16_t*)p.k,
+                                          (const uint16_t*)p.a, p.alpha, p.beta,
+                                          (const uint16_t*)p.W, p.w_r, p.H0, p.y, p.H_T,
+                                          static_cast<uint16_t*>(p.Hs), p.T, p.N, p.K, Tc,
+                                          p.Nqk == 1 ? 0 : 1, p.debug, p.status);
   return cudaGetLastError();
 }
 
-template <int VT, bool WREG>
+template <int VT>
 cudaError_t launch_vt(const Problem& p, EncodeTiledFn enc, cudaStream_t stream) {
-  if (p.Hs) return launch_vt_cache<VT, WREG, true>(p, enc, stream);
-  return launch_vt_cache<VT, WREG, false>(p, enc, stream);
+  constexpr bool kWreg = VT <= 4;  // W as register B fragments up to V = 64, else shared memory
+  const bool ragged = p.K % 16 != 0;
+  if (p.Hs)
+    return ragged ? launch_vt_cache<VT, kWreg, true, true>(p, enc, stream)
+                  : launch_vt_cache<VT, kWreg, true, false>(p, enc, stream);
+  return ragged ? launch_vt_cache<VT, kWreg, false, true>(p, enc, stream)
+                : launch_vt_cache<VT, kWreg, false, false>(p, enc, stream);
 }
 
 }  // namespace
 
 bool mma_rowwarp_supports(int K, int V) {
-  return K >= 16 && K <= 128 && K % 16 == 0 && (V == 16 || V == 32 || V == 64 || V == 128);
+  return K >= 1 && K <= 128 && V >= 16 && V <= 128 && V % 16 == 0;
 }
 
 cudaError_t launch_fwd_bf16_mma_rowwarp(const Problem& p, EncodeTiledFn enc, cudaStream_t stream) {
   switch (p.V) {
-    case 16: return launch_vt<1, true>(p, enc, stream);
-    case 32: return launch_vt<2, true>(p, enc, stream);
-    case 64: return launch_vt<4, true>(p, enc, stream);
-    case 128: return launch_vt<8, false>(p, enc, stream);
+    case 16: return launch_vt<1>(p, enc, stream);
+    case 32: return launch_vt<2>(p, enc, stream);
+    case 48: return launch_vt<3>(p, enc, stream);
+    case 64: return launch_vt<4>(p, enc, stream);
+    case 80: return launch_vt<5>(p, enc, stream);
+    case 96: return launch_vt<6>(p, enc, stream);
+    case 112: return launch_vt<7>(p, enc, stream);
+    case 128: return launch_vt<8>(p, enc, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -13,10 +13,11 @@
 // bit for bit.
 //
 // Two kernels with that arithmetic:
-//  * decode_bf16_mma: one block per pair, K / 16 warps; each warp loads its 16 state rows
-//    straight from global memory into registers, and the block stages W through shared
-//    memory for the B fragments.  Any supported shape; small batches are bound by launch
-//    latency.
+//  * decode_bf16_mma: one block per pair, ceil(K / 16) warps; each warp loads its 16 state
+//    rows straight from global memory into registers, and the block stages W through shared
+//    memory for the B fragments.  Any 1 <= K <= 128 and V = 16, 32, ..., 128: the rows past
+//    K of the last warp are zero (zero state, k and q), stay zero through the step and are
+//    not stored.  Small batches are bound by launch latency.
 //  * decode_bf16_persist (K = V = 64, many pairs): persistent blocks stream the pairs'
 //    states and operands through a TMA-filled shared-memory ring (below); large batches are
 //    bound by HBM traffic (the state is read and written once).
@@ -35,23 +36,28 @@ namespace {
 
 constexpr int kMaxWarps = 8;  // K <= 128
 
-// MAXW: the most warps a launch uses (K / 16 <= MAXW).  Four-warp launches (K <= 64) with
-// V <= 64 are register-capped so that six blocks fit on an SM: more state loads in flight.
-// V = 128 keeps twice the state and accumulator per thread and is not capped.
-template <int VT, int MAXW>
-__global__ void __launch_bounds__(32 * MAXW, (MAXW <= 4 && VT <= 4) ? 6 : 1)
+// MAXW: the most warps a launch uses (ceil(K / 16) <= MAXW).  Four-warp launches (K <= 64)
+// with V <= 64 are register-capped so that six blocks fit on an SM: more state loads in
+// flight.  V > 64 keeps more state and accumulator per thread and is not capped.
+// RAG: K is not a multiple of 16 (the last warp's rows past K are padding); not capped
+// either, since the row masks would spill under the cap.
+template <int VT, int MAXW, bool RAG>
+__global__ void __launch_bounds__(32 * MAXW, (MAXW <= 4 && VT <= 4 && !RAG) ? 6 : 1)
     decode_bf16_mma(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
                     const uint16_t* __restrict__ v, const uint16_t* __restrict__ a,
                     const float* __restrict__ alpha, const float* __restrict__ beta,
                     const uint16_t* __restrict__ W, const float* __restrict__ w_r,
                     const float* H_in, float* H_out, float* __restrict__ y, int N, int Nqk, int K) {
   constexpr int V = 16 * VT, NT = 2 * VT, M = 4 * VT;
+  // Reduce-scatter width: M rounded up to a power of two (slots M .. MP-1 stay zero).
+  constexpr int MP = M <= 4 ? M : M <= 8 ? 8 : M <= 16 ? 16 : 32;
   __shared__ __align__(16) float ypart[MAXW][V];
-  const int nw = K / 16;
+  const int nw = (K + 15) / 16;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int pair = blockIdx.x, b = pair / N, n = pair - (pair / N) * N;
   const int g = lane >> 2, c = lane & 3;
   const int r0 = 16 * warp + g, r1 = r0 + 8;
+  const bool in0 = !RAG || r0 < K, in1 = !RAG || r1 < K;  // false only for padding rows
   const size_t qrow = (size_t)b * Nqk + (Nqk == 1 ? 0 : n);
   const size_t row = (size_t)b * N + n;
 
@@ -70,10 +76,10 @@ __global__ void __launch_bounds__(32 * MAXW, (MAXW <= 4 && VT <= 4) ? 6 : 1)
   const float* hin = H_in ? H_in + (size_t)pair * K * V : nullptr;
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
-    h[nt][0] = hin ? *reinterpret_cast<const float2*>(hin + (size_t)r0 * V + 8 * nt + 2 * c)
-                   : make_float2(0.f, 0.f);
-    h[nt][1] = hin ? *reinterpret_cast<const float2*>(hin + (size_t)r1 * V + 8 * nt + 2 * c)
-                   : make_float2(0.f, 0.f);
+    h[nt][0] = hin && in0 ? *reinterpret_cast<const float2*>(hin + (size_t)r0 * V + 8 * nt + 2 * c)
+                          : make_float2(0.f, 0.f);
+    h[nt][1] = hin && in1 ? *reinterpret_cast<const float2*>(hin + (size_t)r1 * V + 8 * nt + 2 * c)
+                          : make_float2(0.f, 0.f);
   }
   __syncthreads();
   const int lr = lane & 7, lq = lane >> 3;
@@ -83,8 +89,8 @@ __global__ void __launch_bounds__(32 * MAXW, (MAXW <= 4 && VT <= 4) ? 6 : 1)
   // P = k v^T + bf16(H) W
   float2 acc[NT][2];
   {
-    const float kv0 = bf16_bits_to_float(k[qrow * K + r0]);
-    const float kv1 = bf16_bits_to_float(k[qrow * K + r1]);
+    const float kv0 = in0 ? bf16_bits_to_float(k[qrow * K + r0]) : 0.f;
+    const float kv1 = in1 ? bf16_bits_to_float(k[qrow * K + r1]) : 0.f;
     const float2 k0 = make_float2(kv0, kv0), k1 = make_float2(kv1, kv1);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
@@ -121,16 +127,16 @@ __global__ void __launch_bounds__(32 * MAXW, (MAXW <= 4 && VT <= 4) ? 6 : 1)
   if (hout) {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      *reinterpret_cast<float2*>(hout + (size_t)r0 * V + 8 * nt + 2 * c) = h[nt][0];
-      *reinterpret_cast<float2*>(hout + (size_t)r1 * V + 8 * nt + 2 * c) = h[nt][1];
+      if (in0) *reinterpret_cast<float2*>(hout + (size_t)r0 * V + 8 * nt + 2 * c) = h[nt][0];
+      if (in1) *reinterpret_cast<float2*>(hout + (size_t)r1 * V + 8 * nt + 2 * c) = h[nt][1];
     }
   }
   // y = H'^T q + w_r ⊙ v: q-weighted sums of this thread's two rows, reduce-scattered
   // over the warp's 8 row groups (same stages and order as the forward kernel).
-  const float qv0 = bf16_bits_to_float(q[qrow * K + r0]);
-  const float qv1 = bf16_bits_to_float(q[qrow * K + r1]);
+  const float qv0 = in0 ? bf16_bits_to_float(q[qrow * K + r0]) : 0.f;
+  const float qv1 = in1 ? bf16_bits_to_float(q[qrow * K + r1]) : 0.f;
   const float2 q0 = make_float2(qv0, qv0), q1 = make_float2(qv1, qv1);
-  float p[M];
+  float p[MP];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     const float2 pp = fma2(q1, h[nt][1], mul2(q0, h[nt][0]));
@@ -138,9 +144,11 @@ __global__ void __launch_bounds__(32 * MAXW, (MAXW <= 4 && VT <= 4) ? 6 : 1)
     p[2 * nt + 1] = pp.y;
   }
 #pragma unroll
+  for (int i = M; i < MP; ++i) p[i] = 0.f;
+#pragma unroll
   for (int stg = 0; stg < 3; ++stg) {
     const int mask = 16 >> stg;
-    const int half = M >> (stg + 1);
+    const int half = MP >> (stg + 1);
     if (half >= 1) {
       const bool up = (lane & mask) != 0;
 #pragma unroll
@@ -153,12 +161,12 @@ __global__ void __launch_bounds__(32 * MAXW, (MAXW <= 4 && VT <= 4) ? 6 : 1)
       p[0] += __shfl_xor_sync(0xffffffffu, p[0], mask);
     }
   }
-  if constexpr (M >= 8) {
-    constexpr int cnt = M / 8;
+  if constexpr (MP >= 8) {
+    constexpr int cnt = MP / 8;
 #pragma unroll
     for (int i = 0; i < cnt; ++i) {
       const int m = cnt * g + i;
-      ypart[warp][8 * (m >> 1) + 2 * c + (m & 1)] = p[i];
+      if (m < M) ypart[warp][8 * (m >> 1) + 2 * c + (m & 1)] = p[i];
     }
   } else {
     if ((g & 1) == 0) {
@@ -182,7 +190,7 @@ __global__ void __launch_bounds__(32 * MAXW, (MAXW <= 4 && VT <= 4) ? 6 : 1)
 // kPS shared-memory stages with TMA, and writes the pair's gate (f, 1 - f) into the stage,
 // so that the state loads of later pairs are in flight while four compute warps update the
 // current one.  The per-element arithmetic and the
-// readout order are those of decode_bf16_mma<4, 4> above (bit for bit); only the operands'
+// readout order are those of decode_bf16_mma<4, 4, false> above (bit for bit); only the operands'
 // path differs (shared memory filled by TMA instead of per-thread global loads).
 constexpr int kPS = 2;                  // stages per block
 constexpr int kPBlocks = 3;             // blocks per SM
@@ -190,8 +198,8 @@ constexpr int kPStage = 25 * 1024;      // state 16 KB + W 8 KB + q, k, v, gate;
 constexpr int kPH = 0, kPW = 16384, kPQ = 24576, kPK = kPQ + 128, kPV = kPK + 128;
 constexpr int kPG = kPV + 128;          // float2 (f, 1 - f), written by the producer
 constexpr int kPYpart = kPS * kPStage;  // float [2][4][64] readout partials (double buffer)
-constexpr int kPBar = kPYpart + 2 * 4 * 64 * 4;
-constexpr int kPSmem = kPBar + 2 * kPS * 8 + 1024;  // + slack to align the base to 1024
+constexpr int kPBar = kPYpart + 2 * 4 * 64 * 4;  // full[kPS], empty[kPS], never, abort flag
+constexpr int kPSmem = kPBar + (2 * kPS + 2) * 8 + 1024;  // + slack to align the base to 1024
 
 __global__ void __launch_bounds__(160, kPBlocks)
     decode_bf16_persist(const __grid_constant__ CUtensorMap tm_h,
@@ -201,13 +209,16 @@ __global__ void __launch_bounds__(160, kPBlocks)
                         const __grid_constant__ CUtensorMap tm_v, const uint16_t* __restrict__ a,
                         const float* __restrict__ alpha, const float* __restrict__ beta,
                         const float* __restrict__ w_r, bool has_h, float* H_out,
-                        float* __restrict__ y, int npairs, int N, int Nqk, int* status) {
+                        float* __restrict__ y, int npairs, int N, int Nqk, int debug,
+                        int* status) {
   constexpr int V = 64, NT = 8, M = 16;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   float* ypart = reinterpret_cast<float*>(smem + kPYpart);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kPBar);
   uint64_t* empty = full + kPS;
+  uint64_t* never = empty + kPS;  // never armed: the forced-timeout test hook waits on it
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(never + 1);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const long long limit = kWaitLimitCycles;
   if (threadIdx.x == 0) {
@@ -215,6 +226,8 @@ __global__ void __launch_bounds__(160, kPBlocks)
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 4);
     }
+    mbar_init(never, 1);
+    *abort_flag = 0;
     fence_mbar_init();
   }
   __syncthreads();
@@ -246,8 +259,9 @@ __global__ void __launch_bounds__(160, kPBlocks)
           aln = alpha[nn];
           ben = beta[nn];
         }
+        // Gives up early once the compute warps have stopped (their own wait gave up).
         if (i >= kPS)
-          ok = mbar_wait_bounded_sleep(&empty[st], (uint32_t)((i / kPS) - 1) & 1u, limit);
+          ok = wait_or_abort_sleep(&empty[st], (uint32_t)((i / kPS) - 1) & 1u, limit, abort_flag);
         if (!ok) break;
         uint8_t* base = smem + st * kPStage;
         *reinterpret_cast<float2*>(base + kPG) = gate_fg(ac, alc, bec);
@@ -279,9 +293,12 @@ __global__ void __launch_bounds__(160, kPBlocks)
   for (int i = 0; p < npairs; ++i, p += gridDim.x) {
     const int st = i % kPS, n = p - (p / N) * N;
     // A joint decision, so that no warp is left alone at the named barrier below.
-    const bool wok = mbar_wait_bounded(&full[st], (uint32_t)(i / kPS) & 1u, limit);
+    bool wok = mbar_wait_bounded(&full[st], (uint32_t)(i / kPS) & 1u, limit);
+    if ((debug & kDebugForceTimeout) && i == 0)
+      wok = wok && mbar_wait_bounded(never, 0u, kDebugWaitLimitCycles);
     if (named_bar_or(2, 128, !wok)) {
       if (lane == 0) atomicExch(status, kStatusTimeout);
+      if (threadIdx.x == 0) *abort_flag = 1;  // releases the producer's wait for a free stage
       break;
     }
     const uint8_t* base = smem + st * kPStage;
@@ -391,8 +408,7 @@ __global__ void __launch_bounds__(160, kPBlocks)
 }  // namespace
 
 bool decode_supports(int K, int V) {
-  return K >= 16 && K <= 16 * kMaxWarps && K % 16 == 0 &&
-         (V == 16 || V == 32 || V == 64 || V == 128);
+  return K >= 1 && K <= 16 * kMaxWarps && V >= 16 && V <= 128 && V % 16 == 0;
 }
 
 bool make_map_dec(EncodeTiledFn enc, CUtensorMap* map, CUtensorMapDataType dt, const void* base,
@@ -408,12 +424,14 @@ bool make_map_dec(EncodeTiledFn enc, CUtensorMap* map, CUtensorMapDataType dt, c
 
 bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
 
-// The persistent form: K = V = 64, enough pairs to fill every SM twice over, and the
-// 16-byte alignment TMA needs.  Returns false (nothing launched) when it does not apply.
+// The persistent form: K = V = 64, enough pairs to fill every SM twice over (unless
+// `force`), and the 16-byte alignment TMA needs.  Returns false (nothing launched) when it
+// does not apply.
 bool launch_decode_persist(const Problem& p, EncodeTiledFn enc, cudaStream_t stream,
-                           cudaError_t* err) {
+                           cudaError_t* err, bool force) {
   const long long npairs = (long long)p.B * p.N;
-  if (p.K != 64 || p.V != 64 || !enc || !p.status || npairs < 2048 || npairs > 0x7fffffffLL)
+  if (p.K != 64 || p.V != 64 || !enc || !p.status || (!force && npairs < 2048) ||
+      npairs > 0x7fffffffLL)
     return false;
   if (!aligned16(p.q) || !aligned16(p.k) || !aligned16(p.v) || !aligned16(p.W) ||
       !aligned16(p.H_T) || (p.H0 && !aligned16(p.H0)))
@@ -448,28 +466,49 @@ bool launch_decode_persist(const Problem& p, EncodeTiledFn enc, cudaStream_t str
   const unsigned grid = (unsigned)std::min<long long>(npairs, (long long)kPBlocks * sms);
   decode_bf16_persist<<<grid, 160, kPSmem, stream>>>(
       mh, mw, mq, mk, mv, (const uint16_t*)p.a, p.alpha, p.beta, p.w_r, p.H0 != nullptr, p.H_T,
-      p.y, (int)npairs, p.N, p.Nqk, p.status);
+      p.y, (int)npairs, p.N, p.Nqk, p.debug, p.status);
   *err = cudaGetLastError();
   return true;
 }
 
-cudaError_t launch_decode_bf16(const Problem& p, EncodeTiledFn enc, cudaStream_t stream) {
+bool decode_persist_supports(const Problem& p) {
+  return p.K == 64 && p.V == 64 && aligned16(p.q) && aligned16(p.k) && aligned16(p.v) &&
+         aligned16(p.W) && aligned16(p.H_T) && (!p.H0 || aligned16(p.H0));
+}
+
+cudaError_t launch_decode_bf16(const Problem& p, EncodeTiledFn enc, cudaStream_t stream,
+                               int which) {
   cudaError_t perr = cudaSuccess;
-  if (launch_decode_persist(p, enc, stream, &perr)) return perr;
+  if (which != 1 && launch_decode_persist(p, enc, stream, &perr, which == 2)) return perr;
+  if (which == 2) return cudaErrorInvalidValue;
   const unsigned grid = (unsigned)p.B * (unsigned)p.N;
-  const unsigned threads = 32u * (unsigned)(p.K / 16);
+  const unsigned threads = 32u * (unsigned)((p.K + 15) / 16);
   auto args = [&](auto kern) {
     kern<<<grid, threads, 0, stream>>>((const uint16_t*)p.q, (const uint16_t*)p.k,
                                        (const uint16_t*)p.v, (const uint16_t*)p.a, p.alpha, p.beta,
                                        (const uint16_t*)p.W, p.w_r, p.H0, p.H_T, p.y, p.N, p.Nqk,
                                        p.K);
   };
-  const bool small = p.K <= 64;
+  const bool small = p.K <= 64, rag = p.K % 16 != 0;
+  auto pick = [&](auto k4, auto k8, auto k4r, auto k8r) {
+    if (rag) small ? args(k4r) : args(k8r);
+    else small ? args(k4) : args(k8);
+  };
+#define M2RNN_DECODE_CASE(VT)                                                                  \
+  case 16 * VT:                                                                                \
+    pick(decode_bf16_mma<VT, 4, false>, decode_bf16_mma<VT, kMaxWarps, false>,                 \
+         decode_bf16_mma<VT, 4, true>, decode_bf16_mma<VT, kMaxWarps, true>);                  \
+    break;
   switch (p.V) {
-    case 16: small ? args(decode_bf16_mma<1, 4>) : args(decode_bf16_mma<1, kMaxWarps>); break;
-    case 32: small ? args(decode_bf16_mma<2, 4>) : args(decode_bf16_mma<2, kMaxWarps>); break;
-    case 64: small ? args(decode_bf16_mma<4, 4>) : args(decode_bf16_mma<4, kMaxWarps>); break;
-    case 128: small ? args(decode_bf16_mma<8, 4>) : args(decode_bf16_mma<8, kMaxWarps>); break;
+    M2RNN_DECODE_CASE(1)
+    M2RNN_DECODE_CASE(2)
+    M2RNN_DECODE_CASE(3)
+    M2RNN_DECODE_CASE(4)
+    M2RNN_DECODE_CASE(5)
+    M2RNN_DECODE_CASE(6)
+    M2RNN_DECODE_CASE(7)
+    M2RNN_DECODE_CASE(8)
+#undef M2RNN_DECODE_CASE
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();

@@ -19,6 +19,12 @@ constexpr long long kWaitLimitCycles = 2000000000LL;
 // Limit used by the forced-timeout test hook (about 0.5 ms).
 constexpr long long kDebugWaitLimitCycles = 1000000LL;
 
+// Unique id of the calling thread's current CUDA context (cuCtxGetId), or false when no
+// context is current yet.  Device addresses of module symbols are cached per context id,
+// so a device reset (which ends the context and may reload the module elsewhere) makes
+// the next call resolve them again.
+bool current_context_id(unsigned long long* id);
+
 struct Problem {
   const void* q;
   const void* k;
@@ -131,8 +137,13 @@ cudaError_t launch_bwd_bf16_tcc(const BackwardProblem& p, EncodeTiledFn enc, int
 // Uses q, k, v, a, alpha, beta, W, w_r, H0 (state in, may be null), H_T (state out, may
 // equal H0), y, B, N, K, V, Nqk and status of the problem.  K = V = 64 with at least 2048
 // pairs takes a persistent TMA-fed kernel (same arithmetic); `enc` may be null.
+// `which`: 0 picks (persistent kernel at K = V = 64 with >= 2048 pairs), 1 forces the
+// one-block-per-pair kernel, 2 the persistent kernel (decode_persist_supports must hold).
+// The persistent kernel honours p.debug (kDebugForceTimeout).
 bool decode_supports(int K, int V);
-cudaError_t launch_decode_bf16(const Problem& p, EncodeTiledFn enc, cudaStream_t stream);
+bool decode_persist_supports(const Problem& p);
+cudaError_t launch_decode_bf16(const Problem& p, EncodeTiledFn enc, cudaStream_t stream,
+                               int which);
 
 // Block prologue / epilogue (memory-bound): causal depthwise Conv1D (kernel 4) + SiLU
 // over [B, T, C] bf16 (C % 8 == 0), and the output gate + RMSNorm over rows of D

@@ -15,9 +15,12 @@
 //    threads, with no ordering between them) race on it and give wrong results;
 //    calls must be ordered (one stream, or events).
 //  * The first call on a device resolves the scratch address with
-//    cudaGetSymbolAddress (once per device, under a mutex).  That call may load the
-//    module, which is not allowed while a stream is being captured: make one call
-//    on each device before capturing it into a CUDA graph.
+//    cudaGetSymbolAddress (under a mutex) and caches it for the current CUDA context.
+//    That call may load the module, which is not allowed while a stream is being
+//    captured: make one call on each device before capturing it into a CUDA graph.
+//    A later call under another context (after cudaDeviceReset, say, which ends the
+//    context and unloads the module) resolves the address again instead of handing the
+//    kernels a stale one; that call, too, must come before any capture.
 #include <mutex>
 
 #include "../../include/m2rnn.h"
@@ -31,18 +34,24 @@ static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchFloats];
 
 constexpr int kMaxDevices = 64;
 
-// Device address of this device's scratch array, resolved once per device.
+// Device address of this device's scratch array, cached per CUDA context: a new context
+// on the device (the module reloaded, possibly at another address) is resolved again.
 float* scratch_address(int dev) {
-  static float* addr[kMaxDevices] = {};
+  struct Entry {
+    unsigned long long ctx;
+    float* addr;
+  };
+  static Entry cache[kMaxDevices] = {};
   static std::mutex mu;
   if (dev < 0 || dev >= kMaxDevices) return nullptr;
   std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
-    addr[dev] = static_cast<float*>(p);
-  }
-  return addr[dev];
+  unsigned long long id = 0;
+  const bool have_id = current_context_id(&id);
+  if (have_id && cache[dev].addr && cache[dev].ctx == id) return cache[dev].addr;
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+  if (have_id || current_context_id(&id)) cache[dev] = Entry{id, static_cast<float*>(p)};
+  return static_cast<float*>(p);
 }
 
 }  // namespace

@@ -39,6 +39,7 @@ SYMBOLS = {
     "m2rnn_backward_bf16": (_I, [_P] * 21 + [_I] * 7 + [_P, ctypes.c_size_t, _P]),
     "m2rnn_backward_bf16_noalloc": (_I, [_P] * 21 + [_I] * 6 + [_P]),
     "m2rnn_decode_step_bf16": (_I, [_P] * 11 + [_I] * 5 + [_P]),
+    "m2rnn_decode_step_bf16_variant": (_I, [_P] * 11 + [_I] * 6 + [_P]),
     "m2rnn_conv_silu_bf16": (_I, [_P] * 4 + [_I] * 3 + [_P]),
     "m2rnn_gate_rmsnorm_bf16": (_I, [_P] * 3 + [ctypes.c_float, _P, ctypes.c_longlong, _I, _P]),
 }
@@ -318,10 +319,12 @@ def m2rnn_backward_noalloc(inputs: dict, Hs, dy, dH_T=None, grads=None, stream=N
     return out
 
 
-def m2rnn_decode_step(q, k, v, a, alpha, beta, W, w_r, H_in, H_out=None, y=None, stream=None):
+def m2rnn_decode_step(q, k, v, a, alpha, beta, W, w_r, H_in, H_out=None, y=None, stream=None,
+                      variant=0):
     """One decode step (bf16 operands): q, k [B, Nqk, K]; v [B, N, V]; a [B, N]; state
     H_in [B, N, K, V] float32 (None: zero).  Writes H_out (defaults to H_in, in place,
-    when H_in is given) and y [B, N, V]; returns (y, H_out)."""
+    when H_in is given) and y [B, N, V]; returns (y, H_out).  variant: 0 automatic,
+    1 one block per pair, 2 the persistent kernel (K = V = 64)."""
     lib = load_library()
     B, Nqk, K = q.shape
     N, V = v.shape[1], v.shape[2]
@@ -344,9 +347,13 @@ def m2rnn_decode_step(q, k, v, a, alpha, beta, W, w_r, H_in, H_out=None, y=None,
     if y is None:
         y = torch.empty((B, N, V), dtype=torch.float32, device=dev)
     _check(y, "y", torch.float32, (B, N, V), dev)
-    st = lib.m2rnn_decode_step_bf16(*[_ptr(x) for x in (q, k, v, a, alpha, beta, W, w_r, H_in,
-                                                        H_out, y)],
-                                    B, N, Nqk, K, V, ctypes.c_void_p(_stream_ptr(stream)))
+    ptrs = [_ptr(x) for x in (q, k, v, a, alpha, beta, W, w_r, H_in, H_out, y)]
+    if variant == 0:
+        st = lib.m2rnn_decode_step_bf16(*ptrs, B, N, Nqk, K, V,
+                                        ctypes.c_void_p(_stream_ptr(stream)))
+    else:
+        st = lib.m2rnn_decode_step_bf16_variant(*ptrs, B, N, Nqk, K, V, int(variant),
+                                                ctypes.c_void_p(_stream_ptr(stream)))
     if st != OK:
         raise M2RNNError(st, "m2rnn_decode_step_bf16")
     return y, H_out

@@ -69,8 +69,21 @@ def test_variant_support_table(lib):
 
 def test_pick_variant_host_logic(lib):
     assert binding.pick_variant(8, 16384, 16, 64, 64) > 0
-    assert binding.pick_variant(1, 64, 2, 8, 8) == 0       # K = 8: only the fp32 path
-    assert binding.pick_variant(1, 64, 2, 64, 48) == 0     # V not supported by the MMA paths
+    assert binding.pick_variant(1, 64, 2, 8, 8) == 0       # V = 8: not a multiple of 16
+    assert binding.pick_variant(1, 64, 2, 64, 40) == 0     # V = 40: not a multiple of 16
+    assert binding.pick_variant(1, 64, 2, 129, 64) == 0    # K > 128
+    assert binding.pick_variant(1, 64, 2, 64, 144) == 0    # V > 128
+
+
+# Every 1 <= K <= 128 and every V that is a multiple of 16 up to 128 has a bf16 kernel
+# (ragged K on the row-warp kernel with zero padding rows).
+@pytest.mark.parametrize("K", [1, 8, 17, 24, 40, 64, 100, 127, 128])
+@pytest.mark.parametrize("V", [16, 32, 48, 64, 80, 96, 112, 128])
+def test_every_contract_shape_has_a_variant(lib, K, V):
+    v = binding.pick_variant(2, 100, 3, K, V)
+    assert v > 0, (K, V)
+    assert binding.variant_supports(v, 2, 100, 3, K, V)
+    assert binding.variant_supports(1, 2, 100, 3, K, V)   # the row-warp kernel takes them all
 
 
 NULL = None
@@ -114,8 +127,8 @@ def test_f32_too_large_is_unsupported(lib, dims):
     assert call_f32(lib, fake_ptrs(), dims) == binding.ERR_UNSUPPORTED
 
 
-@pytest.mark.parametrize("dims", [(1, 4, 1, 8, 16), (1, 4, 1, 24, 16), (1, 4, 1, 16, 48),
-                                  (1, 4, 1, 144, 64), (1, 4, 1, 64, 256)])
+@pytest.mark.parametrize("dims", [(1, 4, 1, 129, 16), (1, 4, 1, 16, 40), (1, 4, 1, 16, 8),
+                                  (1, 4, 1, 144, 64), (1, 4, 1, 64, 256), (1, 4, 1, 24, 136)])
 def test_bf16_unsupported_shapes(lib, dims):
     assert call_bf16(lib, fake_ptrs(), dims) == binding.ERR_UNSUPPORTED
 
@@ -177,8 +190,8 @@ def test_forward_train_argument_checks(lib):
     p[11] = None                                   # Hs missing with T > 0
     assert lib.m2rnn_forward_train_f32(*p, 1, 4, 1, 1, 8, 8, None) == binding.ERR_INVALID_ARG
     p = fake_ptrs(12)
-    assert lib.m2rnn_forward_train_bf16(*p, 1, 4, 1, 1, 24, 64, None) == binding.ERR_UNSUPPORTED
-    assert lib.m2rnn_forward_train_bf16(*p, 1, 4, 1, 1, 64, 96, None) == binding.ERR_UNSUPPORTED
+    assert lib.m2rnn_forward_train_bf16(*p, 1, 4, 1, 1, 129, 64, None) == binding.ERR_UNSUPPORTED
+    assert lib.m2rnn_forward_train_bf16(*p, 1, 4, 1, 1, 64, 40, None) == binding.ERR_UNSUPPORTED
 
 
 def test_decode_argument_checks(lib):
@@ -186,10 +199,13 @@ def test_decode_argument_checks(lib):
     pp = list(p)
     pp[9] = None                                   # H_out
     assert lib.m2rnn_decode_step_bf16(*pp, 2, 3, 3, 64, 64, None) == binding.ERR_INVALID_ARG
-    assert lib.m2rnn_decode_step_bf16(*p, 2, 3, 3, 24, 64, None) == binding.ERR_UNSUPPORTED
-    assert lib.m2rnn_decode_step_bf16(*p, 2, 3, 3, 64, 96, None) == binding.ERR_UNSUPPORTED
+    assert lib.m2rnn_decode_step_bf16(*p, 2, 3, 3, 129, 64, None) == binding.ERR_UNSUPPORTED
+    assert lib.m2rnn_decode_step_bf16(*p, 2, 3, 3, 64, 40, None) == binding.ERR_UNSUPPORTED
     assert lib.m2rnn_decode_step_bf16(*p, 2, 3, 3, 144, 128, None) == binding.ERR_UNSUPPORTED
     assert lib.m2rnn_decode_step_bf16(*p, 2, 3, 2, 64, 64, None) == binding.ERR_INVALID_ARG
+    v = lib.m2rnn_decode_step_bf16_variant
+    assert v(*p, 2, 3, 3, 64, 64, 3, None) == binding.ERR_INVALID_ARG      # unknown kernel
+    assert v(*p, 2, 3, 3, 64, 40, 1, None) == binding.ERR_UNSUPPORTED
 
 
 def test_block_argument_checks(lib):

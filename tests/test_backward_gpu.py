@@ -106,7 +106,11 @@ def test_forward_train_keeps_states_and_matches_plain_forward():
     for dtype, shape, fwd_variant in [("f32", (2, 37, 3, 8, 24), 0), ("bf16", (2, 150, 3, 64, 64), 0),
                                       ("bf16", (1, 70, 2, 32, 16), 0),
                                       ("bf16", (2, 45, 2, 64, 128), 1),
-                                      ("bf16", (1, 33, 2, 128, 128), 1)]:
+                                      ("bf16", (1, 33, 2, 128, 128), 1),
+                                      # ragged K and V off the power-of-two grid (row-warp)
+                                      ("bf16", (2, 40, 2, 24, 48), 0),
+                                      ("bf16", (1, 30, 1, 100, 112), 0),
+                                      ("bf16", (1, 20, 3, 1, 16), 0)]:
         B, T, N, K, V = shape
         wl = Workload("tr", B, T, N, K, V, dtype=dtype, h0="uniform", rescale_w=dtype == "bf16")
         inp = make_inputs(wl, DEV, 7)
@@ -124,7 +128,9 @@ BF16_SHAPES = [(1, 1, 1, 16, 16), (2, 65, 3, 64, 64), (1, 130, 2, 32, 32), (2, 4
                (1, 7, 2, 64, 64), (1, 24, 2, 64, 128), (1, 12, 1, 128, 128), (1, 10, 2, 96, 128),
                # chunk edges of the 8-step backward chunks: exactly one, one plus one step,
                # exactly two, and a two-step sequence
-               (1, 8, 2, 64, 64), (1, 9, 1, 64, 64), (1, 16, 2, 64, 64), (2, 2, 1, 64, 64)]
+               (1, 8, 2, 64, 64), (1, 9, 1, 64, 64), (1, 16, 2, 64, 64), (2, 2, 1, 64, 64),
+               # ragged K, V of 48 / 80 (row-warp state-keeping forward, SIMT backward)
+               (1, 20, 2, 24, 48), (2, 15, 1, 1, 80)]
 
 
 def bwd_variants(K, V):
@@ -205,3 +211,42 @@ def test_backward_empty_sequence():
     assert torch.equal(g["dH0"], dHT)
     for n in ("dW", "dw_r", "dalpha", "dbeta"):
         assert float(g[n].abs().max()) == 0.0
+
+
+def abs_err(got, want):
+    got = got.double().cpu().numpy() if torch.is_tensor(got) else np.asarray(got)
+    want = np.asarray(want, np.float64)
+    return float(np.abs(got - want).max()) if want.size else 0.0
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("shape,shared,variant", [
+    # the training workload's length and head shape on the tensor-core backward (auto = 5)
+    ((1, 16384, 4, 64, 64), False, 0),
+    ((1, 16384, 4, 64, 64), True, 0),
+    # V = 128 at a long T on the SIMT backward (the kernel that differentiates V = 128)
+    ((1, 4096, 2, 64, 128), False, 0),
+])
+def test_backward_bf16_at_training_length(shape, shared, variant):
+    """Every gradient tensor against the fp64 backward oracle over the whole sequence:
+    thousands of wraps of the 8-step chunk ring and of the state-history stream, so an
+    error that grows along the reverse scan would show.  The bar is the bf16 path's 3e-2
+    on the max-abs error scaled by max(1, max |oracle|); the unscaled max-abs error and
+    the oracle's magnitude are printed beside it."""
+    B, T, N, K, V = shape
+    wl = Workload("bwdT", B, T, N, K, V, h0="zero", shared_qk=shared)
+    inp = make_inputs(wl, DEV, 21)
+    _, _, Hs = pkg.m2rnn_forward_train(inp)
+    dy, dHT = upstream(B, T, N, K, V, 22)
+    g = pkg.m2rnn_backward(inp, Hs, dy, dHT, variant=variant)
+    assert pkg.stream_status() == binding.OK
+    ref = m2rnn_backward_inputs(all_f64(inp), dy.double().cpu().numpy(),
+                                dHT.double().cpu().numpy())
+    worst = 0.0
+    for n in GRADS:
+        scaled, unscaled = rel_err(g[n], ref[n]), abs_err(g[n], ref[n])
+        mag = float(np.abs(np.asarray(ref[n])).max())
+        print(f"{shape} shared={shared} {n}: scaled {scaled:.3e}  max-abs {unscaled:.3e}  "
+              f"max|oracle| {mag:.3e}")
+        worst = max(worst, scaled)
+    assert worst <= TOL["bf16"]

@@ -33,3 +33,42 @@ def test_traffic_scales_with_units_and_needs_the_captured_source(monkeypatch):
     monkeypatch.setattr(bench, "kernel_source_hash", lambda name: "0" * 64)
     assert bench.measured_traffic("mma_sync_pipelined", wl) is None
     assert bench.measured_traffic("no_such_kernel", wl) is None
+
+
+def test_pair_blocks_cover_every_pair_once_and_reproduce_the_oracle():
+    """The CPU baseline splits the pairs over processes; each block through the oracle gives
+    exactly its slice of the full problem's outputs (pairs are independent)."""
+    import numpy as np
+    from matrix_state_nonlinear_gb300.inputs import make_inputs
+    from oracle import m2rnn_forward
+    for shared in (False, True):
+        wl = Workload("blk", 3, 9, 5, 8, 16, h0="uniform", shared_qk=shared)
+        arrs = bench.host_arrays(make_inputs(wl, "cpu", 0))
+        f = {k: bench._as_f64(v) for k, v in arrs.items()}
+        y, HT = m2rnn_forward(f["q"], f["k"], f["v"], f["a"], f["alpha"], f["beta"], f["W"],
+                              f["w_r"], f["H0"])
+        for parts in (1, 4, 7, 16, 40):
+            blocks = bench.pair_blocks(arrs, parts)
+            assert len(blocks) <= parts
+            seen = np.zeros((3, 5), int)
+            for (b0, b1, n0, n1), blk in blocks:
+                seen[b0:b1, n0:n1] += 1
+                g = {k: bench._as_f64(v) for k, v in blk.items()}
+                yb, Hb = m2rnn_forward(g["q"], g["k"], g["v"], g["a"], g["alpha"], g["beta"],
+                                       g["W"], g["w_r"], g["H0"])
+                assert np.array_equal(yb, y[b0:b1, :, n0:n1])
+                assert np.array_equal(Hb, HT[b0:b1, n0:n1])
+            assert (seen == 1).all()
+
+
+def test_oracle_pool_runs_blocks_in_spawned_processes():
+    wl = Workload("pool", 2, 6, 3, 8, 16, h0="uniform")
+    from matrix_state_nonlinear_gb300.inputs import make_inputs
+    pool = bench.OraclePool(2)
+    try:
+        wall, cpu = pool.run("forward", bench.host_arrays(make_inputs(wl, "cpu", 0)))
+    finally:
+        pool.close()
+    assert wall > 0 and cpu >= 0
+    info = bench.host_cores()
+    assert info["host_cpu_count"] >= 1 and info["affinity_cores"] >= 1

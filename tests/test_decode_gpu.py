@@ -38,6 +38,9 @@ def step_args(inp, t):
                                           ((2, 9, 4, 48, 32), True), ((1, 70, 2, 16, 64), False),
                                           ((96, 3, 8, 64, 64), False), ((40, 2, 16, 32, 16), True),
                                           ((70, 2, 9, 48, 32), False),
+                                          # ragged K and V (row-warp forward)
+                                          ((2, 9, 3, 24, 48), False), ((3, 5, 2, 1, 16), True),
+                                          ((2, 6, 2, 100, 96), False), ((2, 4, 2, 40, 80), False),
                                           # >= 2048 pairs at K = V = 64: the persistent kernel
                                           ((160, 2, 16, 64, 64), False), ((130, 3, 16, 64, 64), True)])
 def test_decode_steps_reproduce_the_forward_bitwise(shape, shared):
@@ -101,3 +104,37 @@ def test_decode_cuda_graph_replay(B, N):
     assert torch.equal(H, H_eager)
     for t in range(T):
         assert torch.equal(ys[t], ys_eager[t]), t
+
+
+@pytest.mark.parametrize("B, N", [(4, 4), (160, 16)])   # 16 pairs; 2560 pairs
+def test_decode_kernels_agree_bitwise(B, N):
+    """The per-pair kernel and the persistent kernel (forced at any pair count) give the
+    same bits."""
+    inp = make_inputs(Workload("decv", B, 1, N, 64, 64, h0="uniform"), DEV, 9)
+    outs = []
+    for variant in (1, 2):
+        H = torch.empty_like(inp["H0"])
+        y, _ = pkg.m2rnn_decode_step(*step_args(inp, 0), inp["H0"], H_out=H, variant=variant)
+        assert pkg.stream_status() == binding.OK
+        outs.append((y, H))
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+
+
+def test_persistent_decode_forced_timeout_is_reported_and_context_survives():
+    """The persistent kernel's bounded wait gives up on a barrier nothing arrives at: the
+    status word reports the timeout, the read clears it, and the next decode is still
+    bit-identical to the forward."""
+    B, N, T = 128, 16, 2                                  # 2048 pairs
+    inp = make_inputs(Workload("decto", B, T, N, 64, 64, h0="uniform"), DEV, 10)
+    H = inp["H0"].clone()
+    y = torch.empty((B, N, 64), device=DEV)
+    pkg.m2rnn_decode_step(*step_args(inp, 0), H, y=y, variant=2 | (1 << 8))
+    assert pkg.stream_status() == binding.ERR_TIMEOUT
+    assert pkg.stream_status() == binding.OK
+    y_ref, H_ref = pkg.m2rnn_forward(inp)
+    H = inp["H0"].clone()
+    for t in range(T):
+        y, _ = pkg.m2rnn_decode_step(*step_args(inp, t), H, variant=2)
+        assert torch.equal(y, y_ref[:, t]), t
+    assert pkg.stream_status() == binding.OK
+    assert torch.equal(H, H_ref)

@@ -117,6 +117,28 @@ def test_bf16_shapes(B, T, N, K, V, h0, variant):
     check_full(wl, TOL_BF16, variant=variant, seed=B * 7 + T + K)
 
 
+# Shapes off the tensor-core tile grid: K not a multiple of 16 (rows padded inside the
+# kernel) and V = 48, 80, 96, 112 (readout slots padded to a power of two).
+RAGGED_SHAPES = [(1, 70, 2, 1, 16), (2, 65, 1, 8, 48), (1, 130, 2, 24, 64), (1, 33, 1, 40, 80),
+                 (2, 40, 1, 100, 96), (1, 70, 3, 56, 112), (1, 97, 1, 128, 112),
+                 (1, 64, 1, 17, 16), (2, 33, 2, 1, 128), (1, 66, 2, 7, 32), (1, 129, 2, 127, 48),
+                 (2, 20, 3, 64, 96), (1, 1, 1, 3, 80)]
+
+
+@pytest.mark.parametrize("B,T,N,K,V", RAGGED_SHAPES)
+@pytest.mark.parametrize("h0", ["zero", "uniform"])
+def test_bf16_ragged_shapes(B, T, N, K, V, h0):
+    assert binding.pick_variant(B, T, N, K, V) > 0
+    wl = Workload("bf16r", B, T, N, K, V, h0=h0)
+    check_full(wl, TOL_BF16, seed=B * 5 + T + K)
+
+
+@pytest.mark.parametrize("B,T,N,K,V", [(2, 50, 3, 24, 48), (1, 40, 4, 1, 32)])
+def test_bf16_ragged_shared_qk(B, T, N, K, V):
+    wl = Workload("bf16rs", B, T, N, K, V, h0="uniform", shared_qk=True)
+    check_full(wl, TOL_BF16, seed=11)
+
+
 def test_bf16_small_workload_in_full():
     """B=4, T=2048, N=8, K=V=64, every output against the oracle."""
     ey, eh = check_full(WORKLOADS["b4_t2048_n8_k64_v64"], TOL_BF16)
@@ -203,9 +225,11 @@ def test_bounded_state_with_zero_h0():
     assert float(HT.abs().max()) <= 1.0
 
 
-def test_theorem1_vector_rnn_on_gpu():
-    """f -> 0, w_r = 0, q = k = e_1, H_0 = 0: y_t is the tanh RNN h_t = tanh(W^T h_{t-1} + v_t)."""
-    B, T, N, K, V = 2, 40, 2, 16, 32
+@pytest.mark.parametrize("K,V", [(16, 32), (1, 32), (1, 48)])
+def test_theorem1_vector_rnn_on_gpu(K, V):
+    """f -> 0, w_r = 0, q = k = e_1, H_0 = 0: y_t is the tanh RNN h_t = tanh(W^T h_{t-1} + v_t).
+    K = 1 is the theorem's own case: the matrix state is a single row."""
+    B, T, N = 2, 40, 2
     inp = bf16_inputs(B, T, N, K, V, h0="zero")
     e1 = torch.zeros(K, device=DEV)
     e1[0] = 1
@@ -255,8 +279,9 @@ def test_in_place_state_and_no_final_state():
     assert torch.equal(y3, y_ref)
 
 
-def test_unsupported_and_invalid_from_binding():
-    inp = bf16_inputs(K=24, V=64, T=5)
+@pytest.mark.parametrize("K,V", [(129, 64), (64, 40)])
+def test_unsupported_and_invalid_from_binding(K, V):
+    inp = bf16_inputs(K=K, V=V, T=5)
     with pytest.raises(binding.M2RNNError) as e:
         pkg.m2rnn_forward(inp)
     assert e.value.status == binding.ERR_UNSUPPORTED
