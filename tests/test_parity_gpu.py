@@ -38,8 +38,8 @@ def built():
 
 def run_gpu(inp, variant=0, H_T=True):
     q = inp["q"]
-    B, T, N, K = q.shape
-    V = inp["v"].shape[-1]
+    B, T, _, K = q.shape                     # q may hold one head shared by all
+    N, V = inp["v"].shape[2], inp["v"].shape[3]
     y = torch.full((B, T, N, V), float("nan"), device=q.device)
     if H_T:
         HT = torch.full((B, N, K, V), float("nan"), device=q.device)
