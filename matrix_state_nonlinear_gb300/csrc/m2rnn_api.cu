@@ -51,7 +51,15 @@ EncodeTiledFn encode_fn() {
 
 bool aligned(const void* p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
 
-enum Variant : int { kAuto = 0, kMmaRowWarp = 1, kMmaPipe = 2, kTc5 = 3, kMmaCluster = 4, kNumVariants = 5 };
+enum Variant : int {
+  kAuto = 0,
+  kMmaRowWarp = 1,
+  kMmaPipe = 2,
+  kTc5 = 3,
+  kMmaCluster = 4,
+  kMmaR8 = 5,
+  kNumVariants = 6
+};
 
 m2rnn_status common_checks(const void* q, const void* k, const void* v, const void* a,
                            const float* alpha, const float* beta, const void* W, const float* w_r,
@@ -96,6 +104,7 @@ m2rnn_status backward_checks(const BackwardProblem& p, size_t workspace_bytes) {
 int pick(int K, int V) {
   if (tc5_supports(K, V)) return kTc5;
   if (mma_cluster_supports(K, V)) return kMmaCluster;
+  if (mma_r8_supports(K, V)) return kMmaR8;
   if (mma_pipe_supports(K, V)) return kMmaPipe;
   if (mma_rowwarp_supports(K, V)) return kMmaRowWarp;
   return 0;
@@ -107,6 +116,7 @@ bool supports(int variant, int K, int V) {
     case kMmaPipe: return mma_pipe_supports(K, V);
     case kTc5: return tc5_supports(K, V);
     case kMmaCluster: return mma_cluster_supports(K, V);
+    case kMmaR8: return mma_r8_supports(K, V);
   }
   return false;
 }
@@ -163,6 +173,7 @@ const char* m2rnn_variant_name(int variant) {
     case kMmaPipe: return "mma_sync_pipelined";
     case kTc5: return "tcgen05_k128_v128";
     case kMmaCluster: return "mma_sync_cluster4_k64_v128";
+    case kMmaR8: return "mma_sync_rows8";
   }
   return nullptr;
 }
@@ -235,6 +246,7 @@ m2rnn_status m2rnn_forward_bf16_qk(const uint16_t* q, const uint16_t* k, const u
     case kMmaPipe: err = launch_fwd_bf16_mma_pipe(p, enc, s); break;
     case kTc5: err = launch_fwd_bf16_tc5(p, enc, s); break;
     case kMmaCluster: err = launch_fwd_bf16_mma_cluster(p, enc, s); break;
+    case kMmaR8: err = launch_fwd_bf16_mma_r8(p, enc, s); break;
   }
   return err == cudaSuccess ? M2RNN_OK : M2RNN_ERR_CUDA;
 }

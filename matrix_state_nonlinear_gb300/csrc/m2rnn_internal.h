@@ -110,6 +110,11 @@ cudaError_t launch_fwd_bf16_mma_rowwarp(const Problem& p, EncodeTiledFn enc, cud
 bool mma_pipe_supports(int K, int V);
 cudaError_t launch_fwd_bf16_mma_pipe(const Problem& p, EncodeTiledFn enc, cudaStream_t stream);
 
+// bf16 warp-MMA path with eight state rows per warp, the product taken transposed and the
+// readout on the tensor core, no producer warp: K % 8 == 0, K <= 64, V in {16, 32, 48, 64}.
+bool mma_r8_supports(int K, int V);
+cudaError_t launch_fwd_bf16_mma_r8(const Problem& p, EncodeTiledFn enc, cudaStream_t stream);
+
 // bf16 path on the 5th-generation tensor cores (tcgen05, tensor-memory accumulators),
 // one pair per thread block, two blocks per SM: K = V = 128.
 bool tc5_supports(int K, int V);

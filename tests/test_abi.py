@@ -68,7 +68,10 @@ def test_variant_support_table(lib):
 
 
 def test_pick_variant_host_logic(lib):
-    assert binding.pick_variant(8, 16384, 16, 64, 64) > 0
+    assert binding.pick_variant(8, 16384, 16, 64, 64) == 5   # eight-row warps + helper warps
+    assert binding.pick_variant(8, 16384, 16, 32, 32) == 5
+    assert binding.pick_variant(8, 16384, 16, 48, 64) == 2   # K = 48: the pipelined kernel
+    assert binding.pick_variant(8, 16384, 16, 64, 96) == 1   # V = 96: the row-warp kernel
     assert binding.pick_variant(1, 64, 2, 8, 8) == 0       # V = 8: not a multiple of 16
     assert binding.pick_variant(1, 64, 2, 64, 40) == 0     # V = 40: not a multiple of 16
     assert binding.pick_variant(1, 64, 2, 129, 64) == 0    # K > 128

@@ -102,15 +102,16 @@ def test_backward_without_dHT_and_without_dH0():
 
 
 def test_forward_train_keeps_states_and_matches_plain_forward():
-    # bf16 with V = 128 keeps the states through the row-warp kernel (forward variant 1)
-    for dtype, shape, fwd_variant in [("f32", (2, 37, 3, 8, 24), 0), ("bf16", (2, 150, 3, 64, 64), 0),
-                                      ("bf16", (1, 70, 2, 32, 16), 0),
+    # The bf16 state-keeping forward runs the pipelined kernel's arithmetic (forward variant
+    # 2) for K, V <= 64 with K % 16 == 0 and the row-warp kernel's (variant 1) otherwise.
+    for dtype, shape, fwd_variant in [("f32", (2, 37, 3, 8, 24), 0), ("bf16", (2, 150, 3, 64, 64), 2),
+                                      ("bf16", (1, 70, 2, 32, 16), 2),
                                       ("bf16", (2, 45, 2, 64, 128), 1),
                                       ("bf16", (1, 33, 2, 128, 128), 1),
                                       # ragged K and V off the power-of-two grid (row-warp)
-                                      ("bf16", (2, 40, 2, 24, 48), 0),
-                                      ("bf16", (1, 30, 1, 100, 112), 0),
-                                      ("bf16", (1, 20, 3, 1, 16), 0)]:
+                                      ("bf16", (2, 40, 2, 24, 48), 1),
+                                      ("bf16", (1, 30, 1, 100, 112), 1),
+                                      ("bf16", (1, 20, 3, 1, 16), 1)]:
         B, T, N, K, V = shape
         wl = Workload("tr", B, T, N, K, V, dtype=dtype, h0="uniform", rescale_w=dtype == "bf16")
         inp = make_inputs(wl, DEV, 7)

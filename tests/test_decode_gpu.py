@@ -1,7 +1,9 @@
 """Decode step (T = 1, state in / state out) on the GPU.
 
-The decode kernel performs exactly one step of the pipelined forward kernel, so:
-  * one call equals the forward over a single token, bit for bit;
+The decode kernel performs exactly one step of the warp-MMA forward kernels' arithmetic
+(the pipelined kernel, variant 2, where it applies, else the row-warp kernel, variant 1),
+so:
+  * one call equals that forward over a single token, bit for bit;
   * T calls with the state updated in place equal a T-step forward, bit for bit
     (every y_t and the final state);
 and it matches the fp64 oracle within the bf16 path's 3e-2.  A CUDA graph of
@@ -29,6 +31,12 @@ def built():
     pkg.load_library()
 
 
+def twin(inp, K, V):
+    """The forward pass whose arithmetic the decode kernel reproduces step by step."""
+    variant = 2 if binding.variant_supports(2, 1, 1, 1, K, V) else 1
+    return pkg.m2rnn_forward(inp, variant=variant)
+
+
 def step_args(inp, t):
     return (inp["q"][:, t].contiguous(), inp["k"][:, t].contiguous(), inp["v"][:, t].contiguous(),
             inp["a"][:, t].contiguous(), inp["alpha"], inp["beta"], inp["W"], inp["w_r"])
@@ -46,7 +54,7 @@ def step_args(inp, t):
 def test_decode_steps_reproduce_the_forward_bitwise(shape, shared):
     B, T, N, K, V = shape
     inp = make_inputs(Workload("dec", B, T, N, K, V, h0="uniform", shared_qk=shared), DEV, 5)
-    y_ref, H_ref = pkg.m2rnn_forward(inp)
+    y_ref, H_ref = twin(inp, K, V)
     H = inp["H0"].clone()
     for t in range(T):
         y, _ = pkg.m2rnn_decode_step(*step_args(inp, t), H)   # in place
@@ -74,7 +82,7 @@ def test_decode_large_K_matches_oracle(shape):
 @pytest.mark.parametrize("B, N", [(3, 2), (256, 8)])   # 512 and 2048 pairs
 def test_decode_zero_state_and_separate_output(B, N):
     inp = make_inputs(Workload("dec0", B, 1, N, 64, 64, h0="zero"), DEV, 7)
-    y_ref, H_ref = pkg.m2rnn_forward(inp)
+    y_ref, H_ref = twin(inp, 64, 64)
     H_out = torch.full((B, N, 64, 64), float("nan"), device=DEV)
     y, _ = pkg.m2rnn_decode_step(*step_args(inp, 0), None, H_out=H_out)
     assert pkg.stream_status() == binding.OK
@@ -131,7 +139,7 @@ def test_persistent_decode_forced_timeout_is_reported_and_context_survives():
     pkg.m2rnn_decode_step(*step_args(inp, 0), H, y=y, variant=2 | (1 << 8))
     assert pkg.stream_status() == binding.ERR_TIMEOUT
     assert pkg.stream_status() == binding.OK
-    y_ref, H_ref = pkg.m2rnn_forward(inp)
+    y_ref, H_ref = twin(inp, 64, 64)
     H = inp["H0"].clone()
     for t in range(T):
         y, _ = pkg.m2rnn_decode_step(*step_args(inp, t), H, variant=2)

@@ -100,11 +100,14 @@ def test_f32_shapes(B, T, N, K, V, h0):
 BF16_SHAPES = [(1, 1, 1, 16, 16), (1, 2, 1, 16, 32), (3, 17, 1, 16, 64), (1, 63, 3, 32, 16),
                (2, 64, 1, 64, 64), (1, 65, 3, 64, 64), (1, 130, 2, 48, 32), (2, 97, 1, 128, 64),
                (1, 70, 2, 64, 128), (1, 33, 3, 128, 128), (2, 200, 1, 112, 128),
-               (1, 1, 1, 64, 128), (1, 129, 1, 64, 128), (2, 300, 3, 64, 128)]
+               (1, 1, 1, 64, 128), (1, 129, 1, 64, 128), (2, 300, 3, 64, 128),
+               # K a multiple of 8 (eight-row warps), V = 48
+               (1, 70, 2, 8, 16), (2, 65, 1, 24, 48), (1, 100, 3, 40, 64), (2, 33, 1, 56, 32),
+               (1, 64, 1, 64, 48), (1, 31, 2, 64, 64), (3, 97, 2, 16, 64)]
 
 
 def bf16_variants():
-    return [1, 2, 3, 4]
+    return [1, 2, 3, 4, 5]
 
 
 @pytest.mark.parametrize("B,T,N,K,V", BF16_SHAPES)
@@ -287,7 +290,8 @@ def test_unsupported_and_invalid_from_binding(K, V):
     assert e.value.status == binding.ERR_UNSUPPORTED
 
 
-@pytest.mark.parametrize("variant,K,V", [(1, 64, 64), (2, 64, 64), (3, 128, 128), (4, 64, 128)])
+@pytest.mark.parametrize("variant,K,V", [(1, 64, 64), (2, 64, 64), (3, 128, 128), (4, 64, 128),
+                                         (5, 64, 64)])
 def test_forced_wait_timeout_is_reported_and_context_survives(variant, K, V):
     inp = bf16_inputs(T=70, K=K, V=V)
     y = torch.empty((2, 70, 2, V), device=DEV)
