@@ -58,7 +58,8 @@ enum Variant : int {
   kTc5 = 3,
   kMmaCluster = 4,
   kMmaR8 = 5,
-  kNumVariants = 6
+  kMmaR8Cluster = 6,
+  kNumVariants = 7
 };
 
 m2rnn_status common_checks(const void* q, const void* k, const void* v, const void* a,
@@ -101,9 +102,23 @@ m2rnn_status backward_checks(const BackwardProblem& p, size_t workspace_bytes) {
   return M2RNN_OK;
 }
 
-int pick(int K, int V) {
+// SMs of the current device (152 on GB300, also the answer when no device can be queried).
+int sm_count() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+    return 152;
+  return sms;
+}
+
+// The automatic variant: a function of the shape and of how many (batch, head) pairs there
+// are for the GPU's SMs.  Eight-row warps split over a two-block cluster when the pairs fill
+// at most half the SMs (each block then holds one compute warp per sub-partition), else one
+// block per pair.
+int pick(long long pairs, int K, int V, int sms) {
   if (tc5_supports(K, V)) return kTc5;
   if (mma_cluster_supports(K, V)) return kMmaCluster;
+  if (mma_r8_cluster_supports(K, V) && 2 * pairs <= sms) return kMmaR8Cluster;
   if (mma_r8_supports(K, V)) return kMmaR8;
   if (mma_pipe_supports(K, V)) return kMmaPipe;
   if (mma_rowwarp_supports(K, V)) return kMmaRowWarp;
@@ -117,6 +132,7 @@ bool supports(int variant, int K, int V) {
     case kTc5: return tc5_supports(K, V);
     case kMmaCluster: return mma_cluster_supports(K, V);
     case kMmaR8: return mma_r8_supports(K, V);
+    case kMmaR8Cluster: return mma_r8_cluster_supports(K, V);
   }
   return false;
 }
@@ -174,15 +190,15 @@ const char* m2rnn_variant_name(int variant) {
     case kTc5: return "tcgen05_k128_v128";
     case kMmaCluster: return "mma_sync_cluster4_k64_v128";
     case kMmaR8: return "mma_sync_rows8";
+    case kMmaR8Cluster: return "mma_sync_rows8_cluster2";
   }
   return nullptr;
 }
 
 int m2rnn_pick_variant(int B, int T, int N, int K, int V) {
-  (void)B;
   (void)T;
-  (void)N;
-  return pick(K, V);
+  if (B < 1 || N < 1) return 0;
+  return pick((long long)B * N, K, V, sm_count());
 }
 
 int m2rnn_variant_supports(int variant, int B, int T, int N, int K, int V) {
@@ -225,7 +241,7 @@ m2rnn_status m2rnn_forward_bf16_qk(const uint16_t* q, const uint16_t* k, const u
   const int debug = variant >> 8;
   int base = variant & 0xff;
   if (base < 0 || base >= kNumVariants) return M2RNN_ERR_INVALID_ARG;
-  if (base == kAuto) base = pick(K, V);
+  if (base == kAuto) base = pick((long long)B * N, K, V, sm_count());
   if (base == 0) return M2RNN_ERR_UNSUPPORTED;
   if (!supports(base, K, V)) return M2RNN_ERR_UNSUPPORTED;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(W, 16) ||
@@ -247,6 +263,7 @@ m2rnn_status m2rnn_forward_bf16_qk(const uint16_t* q, const uint16_t* k, const u
     case kTc5: err = launch_fwd_bf16_tc5(p, enc, s); break;
     case kMmaCluster: err = launch_fwd_bf16_mma_cluster(p, enc, s); break;
     case kMmaR8: err = launch_fwd_bf16_mma_r8(p, enc, s); break;
+    case kMmaR8Cluster: err = launch_fwd_bf16_mma_r8_cluster(p, enc, s); break;
   }
   return err == cudaSuccess ? M2RNN_OK : M2RNN_ERR_CUDA;
 }

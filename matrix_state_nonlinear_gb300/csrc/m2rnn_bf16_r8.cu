@@ -1,6 +1,7 @@
 // m2rnn_bf16_r8.cu — bf16-operand / fp32-state forward recurrence with eight state rows per
 // warp and each step's product taken transposed, on the warp-level tensor-core MMA
-// (mma.sync), for K in {32, 64} and V in {16, 32, 48, 64}.
+// (mma.sync), for K in {32, 64} and V in {16, 32, 48, 64}; one thread block per (batch, head)
+// pair, or (K = 64, few pairs) a two-block cluster per pair.
 //
 // The recurrence is the M²RNN study notes' Sec. 2.1 Eq. (10)-(12) with the gate of Sec. 2.2
 // Eq. (13)/(17):
@@ -45,6 +46,19 @@
 //   * the compute warps wait only for chunk c+1's operands before the last trip (two steps)
 //     of chunk c, whose prefetch reads them, and for a free partial buffer at a chunk's
 //     start; both are normally complete long before.
+// Two-block clusters (CS = 2).  When the pairs fill at most half the GPU, a pair's rows are
+// split over the two blocks of a cluster (block r owns rows 32r .. 32r + 31, four compute
+// warps, one per sub-partition), which halves each sub-partition's share of the step chain.
+// Only the readout couples the blocks, and only through the helpers: the compute warps run
+// exactly as in a one-block pair (local partials, local barriers).  Block r owns y columns
+// [rV/2, (r+1)V/2).  Each block's helpers sum their own warps' partials of chunk c and store
+// the sums of each column into the owning block's exchange buffer through distributed shared
+// memory (mapa + st.shared::cluster; `xready`, arrived on at cluster scope); the owner adds
+// the two blocks' sums in block order (deterministic) plus w_r ⊙ v into y and releases the
+// buffers (`xfree`).  Each block loads and converts its own copy of the operands.  Both
+// blocks stay resident until a final cluster barrier that every thread reaches, also after
+// a timeout.
+//
 // With that work off the compute warps, their step machinery fits the 168 registers per
 // thread a 384-thread block allows.  Every wait is bounded; a timeout raises a block-wide
 // abort flag that every other wait also watches.  Every thread arrives on the mbarriers that
@@ -68,16 +82,19 @@ struct R8Layout {
   int qs, ks, vs, stage;  // raw bf16 TMA destinations; three stages `stage` bytes apart
   int cb;                 // operand buffers (two, `cbuf` bytes apart) start here:
   int vd, kf, cbuf;       //   float4 [Tc][8][MT] (v_j, v_j, v_j', v_j'); float [Tc][K]
-  int ypart, ybuf;        // float [2][K / 8][Tc][V] per-warp readout partials, `ybuf` apart
+  int ypart, ybuf;        // float [2][K / 8 / CS][Tc][V] this block's warps' readout partials
+  int xpart, xbuf;        // CS > 1: float [2][CS][Tc][V / CS] per-block sums for this block's
+                          //   columns, `xbuf` apart
   int fgr;                // float2 [2][G Tc] gates of two batches of G chunks
   int wr;                 // float [V]
-  int bar;                // uint64 full[3], pdone[2], ydone[2], cready, never; int abort
+  int bar;                // uint64 full[3], pdone[2], ydone[2], cready, never, xready[2],
+                          //   xfree[2]; int abort
   int total;
 };
 
 __host__ __device__ inline int r8_al128(int x) { return (x + 127) & ~127; }
 
-__host__ __device__ inline R8Layout r8_layout(int K, int V) {
+__host__ __device__ inline R8Layout r8_layout(int K, int V, int CS) {
   constexpr int Tc = kR8Tc;
   R8Layout L;
   const int MT = V / 16;
@@ -90,15 +107,17 @@ __host__ __device__ inline R8Layout r8_layout(int K, int V) {
   L.kf = r8_al128(Tc * 8 * 2 * MT * 8);
   L.cbuf = L.kf + r8_al128(Tc * K * 4);
   L.ypart = L.cb + 2 * L.cbuf;
-  L.ybuf = r8_al128((K / 8) * Tc * V * 4);
-  L.fgr = L.ypart + 2 * L.ybuf;
+  L.ybuf = r8_al128((K / 8 / CS) * Tc * V * 4);
+  L.xpart = L.ypart + 2 * L.ybuf;
+  L.xbuf = CS > 1 ? r8_al128(CS * Tc * (V / CS) * 4) : 0;
+  L.fgr = L.xpart + 2 * L.xbuf;
   L.wr = L.fgr + r8_al128(2 * kR8GateChunks * Tc * 8);
   L.bar = L.wr + r8_al128(V * 4);
-  L.total = L.bar + 128;
+  L.total = L.bar + 160;
   return L;
 }
 
-template <int MT>
+template <int MT, int CS>
 __global__ void __launch_bounds__(384, 1)
     fwd_bf16_r8(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const uint16_t* __restrict__ a,
@@ -107,13 +126,16 @@ __global__ void __launch_bounds__(384, 1)
                 float* __restrict__ y, float* H_T, int T, int N, int K, int qk_hs, int debug,
                 int* status) {
   constexpr int V = 16 * MT;
+  constexpr int VL = V / CS;  // y columns this block owns: rank VL .. rank VL + VL - 1
   constexpr int Tc = kR8Tc;
   constexpr int G = kR8GateChunks, GB = G * Tc;  // chunks and steps per gate batch
   extern __shared__ __align__(128) uint8_t smem[];
-  const R8Layout L = r8_layout(K, V);
-  const int nw = K / 8;  // compute warps; warps nw .. nw + 3 are the helpers
+  const R8Layout L = r8_layout(K, V, CS);
+  const int wt = K / 8;       // compute warps of the pair
+  const int nw = wt / CS;     // compute warps of this block; warps nw .. nw + 3 are the helpers
+  const int rank = CS > 1 ? (int)cluster_ctarank() : 0;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nthreads = blockDim.x;
-  const int pair = blockIdx.x, b = pair / N, n = pair - (pair / N) * N;
+  const int pair = blockIdx.x / CS, b = pair / N, n = pair - (pair / N) * N;
   const int nchunks = (T + Tc - 1) / Tc;
   const size_t row_base = (size_t)b * T;  // (b, t) row index base
   const int tma_tid = 32 * nw;            // helper thread 0 issues every TMA load
@@ -123,7 +145,10 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t* ydone = full + 5;   // [2]: chunk c's y summed, on ydone[c & 1]
   uint64_t* cready = full + 7;  // chunk c's operands converted (c >= 2)
   uint64_t* never = full + 8;   // never armed: the forced-timeout test hook waits on it
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(full + 9);
+  uint64_t* xready = full + 9;  // [2]: both blocks' sums of chunk c stored here (CS > 1)
+  uint64_t* xfree = full + 11;  // [2]: both owners have read this block's sums of chunk c
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(full + 13);
+  float* xpart = reinterpret_cast<float*>(smem + L.xpart);
   float2* fgr = reinterpret_cast<float2*>(smem + L.fgr);
   float* ypart = reinterpret_cast<float*>(smem + L.ypart);
   float* wrs = reinterpret_cast<float*>(smem + L.wr);
@@ -133,17 +158,22 @@ __global__ void __launch_bounds__(384, 1)
 
   if (tid == 0) {
     for (int i = 0; i < 3; ++i) mbar_init(&full[i], 1);
-    mbar_init(&pdone[0], 32 * nw);
+    mbar_init(&pdone[0], 32 * nw);  // every compute lane of the block
     mbar_init(&pdone[1], 32 * nw);
-    mbar_init(&ydone[0], 32 * kR8Helpers);
+    mbar_init(&ydone[0], 32 * kR8Helpers);  // every helper lane of the block
     mbar_init(&ydone[1], 32 * kR8Helpers);
     mbar_init(cready, 32 * kR8Helpers);
     mbar_init(never, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&xready[i], 32 * kR8Helpers * CS);  // every helper lane of the pair
+      mbar_init(&xfree[i], 32 * kR8Helpers * CS);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
   for (int j = tid; j < V; j += nthreads) wrs[j] = w_r[(size_t)n * V + j];
   __syncthreads();
+  if constexpr (CS > 1) cluster_sync_all();  // every block's barriers exist before remote arrives
 
   int issued = 0;  // chunks whose TMA load this thread has started (the TMA thread only)
   auto issue = [&](int cc) {
@@ -161,13 +191,32 @@ __global__ void __launch_bounds__(384, 1)
     for (int ci = issued > 3 ? issued - 3 : 0; ci < issued; ++ci)
       mbar_wait_bounded(&full[ci % 3], (uint32_t)(ci / 3) & 1u, kDebugWaitLimitCycles);
   };
-  // Bounded wait that also gives up once another warp has given up; on failure this thread
-  // raises the block's abort flag and records the timeout.
-  auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
-    if (wait_or_abort(bar, parity, limit, abort_flag)) return true;
+  // Bounded wait that also gives up once another warp of the block has given up; on failure
+  // this thread raises the block's abort flag and records the timeout.  `remote`: arrivals
+  // may come from the other block of the cluster (acquire at cluster scope).
+  // `sleep`: a warp that waits long (a helper waiting for the compute warps) sleeps on the
+  // barrier instead of polling it, so it takes no issue slots from its sub-partition.
+  auto wait = [&](uint64_t* bar, uint32_t parity, bool remote = false,
+                  bool sleep = false) -> bool {
+    const bool ok =
+        (CS > 1 && remote)
+            ? (sleep ? mbar_wait_cluster_sleep(bar, parity, limit, abort_flag)
+                     : mbar_wait_cluster(bar, parity, limit, abort_flag))
+            : (sleep ? wait_or_abort_sleep(bar, parity, limit, abort_flag)
+                     : wait_or_abort(bar, parity, limit, abort_flag));
+    if (ok) return true;
     *abort_flag = 1;
     if (lane == 0) atomicExch(status, kStatusTimeout);
     return false;
+  };
+  // Arrive on a barrier of every block of the pair (release at cluster scope when CS > 1).
+  auto arrive_all = [&](uint64_t* bar) {
+    if constexpr (CS == 1) {
+      mbar_arrive(bar);
+    } else {
+#pragma unroll
+      for (int r = 0; r < CS; ++r) mbar_arrive_cluster(mapa_shared(smem_u32(bar), (uint32_t)r));
+    }
   };
 
   // ---------------------------------------------------------------- staging helpers
@@ -204,9 +253,9 @@ __global__ void __launch_bounds__(384, 1)
       kf[2 * e + 1] = make_float4(bf16_lo(u.z), bf16_hi(u.z), bf16_lo(u.w), bf16_hi(u.w));
     }
   };
-  // y of chunk cc: w_r ⊙ v plus the compute warps' partials in warp order, float4 rows;
-  // outputs i0, i0 + count, ...  The loop over warps is unrolled so that an output's partial
-  // loads are in flight together.
+  // y of chunk cc (CS == 1): w_r ⊙ v plus the compute warps' partials in warp order, float4
+  // rows; outputs i0, i0 + count, ...  The loop over warps is unrolled so that an output's
+  // partial loads are in flight together.
   auto ysum = [&](int cc, int i0, int count) {
     const int steps = min(Tc, T - cc * Tc);
     const uint16_t* vs = reinterpret_cast<const uint16_t*>(smem + (cc % 3) * L.stage + L.vs);
@@ -233,37 +282,106 @@ __global__ void __launch_bounds__(384, 1)
       *reinterpret_cast<float4*>(y + ((row_base + (size_t)cc * Tc + s) * N + n) * V + j) = o;
     }
   };
+  // CS > 1, first half: this block's warps' partials of chunk cc summed in warp order, each
+  // float4 of columns stored into its owner's exchange buffer (slot `rank`).
+  auto xsum = [&](int cc, int i0, int count) {
+    const int steps = min(Tc, T - cc * Tc);
+    const float* yp = ypart + (size_t)(cc & 1) * (L.ybuf / 4);
+    constexpr int V4 = V / 4;
+    for (int idx = i0; idx < steps * V4; idx += count) {
+      const int s = idx / V4, j = (idx - s * V4) * 4;
+      float4 u[8];
+#pragma unroll
+      for (int w = 0; w < 8; ++w)
+        if (w < nw) u[w] = *reinterpret_cast<const float4*>(yp + ((size_t)w * Tc + s) * V + j);
+      float4 o = u[0];
+#pragma unroll
+      for (int w = 1; w < 8; ++w)
+        if (w < nw) {
+          o.x += u[w].x;
+          o.y += u[w].y;
+          o.z += u[w].z;
+          o.w += u[w].w;
+        }
+      const int owner = j / VL;
+      const uint32_t a = smem_u32(xpart + (size_t)(cc & 1) * (L.xbuf / 4) +
+                                  ((size_t)rank * Tc + s) * VL + (j - owner * VL));
+      st_cluster_v4_f32(mapa_shared(a, (uint32_t)owner), o);
+    }
+  };
+  // CS > 1, second half: y of chunk cc for this block's columns: w_r ⊙ v plus the blocks' sums
+  // in block order.
+  auto ysum_x = [&](int cc, int i0, int count) {
+    const int steps = min(Tc, T - cc * Tc);
+    const uint16_t* vs = reinterpret_cast<const uint16_t*>(smem + (cc % 3) * L.stage + L.vs);
+    const float* xp = xpart + (size_t)(cc & 1) * (L.xbuf / 4);
+    constexpr int V4 = VL / 4;
+    for (int idx = i0; idx < steps * V4; idx += count) {
+      const int s = idx / V4, jl = (idx - s * V4) * 4, j = rank * VL + jl;
+      float4 u[CS];
+#pragma unroll
+      for (int r = 0; r < CS; ++r)
+        u[r] = *reinterpret_cast<const float4*>(xp + ((size_t)r * Tc + s) * VL + jl);
+      const uint2 vv = *reinterpret_cast<const uint2*>(vs + s * V + j);
+      const float4 w4 = *reinterpret_cast<const float4*>(wrs + j);
+      float4 o = make_float4(w4.x * bf16_lo(vv.x), w4.y * bf16_hi(vv.x), w4.z * bf16_lo(vv.y),
+                             w4.w * bf16_hi(vv.y));
+#pragma unroll
+      for (int r = 0; r < CS; ++r) {
+        o.x += u[r].x;
+        o.y += u[r].y;
+        o.z += u[r].z;
+        o.w += u[r].w;
+      }
+      *reinterpret_cast<float4*>(y + ((row_base + (size_t)cc * Tc + s) * N + n) * V + j) = o;
+    }
+  };
 
   // ---------------------------------------------------------------- prologue (all threads)
   // Chunks 0, 1, 2 start loading; chunks 0 and 1 are converted and gate batch 0 computed by
   // every thread before the roles split.
   if (tid == tma_tid)
     for (int cc = 0; cc < 3 && cc < nchunks; ++cc) issue(cc);
+  bool started;
   {
     const float a0 = load_a(0, tid);
     bool ok = mbar_wait_bounded(&full[0], 0u, limit);
     if (debug & kDebugForceTimeout) ok = ok && mbar_wait_bounded(never, 0u, kDebugWaitLimitCycles);
     if (nchunks > 1) ok = ok && mbar_wait_bounded(&full[1], 0u, limit);
-    if (__syncthreads_or(!ok)) {
+    started = !__syncthreads_or(!ok);
+    if (!started) {
       if (tid == 0) atomicExch(status, kStatusTimeout);
       if (tid == tma_tid) drain();
-      return;
+      if constexpr (CS == 1) return;  // (a cluster's blocks leave together, below)
+    } else {
+      convert(0, tid, nthreads);
+      if (nchunks > 1) convert(1, tid, nthreads);
+      gate(0, tid, a0);
     }
-    convert(0, tid, nthreads);
-    if (nchunks > 1) convert(1, tid, nthreads);
-    gate(0, tid, a0);
   }
   __syncthreads();
 
   // ================================================================ helper warps
-  if (warp >= nw) {
+  if (started && warp >= nw) {
     const int hid = tid - tma_tid;  // 0 .. 127
     float a_nx = load_a(1, hid);    // logits of gate batch 1
     for (int cc = 0; cc < nchunks; ++cc) {
-      bool ok = wait(&pdone[cc & 1], (uint32_t)(cc >> 1) & 1u);
+      bool ok = wait(&pdone[cc & 1], (uint32_t)(cc >> 1) & 1u, false, true);
+      if constexpr (CS > 1)  // both owners have read what this block stored for chunk cc-2
+        if (ok && cc >= 2) ok = wait(&xfree[cc & 1], (uint32_t)((cc - 2) >> 1) & 1u, true, true);
       if (named_bar_or(1, 32 * kR8Helpers, !ok)) break;
-      ysum(cc, hid, 32 * kR8Helpers);
-      mbar_arrive(&ydone[cc & 1]);
+      if constexpr (CS == 1) {
+        ysum(cc, hid, 32 * kR8Helpers);
+        mbar_arrive(&ydone[cc & 1]);
+      } else {
+        xsum(cc, hid, 32 * kR8Helpers);
+        mbar_arrive(&ydone[cc & 1]);
+        arrive_all(&xready[cc & 1]);
+        ok = wait(&xready[cc & 1], (uint32_t)(cc >> 1) & 1u, true, true);
+        if (named_bar_or(4, 32 * kR8Helpers, !ok)) break;
+        ysum_x(cc, hid, 32 * kR8Helpers);
+        arrive_all(&xfree[cc & 1]);
+      }
       if (cc + 3 < nchunks) {
         // Stage cc % 3 is free: every helper has read chunk cc's v, the compute warps its q.
         named_bar_sync(2, 32 * kR8Helpers);
@@ -271,7 +389,7 @@ __global__ void __launch_bounds__(384, 1)
       }
       if (cc + 2 < nchunks) {
         const int nc = cc + 2;  // into operand buffer cc & 1, which chunk cc has released
-        ok = wait(&full[nc % 3], (uint32_t)(nc / 3) & 1u);
+        ok = wait(&full[nc % 3], (uint32_t)(nc / 3) & 1u, false, true);
         if (named_bar_or(3, 32 * kR8Helpers, !ok)) break;
         convert(nc, hid, 32 * kR8Helpers);
         if (nc % G == 0) {  // the gate batch that starts with chunk nc
@@ -282,10 +400,11 @@ __global__ void __launch_bounds__(384, 1)
       }
     }
     if (hid == 0) drain();  // nothing is in flight unless the loop was left on a timeout
-    return;
+    if constexpr (CS == 1) return;
   }
 
   // ================================================================ compute warps
+  if (started && warp < nw) {
   const int g = lane >> 2, c = lane & 3;
 
   // W^T as m16n8k16 A fragments: wa[m][kt] covers rows j = 16m + g (+8) of W^T and columns
@@ -304,7 +423,8 @@ __global__ void __launch_bounds__(384, 1)
     }
 
   // State (fp32) in the accumulator layout: h[m][hh] = (H[i0][j], H[i0 + 1][j]), j = 16m + 8hh + g.
-  const int i0 = 8 * warp + 2 * c;
+  const int wg = nw * rank + warp;  // this warp's index among the pair's compute warps
+  const int i0 = 8 * wg + 2 * c;
   float2 h[MT][2];
   if (H0) {
     const float* hp = H0 + (size_t)pair * K * V;
@@ -411,6 +531,9 @@ __global__ void __launch_bounds__(384, 1)
       for (int m2 = 0; m2 < MT; ++m2) mma2(nx[m2], wa[m2][m], b0, b1);
     }
   };
+  auto store_part = [&](float* yp, int s, int j, float val) {
+    yp[((size_t)warp * Tc + s) * V + j] = val;
+  };
   // Eq. (12) readout of steps s and s + 1 over this warp's rows, one m16n8k16 MMA per column
   // tile (see the header), into partial buffer yp; `two` is false for a lone last step.
   auto readout2 = [&](float* yp, const uint32_t (&apA)[MT][2], const uint32_t (&apB)[MT][2],
@@ -428,12 +551,11 @@ __global__ void __launch_bounds__(384, 1)
       hi = add2(hi, make_float2(d[m][2], d[m][3]));
     }
     if (c < MT) {
-      float* yrow = yp + ((size_t)warp * Tc + s) * V;
-      yrow[16 * c + g] = lo.x;
-      yrow[16 * c + 8 + g] = hi.x;
+      store_part(yp, s, 16 * c + g, lo.x);
+      store_part(yp, s, 16 * c + 8 + g, hi.x);
       if (two) {
-        yrow[V + 16 * c + g] = lo.y;
-        yrow[V + 16 * c + 8 + g] = hi.y;
+        store_part(yp, s + 1, 16 * c + g, lo.y);
+        store_part(yp, s + 1, 16 * c + 8 + g, hi.y);
       }
     }
   };
@@ -443,7 +565,7 @@ __global__ void __launch_bounds__(384, 1)
     const int steps = min(Tc, T - cc * Tc);
     const ChunkPtrs P = chunk_ptrs(cc);
     float* yp = ypart + (size_t)(cc & 1) * (L.ybuf / 4);
-    // The partial buffer was last read by the y sum of chunk cc-2.
+    // The partial buffer was last read by the helpers' sums of chunk cc-2.
     if (cc >= 2 && !wait(&ydone[cc & 1], (uint32_t)((cc - 2) >> 1) & 1u)) {
       ok = false;
       break;
@@ -480,9 +602,10 @@ __global__ void __launch_bounds__(384, 1)
     }
     mbar_arrive(&pdone[cc & 1]);
   }
-  if (!ok) return;
+  if constexpr (CS == 1)
+    if (!ok) return;
 
-  if (H_T) {
+  if (ok && H_T) {
     float* hp = H_T + (size_t)pair * K * V;
 #pragma unroll
     for (int m = 0; m < MT; ++m)
@@ -493,6 +616,10 @@ __global__ void __launch_bounds__(384, 1)
         hp[(size_t)(i0 + 1) * V + j] = h[m][hh].y;
       }
   }
+  }
+  // Neither block of a cluster leaves while the other may still store to its shared memory
+  // or arrive on its barriers.
+  if constexpr (CS > 1) cluster_sync_all();
 }
 
 bool make_map_r8(EncodeTiledFn enc, CUtensorMap* map, const void* base, int inner, int N, int T,
@@ -507,24 +634,45 @@ bool make_map_r8(EncodeTiledFn enc, CUtensorMap* map, const void* base, int inne
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int MT>
+template <int MT, int CS>
 cudaError_t launch_r8(const Problem& p, EncodeTiledFn enc, cudaStream_t stream) {
   constexpr int V = 16 * MT;
-  auto kern = fwd_bf16_r8<MT>;
-  const R8Layout L = r8_layout(p.K, V);
+  const R8Layout L = r8_layout(p.K, V, CS);
   CUtensorMap mq, mk, mv;
   if (!make_map_r8(enc, &mq, p.q, p.K, p.Nqk, p.T, p.B, kR8Tc) ||
       !make_map_r8(enc, &mk, p.k, p.K, p.Nqk, p.T, p.B, kR8Tc) ||
       !make_map_r8(enc, &mv, p.v, V, p.N, p.T, p.B, kR8Tc))
     return cudaErrorInvalidValue;
+  auto kern = fwd_bf16_r8<MT, CS>;
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
   if (err != cudaSuccess) return err;
-  const unsigned grid = (unsigned)p.B * (unsigned)p.N;
-  kern<<<grid, 32 * (p.K / 8 + kR8Helpers), L.total, stream>>>(
-      mq, mk, mv, (const uint16_t*)p.a, p.alpha, p.beta, (const uint16_t*)p.W, p.w_r, p.H0, p.y,
-      p.H_T, p.T, p.N, p.K, p.Nqk == 1 ? 0 : 1, p.debug, p.status);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)CS * (unsigned)p.B * (unsigned)p.N, 1, 1);
+  cfg.blockDim = dim3(32u * (unsigned)(p.K / 8 / CS + kR8Helpers), 1, 1);
+  cfg.dynamicSmemBytes = (size_t)L.total;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CS;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = CS > 1 ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, (const uint16_t*)p.a, p.alpha, p.beta,
+                            (const uint16_t*)p.W, p.w_r, p.H0, p.y, p.H_T, p.T, p.N, p.K,
+                            p.Nqk == 1 ? 0 : 1, p.debug, p.status);
+}
+
+template <int CS>
+cudaError_t launch_r8_cs(const Problem& p, EncodeTiledFn enc, cudaStream_t stream) {
+  switch (p.V) {
+    case 16: return launch_r8<1, CS>(p, enc, stream);
+    case 32: return launch_r8<2, CS>(p, enc, stream);
+    case 48: return launch_r8<3, CS>(p, enc, stream);
+    case 64: return launch_r8<4, CS>(p, enc, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace
@@ -533,14 +681,15 @@ bool mma_r8_supports(int K, int V) {
   return (K == 32 || K == 64) && (V == 16 || V == 32 || V == 48 || V == 64);
 }
 
+bool mma_r8_cluster_supports(int K, int V) { return K == 64 && mma_r8_supports(K, V); }
+
 cudaError_t launch_fwd_bf16_mma_r8(const Problem& p, EncodeTiledFn enc, cudaStream_t stream) {
-  switch (p.V) {
-    case 16: return launch_r8<1>(p, enc, stream);
-    case 32: return launch_r8<2>(p, enc, stream);
-    case 48: return launch_r8<3>(p, enc, stream);
-    case 64: return launch_r8<4>(p, enc, stream);
-    default: return cudaErrorInvalidValue;
-  }
+  return launch_r8_cs<1>(p, enc, stream);
+}
+
+cudaError_t launch_fwd_bf16_mma_r8_cluster(const Problem& p, EncodeTiledFn enc,
+                                           cudaStream_t stream) {
+  return launch_r8_cs<2>(p, enc, stream);
 }
 
 }  // namespace m2rnn

@@ -114,6 +114,12 @@ cudaError_t launch_fwd_bf16_mma_pipe(const Problem& p, EncodeTiledFn enc, cudaSt
 // readout on the tensor core, no producer warp: K % 8 == 0, K <= 64, V in {16, 32, 48, 64}.
 bool mma_r8_supports(int K, int V);
 cudaError_t launch_fwd_bf16_mma_r8(const Problem& p, EncodeTiledFn enc, cudaStream_t stream);
+// The same kernel with a pair's rows split over a two-block cluster (readout partials through
+// distributed shared memory): K = 64, V in {16, 32, 48, 64}.  For pair counts that fill at
+// most half the GPU.
+bool mma_r8_cluster_supports(int K, int V);
+cudaError_t launch_fwd_bf16_mma_r8_cluster(const Problem& p, EncodeTiledFn enc,
+                                           cudaStream_t stream);
 
 // bf16 path on the 5th-generation tensor cores (tcgen05, tensor-memory accumulators),
 // one pair per thread block, two blocks per SM: K = V = 128.

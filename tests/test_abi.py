@@ -69,6 +69,11 @@ def test_variant_support_table(lib):
 
 def test_pick_variant_host_logic(lib):
     assert binding.pick_variant(8, 16384, 16, 64, 64) == 5   # eight-row warps + helper warps
+    assert binding.pick_variant(4, 2048, 8, 64, 64) == 6     # 32 pairs: two-block clusters
+    assert binding.pick_variant(4, 2048, 19, 64, 64) == 6    # 76 pairs fill half of 152 SMs
+    assert binding.pick_variant(4, 2048, 20, 64, 64) == 5    # 80 pairs: one block per pair
+    assert binding.variant_supports(6, 1, 8, 1, 64, 48)
+    assert not binding.variant_supports(6, 1, 8, 1, 32, 64)  # K = 32: one warp per SP already
     assert binding.pick_variant(8, 16384, 16, 32, 32) == 5
     assert binding.pick_variant(8, 16384, 16, 48, 64) == 2   # K = 48: the pipelined kernel
     assert binding.pick_variant(8, 16384, 16, 64, 96) == 1   # V = 96: the row-warp kernel

@@ -107,7 +107,7 @@ BF16_SHAPES = [(1, 1, 1, 16, 16), (1, 2, 1, 16, 32), (3, 17, 1, 16, 64), (1, 63,
 
 
 def bf16_variants():
-    return [1, 2, 3, 4, 5]
+    return [1, 2, 3, 4, 5, 6]
 
 
 @pytest.mark.parametrize("B,T,N,K,V", BF16_SHAPES)
@@ -291,7 +291,7 @@ def test_unsupported_and_invalid_from_binding(K, V):
 
 
 @pytest.mark.parametrize("variant,K,V", [(1, 64, 64), (2, 64, 64), (3, 128, 128), (4, 64, 128),
-                                         (5, 64, 64)])
+                                         (5, 64, 64), (6, 64, 64)])
 def test_forced_wait_timeout_is_reported_and_context_survives(variant, K, V):
     inp = bf16_inputs(T=70, K=K, V=V)
     y = torch.empty((2, 70, 2, V), device=DEV)
