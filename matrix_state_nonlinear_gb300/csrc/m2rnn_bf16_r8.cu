@@ -194,15 +194,17 @@ __global__ void __launch_bounds__(384, 1)
   // Bounded wait that also gives up once another warp of the block has given up; on failure
   // this thread raises the block's abort flag and records the timeout.  `remote`: arrivals
   // may come from the other block of the cluster (acquire at cluster scope).
-  // `sleep`: a warp that waits long (a helper waiting for the compute warps) sleeps on the
-  // barrier instead of polling it, so it takes no issue slots from its sub-partition.
+  // `sleep` (two-block clusters only): a warp that waits long (a helper waiting for the
+  // compute warps) sleeps on the barrier instead of polling it, so it takes no issue slots
+  // from its sub-partition.  One-block pairs keep polling helpers: the hot loop's schedule
+  // depends on the code around it, and theirs is the one measured fastest.
   auto wait = [&](uint64_t* bar, uint32_t parity, bool remote = false,
                   bool sleep = false) -> bool {
     const bool ok =
         (CS > 1 && remote)
             ? (sleep ? mbar_wait_cluster_sleep(bar, parity, limit, abort_flag)
                      : mbar_wait_cluster(bar, parity, limit, abort_flag))
-            : (sleep ? wait_or_abort_sleep(bar, parity, limit, abort_flag)
+            : ((sleep && CS > 1) ? wait_or_abort_sleep(bar, parity, limit, abort_flag)
                      : wait_or_abort(bar, parity, limit, abort_flag));
     if (ok) return true;
     *abort_flag = 1;
@@ -362,7 +364,7 @@ __global__ void __launch_bounds__(384, 1)
   __syncthreads();
 
   // ================================================================ helper warps
-  if (started && warp >= nw) {
+  if ((CS == 1 || started) && warp >= nw) {
     const int hid = tid - tma_tid;  // 0 .. 127
     float a_nx = load_a(1, hid);    // logits of gate batch 1
     for (int cc = 0; cc < nchunks; ++cc) {
@@ -404,7 +406,7 @@ __global__ void __launch_bounds__(384, 1)
   }
 
   // ================================================================ compute warps
-  if (started && warp < nw) {
+  if ((CS == 1 || started) && warp < nw) {
   const int g = lane >> 2, c = lane & 3;
 
   // W^T as m16n8k16 A fragments: wa[m][kt] covers rows j = 16m + g (+8) of W^T and columns
