@@ -28,8 +28,8 @@
  * The library allocates no device memory per call, keeps no per-call state, and
  * only enqueues work on `stream` (a cudaStream_t passed as void*; NULL is the
  * legacy default stream); it returns before the GPU finishes.  Calls from
- * several host threads are safe.  H0 == H_T (in place) is allowed: the state is
- * read once at the start and written once at the end by the same thread block.
+ * several host threads are safe.  H0 == H_T (in place) is allowed: each pair's
+ * initial state is read before anything of that pair's final state is written.
  * No other output may alias an input.
  *
  * Errors.  Arguments are validated on the host before anything is enqueued;
@@ -306,6 +306,22 @@ int m2rnn_pick_variant(int B, int T, int N, int K, int V);
 
 /* 1 if bf16 kernel variant `variant` (> 0) can run this shape, else 0. */
 int m2rnn_variant_supports(int variant, int B, int T, int N, int K, int V);
+
+/*
+ * The balanced schedule of the K = V = 128 tensor-core forward (variant
+ * "tcgen05_k128_v128_balanced", chosen automatically when there are more
+ * (batch, head) pairs than resident thread blocks).  Lay the B*N pairs' steps
+ * end to end (pair p = b*N + n owns positions [p*T, (p+1)*T)); stretch `worker`
+ * of `workers` (one thread block each) covers positions [*begin, *end).  A pair
+ * cut by a boundary runs its
+ * first steps at the start of the later block's stretch and its last steps at
+ * the end of the earlier block's stretch (at least 129 of them: the handed-over
+ * state travels through that pair's own y rows before they are written).
+ * Host-only arithmetic, exposed so the schedule can be checked without a GPU.
+ * Returns 0, or -1 for pairs, T or workers < 1, or worker outside [0, workers).
+ */
+int m2rnn_balanced_stretch(long long pairs, int T, long long workers, long long worker,
+                           long long* begin, long long* end);
 
 /*
  * Synchronises `stream`, then returns and clears the current device's status

@@ -59,7 +59,8 @@ enum Variant : int {
   kMmaCluster = 4,
   kMmaR8 = 5,
   kMmaR8Cluster = 6,
-  kNumVariants = 7
+  kTc5Balanced = 7,
+  kNumVariants = 8
 };
 
 m2rnn_status common_checks(const void* q, const void* k, const void* v, const void* a,
@@ -116,7 +117,7 @@ int sm_count() {
 // at most half the SMs (each block then holds one compute warp per sub-partition), else one
 // block per pair.
 int pick(long long pairs, int K, int V, int sms) {
-  if (tc5_supports(K, V)) return kTc5;
+  if (tc5_supports(K, V)) return pairs > 2LL * sms ? kTc5Balanced : kTc5;
   if (mma_cluster_supports(K, V)) return kMmaCluster;
   if (mma_r8_cluster_supports(K, V) && 2 * pairs <= sms) return kMmaR8Cluster;
   if (mma_r8_supports(K, V)) return kMmaR8;
@@ -129,7 +130,8 @@ bool supports(int variant, int K, int V) {
   switch (variant) {
     case kMmaRowWarp: return mma_rowwarp_supports(K, V);
     case kMmaPipe: return mma_pipe_supports(K, V);
-    case kTc5: return tc5_supports(K, V);
+    case kTc5:
+    case kTc5Balanced: return tc5_supports(K, V);
     case kMmaCluster: return mma_cluster_supports(K, V);
     case kMmaR8: return mma_r8_supports(K, V);
     case kMmaR8Cluster: return mma_r8_cluster_supports(K, V);
@@ -188,6 +190,7 @@ const char* m2rnn_variant_name(int variant) {
     case kMmaRowWarp: return "mma_sync_rowwarp";
     case kMmaPipe: return "mma_sync_pipelined";
     case kTc5: return "tcgen05_k128_v128";
+    case kTc5Balanced: return "tcgen05_k128_v128_balanced";
     case kMmaCluster: return "mma_sync_cluster4_k64_v128";
     case kMmaR8: return "mma_sync_rows8";
     case kMmaR8Cluster: return "mma_sync_rows8_cluster2";
@@ -199,6 +202,17 @@ int m2rnn_pick_variant(int B, int T, int N, int K, int V) {
   (void)T;
   if (B < 1 || N < 1) return 0;
   return pick((long long)B * N, K, V, sm_count());
+}
+
+int m2rnn_balanced_stretch(long long pairs, int T, long long workers, long long worker,
+                           long long* begin, long long* end) {
+  if (pairs < 1 || T < 1 || workers < 1 || worker < 0 || worker >= workers || !begin || !end)
+    return -1;
+  const long long total = pairs * (long long)T;
+  const long long line = tc5_line_per_block(pairs, T, workers);
+  *begin = tc5_cut(worker * line, total, T);
+  *end = tc5_cut((worker + 1) * line, total, T);
+  return 0;
 }
 
 int m2rnn_variant_supports(int variant, int B, int T, int N, int K, int V) {
@@ -260,7 +274,8 @@ m2rnn_status m2rnn_forward_bf16_qk(const uint16_t* q, const uint16_t* k, const u
   switch (base) {
     case kMmaRowWarp: err = launch_fwd_bf16_mma_rowwarp(p, enc, s); break;
     case kMmaPipe: err = launch_fwd_bf16_mma_pipe(p, enc, s); break;
-    case kTc5: err = launch_fwd_bf16_tc5(p, enc, s); break;
+    case kTc5: err = launch_fwd_bf16_tc5(p, enc, s, false); break;
+    case kTc5Balanced: err = launch_fwd_bf16_tc5(p, enc, s, true); break;
     case kMmaCluster: err = launch_fwd_bf16_mma_cluster(p, enc, s); break;
     case kMmaR8: err = launch_fwd_bf16_mma_r8(p, enc, s); break;
     case kMmaR8Cluster: err = launch_fwd_bf16_mma_r8_cluster(p, enc, s); break;

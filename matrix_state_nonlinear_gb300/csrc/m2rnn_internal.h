@@ -122,9 +122,33 @@ cudaError_t launch_fwd_bf16_mma_r8_cluster(const Problem& p, EncodeTiledFn enc,
                                            cudaStream_t stream);
 
 // bf16 path on the 5th-generation tensor cores (tcgen05, tensor-memory accumulators),
-// one pair per thread block, two blocks per SM: K = V = 128.
+// two blocks per SM: K = V = 128.  Unbalanced: one block per pair.  Balanced (more pairs
+// than resident blocks): every block resident at once, each taking an equal stretch of the
+// line of all pairs' steps laid end to end (pair p owns [p T, (p+1) T)); a pair cut by a
+// stretch boundary runs its first steps at the start of the later block's stretch and its
+// last steps at the end of the earlier block's stretch, the state handed over in between.
 bool tc5_supports(int K, int V);
-cudaError_t launch_fwd_bf16_tc5(const Problem& p, EncodeTiledFn enc, cudaStream_t stream);
+cudaError_t launch_fwd_bf16_tc5(const Problem& p, EncodeTiledFn enc, cudaStream_t stream,
+                                bool balanced);
+
+// Rows of y a handed-off state occupies (K = 128 state rows and one ready word): the
+// block that takes a pair over must run at least this many of its steps.
+constexpr int kTc5HandoffRows = 129;
+// Blocks of the balanced schedule: one per resident slot, at most one per pair.
+__host__ __device__ inline long long tc5_balanced_workers(long long pairs, long long slots) {
+  return pairs < slots ? pairs : slots;
+}
+// Steps of the line per block (rounded up).
+__host__ __device__ inline long long tc5_line_per_block(long long pairs, int T, long long workers) {
+  return (pairs * (long long)T + workers - 1) / workers;
+}
+// Stretch boundary near line position c: a cut that would leave the earlier block fewer
+// than kTc5HandoffRows last steps of a pair moves down to the pair's start instead.
+__host__ __device__ inline long long tc5_cut(long long c, long long total, int T) {
+  if (c >= total) return total;
+  const long long r = c % T;
+  return (r != 0 && r < kTc5HandoffRows) ? c - r : c;
+}
 
 // bf16 warp-MMA path with a 4-CTA thread-block cluster per pair (rows split over four
 // SMs, readout partials exchanged through distributed shared memory): K = 64, V = 128.

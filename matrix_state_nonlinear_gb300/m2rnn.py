@@ -29,6 +29,9 @@ SYMBOLS = {
     "m2rnn_variant_name": (ctypes.c_char_p, [_I]),
     "m2rnn_pick_variant": (_I, [_I] * 5),
     "m2rnn_variant_supports": (_I, [_I] * 6),
+    "m2rnn_balanced_stretch": (_I, [ctypes.c_longlong, _I, ctypes.c_longlong, ctypes.c_longlong,
+                                    ctypes.POINTER(ctypes.c_longlong),
+                                    ctypes.POINTER(ctypes.c_longlong)]),
     "m2rnn_stream_status": (_I, [_P]),
     "m2rnn_status_string": (ctypes.c_char_p, [_I]),
     "m2rnn_version": (_I, []),
@@ -89,6 +92,17 @@ def pick_variant(B: int, T: int, N: int, K: int, V: int) -> int:
 
 def variant_supports(variant: int, B: int, T: int, N: int, K: int, V: int) -> bool:
     return bool(load_library().m2rnn_variant_supports(variant, B, T, N, K, V))
+
+
+def balanced_stretch(pairs: int, T: int, workers: int, worker: int) -> tuple[int, int]:
+    """Positions [begin, end) of the steps line that block `worker` of the balanced K = V = 128
+    forward runs (pair p owns [p T, (p + 1) T))."""
+    b, e = ctypes.c_longlong(), ctypes.c_longlong()
+    st = load_library().m2rnn_balanced_stretch(pairs, T, workers, worker, ctypes.byref(b),
+                                               ctypes.byref(e))
+    if st != 0:
+        raise ValueError(f"invalid balanced schedule arguments {pairs, T, workers, worker}")
+    return b.value, e.value
 
 
 def _stream_ptr(stream) -> int:

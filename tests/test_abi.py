@@ -60,7 +60,12 @@ def test_variant_support_table(lib):
     assert not binding.variant_supports(0, 1, 8, 1, 64, 64)    # 0 is "auto", not a kernel
     assert binding.variant_supports(3, 1, 8, 1, 128, 128)      # tcgen05: K = V = 128 only
     assert not binding.variant_supports(3, 1, 8, 1, 64, 128)
-    assert binding.pick_variant(16, 8192, 32, 128, 128) == 3
+    assert binding.pick_variant(16, 8192, 32, 128, 128) == 7    # 512 pairs > 2 per SM: balanced
+    assert binding.pick_variant(8, 8192, 38, 128, 128) == 3     # 304 pairs: one wave
+    assert binding.pick_variant(8, 8192, 39, 128, 128) == 7
+    assert binding.variant_supports(7, 1, 8, 1, 128, 128)
+    assert not binding.variant_supports(7, 1, 8, 1, 64, 128)
+    assert binding.variant_name(7) == "tcgen05_k128_v128_balanced"
     assert binding.variant_supports(4, 1, 8, 1, 64, 128)       # 4-CTA cluster: K = 64, V = 128
     assert not binding.variant_supports(4, 1, 8, 1, 64, 64)
     assert binding.pick_variant(1, 65536, 16, 64, 128) == 4

@@ -107,7 +107,7 @@ BF16_SHAPES = [(1, 1, 1, 16, 16), (1, 2, 1, 16, 32), (3, 17, 1, 16, 64), (1, 63,
 
 
 def bf16_variants():
-    return [1, 2, 3, 4, 5, 6]
+    return [1, 2, 3, 4, 5, 6, 7]
 
 
 @pytest.mark.parametrize("B,T,N,K,V", BF16_SHAPES)
@@ -291,7 +291,7 @@ def test_unsupported_and_invalid_from_binding(K, V):
 
 
 @pytest.mark.parametrize("variant,K,V", [(1, 64, 64), (2, 64, 64), (3, 128, 128), (4, 64, 128),
-                                         (5, 64, 64), (6, 64, 64)])
+                                         (5, 64, 64), (6, 64, 64), (7, 128, 128)])
 def test_forced_wait_timeout_is_reported_and_context_survives(variant, K, V):
     inp = bf16_inputs(T=70, K=K, V=V)
     y = torch.empty((2, 70, 2, V), device=DEV)
@@ -302,3 +302,69 @@ def test_forced_wait_timeout_is_reported_and_context_survives(variant, K, V):
     y2, HT2 = run_gpu(inp)                            # the context is still usable
     yo, HTo = m2rnn_forward_inputs(all_f64(inp))
     assert max_err(y2, yo) <= TOL_BF16
+
+
+# ---------------------------------------------------------------- balanced K = V = 128 forward
+def balanced_cut_pairs(pairs, T):
+    """Pairs the balanced schedule splits between two blocks (two blocks per SM)."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    workers = min(pairs, 2 * sms)
+    cut = []
+    for w in range(workers):
+        _, e = binding.balanced_stretch(pairs, T, workers, w)
+        if e % T:
+            cut.append(e // T)
+    return cut
+
+
+@pytest.mark.parametrize("B,T,N", [(3, 300, 120), (2, 100, 200), (1, 1000, 320), (2, 260, 160)])
+def test_balanced_equals_one_block_per_pair_bitwise(B, T, N):
+    """More pairs than resident blocks: the balanced schedule (pairs cut between blocks, the
+    state handed over through y) gives the bits of one block per pair, and the cut pairs
+    match the oracle."""
+    wl = Workload("bal", B, T, N, 128, 128, h0="uniform")
+    inp = make_inputs(wl, DEV, 21)
+    y3, H3 = run_gpu(inp, variant=3)
+    y7, H7 = run_gpu(inp, variant=7)
+    assert torch.equal(y7, y3) and torch.equal(H7, H3)
+    cut = balanced_cut_pairs(B * N, T)
+    if T >= 2 * 129:
+        assert cut, "expected cut pairs"
+    for p in cut[:3] + cut[-1:]:
+        b, n = divmod(p, N)
+        yo, HTo = m2rnn_forward_inputs(slice_pair(inp, b, n))
+        assert max_err(y7[b:b + 1, :, n:n + 1], yo) <= TOL_BF16
+        assert max_err(H7[b:b + 1, n:n + 1], HTo) <= TOL_BF16
+
+
+def test_balanced_in_place_state_no_final_state_and_shared_qk():
+    wl = Workload("bal", 2, 300, 170, 128, 128, h0="uniform")
+    inp = make_inputs(wl, DEV, 22)
+    y_ref, HT_ref = run_gpu(inp, variant=3)
+    state = inp["H0"].clone()
+    inp2 = dict(inp)
+    inp2["H0"] = state
+    y = torch.empty_like(y_ref)
+    pkg.m2rnn_forward(inp2, y=y, H_T=state, variant=7)       # H0 == H_T
+    assert pkg.stream_status() == binding.OK
+    assert torch.equal(state, HT_ref) and torch.equal(y, y_ref)
+    y3, _ = run_gpu(inp, variant=7, H_T=False)                # H_T = NULL
+    assert torch.equal(y3, y_ref)
+    wls = Workload("bals", 2, 300, 170, 128, 128, h0="zero", shared_qk=True)
+    inps = make_inputs(wls, DEV, 23)
+    ya, Ha = run_gpu(inps, variant=3)
+    yb, Hb = run_gpu(inps, variant=7)
+    assert torch.equal(ya, yb) and torch.equal(Ha, Hb)
+
+
+def test_balanced_forced_timeout_with_cut_pairs():
+    wl = Workload("bal", 2, 300, 160, 128, 128, h0="uniform")
+    inp = make_inputs(wl, DEV, 24)
+    y = torch.empty((2, 300, 160, 128), device=DEV)
+    HT = torch.empty_like(inp["H0"])
+    pkg.m2rnn_forward(inp, y=y, H_T=HT, variant=7 | (1 << 8))
+    assert pkg.stream_status() == binding.ERR_TIMEOUT
+    assert pkg.stream_status() == binding.OK
+    y3, H3 = run_gpu(inp, variant=3)
+    y7, H7 = run_gpu(inp, variant=7)
+    assert torch.equal(y7, y3) and torch.equal(H7, H3)
