@@ -66,8 +66,10 @@ KERNEL_SOURCES = {
     "mma_sync_rowwarp": ["m2rnn_bf16_mma.cu"],
     "mma_sync_pipelined": ["m2rnn_bf16_pipe.cu"],
     "tcgen05_k128_v128": ["m2rnn_bf16_tc5.cu"],
+    "tcgen05_k128_v128_balanced": ["m2rnn_bf16_tc5.cu"],
     "mma_sync_cluster4_k64_v128": ["m2rnn_bf16_cluster.cu"],
     "mma_sync_rows8": ["m2rnn_bf16_r8.cu"],
+    "mma_sync_rows8_cluster2": ["m2rnn_bf16_r8.cu"],
     "backward_mma_k64_v64": ["m2rnn_bwd_bf16_mma.cu"],
     "backward_tc_k64_v64": ["m2rnn_bwd_bf16_tc.cu"],
     "backward_tc8_k64_v64": ["m2rnn_bwd_bf16_tc.cu"],

@@ -94,13 +94,15 @@ __device__ __forceinline__ unsigned long long ld_acquire_gpu(const unsigned long
   return v;
 }
 
+// kBalanced = false: block b runs pair b whole (the stretch logic folds away).
+template <bool kBalanced>
 __global__ void __launch_bounds__(kThreads, 2)
     fwd_bf16_tc5(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const uint16_t* __restrict__ a,
                  const float* __restrict__ alpha, const float* __restrict__ beta,
                  const uint16_t* __restrict__ W, const float* __restrict__ w_r, const float* H0,
                  float* y, float* H_T, int T, int N, int qk_hs, long long pairs,
-                 long long line_per_block, int reversed, uint32_t epoch, int debug,
+                 long long line_per_block, uint32_t epoch, int debug,
                  int* status) {
   extern __shared__ uint8_t smem_raw[];
   // Round the dynamic shared-memory base up to 1024 bytes (128-byte swizzle atoms).
@@ -130,12 +132,12 @@ __global__ void __launch_bounds__(kThreads, 2)
   // state over (the later stretch) has the lower block index and starts no later than the
   // block that waits for it.
   const long long worker =
-      reversed ? (long long)gridDim.x - 1 - blockIdx.x : (long long)blockIdx.x;
+      kBalanced ? (long long)gridDim.x - 1 - blockIdx.x : (long long)blockIdx.x;
   const long long total = pairs * (long long)T;
   const long long s_line =
-      tc5_cut(worker * line_per_block, total, T);
+      kBalanced ? tc5_cut(worker * line_per_block, total, T) : worker * (long long)T;
   const long long e_line =
-      tc5_cut((worker + 1) * line_per_block, total, T);
+      kBalanced ? tc5_cut((worker + 1) * line_per_block, total, T) : s_line + T;
 
   // ---------------------------------------------------------------- set-up
   if (tid == 0) {
@@ -199,9 +201,10 @@ __global__ void __launch_bounds__(kThreads, 2)
   // Segments in the block's order: the first steps of a pair that another block finishes
   // (state handed off), whole pairs, then the last steps of a pair that another block
   // started (state taken over).  Each step of each pair is run by exactly one block.
-  for (long long p = s_line / T; !abort && p * (long long)T < e_line; ++p) {
-    const long long lo = (s_line > p * T ? s_line : p * T) - p * T;
-    const long long hi = (e_line < (p + 1) * T ? e_line : (p + 1) * T) - p * T;
+  for (long long p = kBalanced ? s_line / T : worker;
+       kBalanced ? (!abort && p * (long long)T < e_line) : p == worker; ++p) {
+    const long long lo = kBalanced ? (s_line > p * T ? s_line : p * T) - p * T : 0;
+    const long long hi = kBalanced ? (e_line < (p + 1) * T ? e_line : (p + 1) * T) - p * T : T;
     const bool to_handoff = lo > 0;      // the line's [lo, T) is this pair's first T - lo steps
     const bool from_handoff = hi < T;    // the line's [0, hi) is this pair's last hi steps
     const int t0 = from_handoff ? T - (int)hi : 0;
@@ -434,8 +437,11 @@ cudaError_t launch_fwd_bf16_tc5(const Problem& p, EncodeTiledFn enc, cudaStream_
       !make_map_tc5(enc, &mk, p.k, p.Nqk, p.T, p.B) ||
       !make_map_tc5(enc, &mv, p.v, p.N, p.T, p.B))
     return cudaErrorInvalidValue;
-  cudaError_t err =
-      cudaFuncSetAttribute(fwd_bf16_tc5, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  cudaError_t err = cudaFuncSetAttribute(fwd_bf16_tc5<false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (err == cudaSuccess)
+    err = cudaFuncSetAttribute(fwd_bf16_tc5<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kSmemBytes);
   if (err != cudaSuccess) return err;
   const long long pairs = (long long)p.B * p.N;
   const int qk_hs = p.Nqk == 1 ? 0 : 1;
@@ -449,16 +455,16 @@ cudaError_t launch_fwd_bf16_tc5(const Problem& p, EncodeTiledFn enc, cudaStream_
     workers = tc5_balanced_workers(pairs, 2LL * sms);
   }
   if (workers >= pairs) {  // one block per pair
-    fwd_bf16_tc5<<<(unsigned)pairs, kThreads, kSmemBytes, stream>>>(
+    fwd_bf16_tc5<false><<<(unsigned)pairs, kThreads, kSmemBytes, stream>>>(
         mq, mk, mv, (const uint16_t*)p.a, p.alpha, p.beta, (const uint16_t*)p.W, p.w_r, p.H0, p.y,
-        p.H_T, p.T, p.N, qk_hs, pairs, (long long)p.T, 0, 0u, p.debug, p.status);
+        p.H_T, p.T, p.N, qk_hs, pairs, (long long)p.T, 0u, p.debug, p.status);
     return cudaGetLastError();
   }
   static std::atomic<uint32_t> epochs{0};
   const uint32_t epoch = epochs.fetch_add(1, std::memory_order_relaxed) + 1;
-  fwd_bf16_tc5<<<(unsigned)workers, kThreads, kSmemBytes, stream>>>(
+  fwd_bf16_tc5<true><<<(unsigned)workers, kThreads, kSmemBytes, stream>>>(
       mq, mk, mv, (const uint16_t*)p.a, p.alpha, p.beta, (const uint16_t*)p.W, p.w_r, p.H0, p.y,
-      p.H_T, p.T, p.N, qk_hs, pairs, tc5_line_per_block(pairs, p.T, workers), 1, epoch, p.debug,
+      p.H_T, p.T, p.N, qk_hs, pairs, tc5_line_per_block(pairs, p.T, workers), epoch, p.debug,
       p.status);
   return cudaGetLastError();
 }
