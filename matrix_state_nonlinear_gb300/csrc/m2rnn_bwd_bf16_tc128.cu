@@ -1,0 +1,549 @@
+// m2rnn_bwd_bf16_tc128.cu — backward pass of the M²RNN recurrence for V = 128 (K a multiple of
+// 16 up to 128) with every product of a step on the 5th-generation tensor cores.
+//
+// Reverse scan of the M²RNN study notes, Sec. 2.7 (gate of Eq. (13)/(17)), on the kept bf16
+// states S_t = bf16(H_t).  Per step t, from C_t = dL/dH_t (C_{T-1} = dH_T):
+//   P_t = S_{t-1} W + k_t v_t^T (recomputed),  Z_t = tanh(P_t),
+//   R_t = C_t + q_t u_t^T,  D_t = ((1 - f_t) R_t) ⊙ (1 - Z_t^2),
+//   C_{t-1} = f_t R_t + D_t W^T,  dW += S_{t-1}^T D_t,  dL/df_t = <R_t, S_{t-1} - Z_t>,
+//   dk_t = D_t v_t,  dv_t = D_t^T k_t + w_r ⊙ u_t,  dq_t = S_t u_t.
+// One thread block per (batch, head) pair, 256 threads: thread (row i = 32 (warp & 3) + lane,
+// column half warp >> 2) keeps its 64 entries of f R in fp32 registers and does the step's
+// elementwise work; thread 0 issues the TMA loads and the tensor-core products.  Rows are
+// padded to 128 (state rows K .. 127 stay zero, so they add nothing anywhere).
+//
+// Products of one step, issued together after the block has written the bf16 D_t tile (128-byte
+// swizzle, K-major) and committed to one mbarrier, in this order:
+//   G_t = D_t W^T            (A = D K-major, B = the W^T tile read N-major; M = N = 128)
+//   dW += S_{t-1}^T D_t      (A = the state tile read M-major, B = D read N-major; one
+//                             accumulator over the whole sequence)
+//   dk_t = D_t v_t, dv_t = D_t^T k_t   (N = 16 products whose B row 0 holds v_t / k_t)
+//   dq_{t-1} = S_{t-1} u_{t-1}         (B rows 0 and 1 hold the bf16 high and low parts of u,
+//                                       so u keeps fp32 accuracy)
+//   P_{t-1} = S_{t-2} W + k_{t-1} v_{t-1}^T   (8 K = 16 steps, then the rank-1 step whose A
+//                                               column 0 is k and B column 0 is v)
+// The next step waits for that one commit: G and P are then ready, and D, the small tiles and
+// the state slot of S_t are free again.  The state tiles (32 KB each) stream through a ring of
+// three slots, one TMA load per step, three steps ahead of their first use; the per-step
+// inputs (q, k, v, dy) are copied one step ahead with cp.async.  Every wait is bounded; a
+// timeout is decided jointly by the block (OR-reduction barrier), in-flight work gets a bounded
+// chance to finish, and the block releases tensor memory and exits.
+#include <cuda_bf16.h>
+
+#include "m2rnn_internal.h"
+#include "ptx_util.cuh"
+
+namespace m2rnn {
+namespace {
+
+constexpr int kV = 128;         // value width (the products are M = N = 128)
+constexpr int kR = 128;         // rows of the padded state
+constexpr int kThreads = 256;   // 8 warps: lane quadrant (warp & 3) x column half (warp >> 2)
+constexpr int kTile = kR * kV * 2;         // one bf16 128 x 128 tile: [2 column halves][128][128 B]
+constexpr int kSmallTile = 16 * kV * 2;    // an N = 16 B operand: [2 K-blocks][16 rows][128 B]
+constexpr int kSlots = 3;                  // state ring
+
+// Tensor-memory columns.
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColP = 0, kColG = 128, kColW = 256, kColDk = 384, kColDv = 400, kColDq = 416;
+
+// Shared memory layout (bytes from a 1024-aligned base).
+constexpr int kOffWt = 0;                          // W^T: row j, column l holds W[l][j]
+constexpr int kOffD = kOffWt + kTile;              // D_t (bf16), row i, column j
+constexpr int kOffS = kOffD + kTile;               // state slots [kSlots]
+constexpr int kOffBv = kOffS + kSlots * kTile;     // dk's B: row 0 = v_t
+constexpr int kOffBk = kOffBv + kSmallTile;        // dv's B: row 0 = k_t (K index = row i)
+constexpr int kOffBu = kOffBk + kSmallTile;        // dq's B: rows 0, 1 = bf16 hi, lo of u_{t-1}
+constexpr int kOffAx = kOffBu + kSmallTile;        // rank-1 A: [128 rows x 16] core matrices
+constexpr int kOffBx = kOffAx + 4096;              // rank-1 B: same layout
+constexpr int kInBytes = kV * 4 + kV * 2 + 2 * kR * 2;  // u (f32), v, q, k (bf16)
+constexpr int kOffIn = kOffBx + 4096;              // per-step inputs [2]
+constexpr int kInU = 0, kInV = kV * 4, kInQ = kInV + kV * 2, kInK = kInQ + kR * 2;
+constexpr int kOffGate = kOffIn + 2 * kInBytes;    // float4 [2]: f, 1 - f, sigmoid(x), softplus(x)
+constexpr int kOffDf = kOffGate + 2 * 16;          // float [2][8]: dL/df partials per warp
+constexpr int kOffBar = kOffDf + 2 * 8 * 4;        // batch, state_full[kSlots], never; tmem slot
+constexpr int kSmemBytes = kOffBar + 64 + 1024;    // + slack to align the base to 1024
+
+__device__ __forceinline__ uint32_t sw128_off(int r, int k, int rows) {
+  return (uint32_t)((k >> 6) * rows * 128 + (r >> 3) * 1024 + (r & 7) * 128 +
+                    ((((k & 63) >> 3) ^ (r & 7)) << 4) + (k & 7) * 2);
+}
+__device__ __forceinline__ uint32_t core_off(int r, int k) {  // no-swizzle, K = 16
+  return (uint32_t)((r >> 3) * 256 + (k >> 3) * 128 + (r & 7) * 16 + (k & 7) * 2);
+}
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gsrc)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+}
+// Gate of Eq. (13)/(17) and the factors of its derivative: f, 1 - f, sigmoid(x), softplus(x)
+// with x = a + beta.
+__device__ __forceinline__ float4 gate4(float a, float al, float be) {
+  const float x = a + be;
+  const float ex = expf(-fabsf(x));
+  const float sp = fmaxf(x, 0.f) + log1pf(ex);
+  const float sg = x >= 0.f ? 1.f / (1.f + ex) : ex / (1.f + ex);
+  return make_float4(expf(-al * sp), -expm1f(-al * sp), sg, sp);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_bf16_tc128(const __grid_constant__ CUtensorMap tm_h, const uint16_t* __restrict__ q,
+                   const uint16_t* __restrict__ k, const uint16_t* __restrict__ v,
+                   const uint16_t* __restrict__ a, const float* __restrict__ alpha,
+                   const float* __restrict__ beta, const uint16_t* __restrict__ W,
+                   const float* __restrict__ w_r, const float* __restrict__ H0,
+                   const float* __restrict__ dy, const float* __restrict__ dH_T,
+                   float* __restrict__ dq, float* __restrict__ dk, float* __restrict__ dv,
+                   float* __restrict__ da, float* __restrict__ dH0, float* __restrict__ ws,
+                   float* __restrict__ dqk_heads, int T, int N, int Nqk, int K, int debug,
+                   int* status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int qd = warp & 3, ch = warp >> 2;
+  const int i = 32 * qd + lane;  // row of the state owned by this thread (and TMEM lane)
+  const int c0 = 64 * ch;        // first of its 64 columns
+  const int pair = blockIdx.x, b = pair / N, n = pair - (pair / N) * N;
+  const bool shared_qk = Nqk == 1 && N > 1;
+  const int nq = Nqk == 1 ? 0 : n;
+  const int krows = (K + 15) >> 4;  // 16-row groups of the state
+  const float al = alpha[n], be = beta[n];
+
+  uint8_t* sWt = smem + kOffWt;
+  uint8_t* sD = smem + kOffD;
+  uint8_t* sBv = smem + kOffBv;
+  uint8_t* sBk = smem + kOffBk;
+  uint8_t* sBu = smem + kOffBu;
+  uint8_t* sAx = smem + kOffAx;
+  uint8_t* sBx = smem + kOffBx;
+  float4* gates = reinterpret_cast<float4*>(smem + kOffGate);
+  float* dfpart = reinterpret_cast<float*>(smem + kOffDf);
+  uint64_t* batch = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  uint64_t* sfull = batch + 1;  // [kSlots]
+  uint64_t* never = batch + 1 + kSlots;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(batch + 2 + kSlots);
+  auto slot_of = [](int s) { return (s + 1) % kSlots; };  // state s >= -1
+  auto state_tile = [&](int s) { return smem + kOffS + slot_of(s) * kTile; };
+  // Parity of the load of state s into its slot (loads go in decreasing s).
+  auto state_parity = [&](int s) { return (uint32_t)((T - 1 - s) / kSlots) & 1u; };
+  auto in_buf = [&](int t) { return smem + kOffIn + (t & 1) * kInBytes; };
+  const long long limit = kWaitLimitCycles;
+
+  // Copies of step t's inputs into in_buf(t) (threads 0 .. 63); thread 64 loads a_t, whose
+  // gate it writes later (put_gate), once the load has long arrived.
+  float a_pref = 0.f;
+  auto fetch_inputs = [&](int t) {
+    uint8_t* dst = in_buf(t);
+    const size_t row = ((size_t)b * T + t) * N + n;
+    const size_t qrow = ((size_t)b * T + t) * Nqk + nq;
+    if (tid < 32) {
+      cp_async16(dst + kInU + 16 * tid, dy + row * kV + 4 * tid);
+    } else if (tid < 48) {
+      cp_async16(dst + kInV + 16 * (tid - 32), v + row * kV + 8 * (tid - 32));
+    } else if (tid < 64) {
+      const int c = tid - 48;  // 16-byte chunks of q then k (K / 8 each)
+      if (c < (K >> 3)) {
+        cp_async16(dst + kInQ + 16 * c, q + qrow * K + 8 * c);
+        cp_async16(dst + kInK + 16 * c, k + qrow * K + 8 * c);
+      }
+    } else if (tid == 64) {
+      a_pref = bf16_bits_to_float(a[row]);
+    }
+    cp_async_commit();
+  };
+  auto put_gate = [&](int t) {
+    if (tid == 64) gates[t & 1] = gate4(a_pref, al, be);
+  };
+  // Writes the bf16 of H_0 (or zeros) as state -1 (all threads; rows < K).
+  auto put_h0 = [&](uint8_t* tile) {
+    if (i < K) {
+      const float* hp = H0 ? H0 + ((size_t)pair * K + i) * kV + c0 : nullptr;
+#pragma unroll 4
+      for (int c = 0; c < 64; c += 8) {
+        float x[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = hp ? hp[c + e] : 0.f;
+        *reinterpret_cast<uint4*>(tile + sw128_off(i, c0 + c, kR)) =
+            make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]),
+                       pack_bf16x2(x[4], x[5]), pack_bf16x2(x[6], x[7]));
+      }
+    }
+    fence_proxy_async_smem();
+  };
+  // Starts the load of state s >= -1 into its slot: TMA for s >= 0 (thread 0); the bf16 of
+  // H_0 for s = -1 (every thread writes its row; thread 0 completes the slot's phase).
+  auto load_state = [&](int s) {
+    uint64_t* bar = &sfull[slot_of(s)];
+    if (s >= 0) {
+      if (tid == 0) {
+        mbar_arrive_expect_tx(bar, (uint32_t)(2 * 64 * K * 2));
+        tma_load_4d(state_tile(s), &tm_h, bar, 0, 0, s, pair);
+        tma_load_4d(state_tile(s) + kR * 128, &tm_h, bar, 64, 0, s, pair);
+      }
+    } else {
+      put_h0(state_tile(s));
+      if (tid == 0) mbar_arrive(bar);
+    }
+  };
+
+  // ---------------------------------------------------------------- set-up
+  if (tid == 0) {
+    prefetch_tensormap(&tm_h);
+    mbar_init(batch, 1);
+    for (int s = 0; s < kSlots; ++s) mbar_init(&sfull[s], 1);
+    mbar_init(never, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) tmem_alloc(tmem_slot, kTmemCols);
+  // Zero D, the state slots and the small tiles (padding rows and unused operand rows stay 0).
+  for (int e = tid; e < (kOffIn - kOffD) / 16; e += kThreads)
+    reinterpret_cast<uint4*>(sD)[e] = make_uint4(0u, 0u, 0u, 0u);
+  fence_proxy_async_smem();  // the zeros before any TMA write into the same tiles
+  // W^T tile: row j, column l holds W[l][j].
+  const uint16_t* Wn = W + (size_t)n * kV * kV;
+  for (int e = tid; e < kV * kV; e += kThreads) {
+    const int l = e >> 7, j = e & 127;
+    *reinterpret_cast<uint16_t*>(sWt + sw128_off(j, l, kR)) = Wn[e];
+  }
+  // The running f R of this thread's row: C_{T-1} = dH_T (or 0), no G yet.
+  float2 cf[32];
+  {
+    const float* gp = (dH_T && i < K) ? dH_T + ((size_t)pair * K + i) * kV + c0 : nullptr;
+#pragma unroll
+    for (int u = 0; u < 32; ++u)
+      cf[u] = gp ? *reinterpret_cast<const float2*>(gp + 2 * u) : make_float2(0.f, 0.f);
+  }
+  float dwr_acc = 0.f, dal_acc = 0.f, dbe_acc = 0.f;
+  const float wr_j = w_r[(size_t)n * kV + i];  // w_r of column j = i (column-half 1 threads)
+  __syncthreads();  // the zeroed slots before any load lands in them
+  for (int s = T - 1; s >= T - 3 && s >= -1; --s) load_state(s);
+  fetch_inputs(T - 1);
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t t_lane = tmem + ((uint32_t)(32 * qd) << 16);
+
+  const uint32_t idesc_kk = umma_idesc_bf16(kR, kV, false);              // K-major A and B
+  const uint32_t idesc_g = umma_idesc_bf16_ab(kR, kV, false, true);      // B read N-major
+  const uint32_t idesc_w = umma_idesc_bf16_ab(kV, kV, true, true);       // both M/N-major
+  const uint32_t idesc_s = umma_idesc_bf16(kR, 16, false);               // N = 16, A K-major
+  const uint32_t idesc_sm = umma_idesc_bf16(kV, 16, true);               // N = 16, A M-major
+  auto dK = [&](const uint8_t* tile) { return umma_desc(smem_u32(tile), 16, 1024, 2); };
+  auto dMN = [&](const uint8_t* tile) { return umma_desc(smem_u32(tile), 16384, 1024, 2); };
+  // K-step kk (16 columns) of a K-major 128-column tile with `rows` rows, in 16-byte units.
+  auto koff = [](int kk, int rows) {
+    return (uint64_t)(((kk >> 2) * rows * 128 + (kk & 3) * 32) >> 4);
+  };
+  const uint64_t mnstep = 2048 >> 4;  // 16 rows of an M/N-major read
+  const uint64_t dAx = umma_desc(smem_u32(sAx), 128, 256, 0);
+  const uint64_t dBx = umma_desc(smem_u32(sBx), 128, 256, 0);
+
+  // Small operands of the batch issued at the end of step t (t = T means the first batch):
+  // rank-1 of step t - 1 (k, v), dq_{t-1}'s u rows, and for t < T dk_t's v and dv_t's k rows.
+  auto put_small = [&](int t) {
+    if (t - 1 >= 0) {
+      const uint8_t* in1 = in_buf(t - 1);
+      // Rank-1 A column 0 = k_{t-1} (rows < K), B column 0 = v_{t-1}: column-half 0 / 1.
+      if (ch == 0) {
+        const uint16_t kv = i < K ? reinterpret_cast<const uint16_t*>(in1 + kInK)[i] : 0;
+        *reinterpret_cast<uint16_t*>(sAx + core_off(i, 0)) = kv;
+      } else {
+        *reinterpret_cast<uint16_t*>(sBx + core_off(i, 0)) =
+            reinterpret_cast<const uint16_t*>(in1 + kInV)[i];
+      }
+      // u_{t-1} as bf16 hi (row 0) and lo (row 1) parts; thread pairs cover the 128 columns.
+      if (tid < 64) {
+        const float2 x = reinterpret_cast<const float2*>(in1 + kInU)[tid];
+        const uint32_t hi = pack_bf16x2(x.x, x.y);
+        const float2 hf = bf16x2_to_float2(hi);
+        *reinterpret_cast<uint32_t*>(sBu + sw128_off(0, 2 * tid, 16)) = hi;
+        *reinterpret_cast<uint32_t*>(sBu + sw128_off(1, 2 * tid, 16)) =
+            pack_bf16x2(x.x - hf.x, x.y - hf.y);
+      }
+    }
+    if (t < T) {
+      const uint8_t* in0 = in_buf(t);
+      if (ch == 0) {  // dv's B row 0: k_t over the rows (K index = row i)
+        const uint16_t kv = i < K ? reinterpret_cast<const uint16_t*>(in0 + kInK)[i] : 0;
+        *reinterpret_cast<uint16_t*>(sBk + sw128_off(0, i, 16)) = kv;
+      } else {        // dk's B row 0: v_t over the columns
+        *reinterpret_cast<uint16_t*>(sBv + sw128_off(0, i, 16)) =
+            reinterpret_cast<const uint16_t*>(in0 + kInV)[i];
+      }
+    }
+    fence_proxy_async_smem();
+  };
+  // The batch of products issued at the end of step t (thread 0), see the file comment.
+  // t = T: only dq_{T-1} and P_{T-1}.
+  auto issue = [&](int t) {
+    tc_fence_after();
+    if (t < T) {
+      const uint8_t* sprev = state_tile(t - 1);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)  // G_t = D_t W^T
+        umma_bf16(tmem + kColG, dK(sD) + koff(kk, kR), dMN(sWt) + kk * mnstep, idesc_g, kk);
+      for (int kk = 0; kk < krows; ++kk)  // dW += S_{t-1}^T D_t
+        umma_bf16(tmem + kColW, dMN(sprev) + kk * mnstep, dMN(sD) + kk * mnstep, idesc_w,
+                  (t < T - 1 || kk > 0) ? 1u : 0u);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)  // dk_t = D_t v_t
+        umma_bf16(tmem + kColDk, dK(sD) + koff(kk, kR), dK(sBv) + koff(kk, 16), idesc_s, kk);
+      for (int kk = 0; kk < krows; ++kk)  // dv_t = D_t^T k_t
+        umma_bf16(tmem + kColDv, dMN(sD) + kk * mnstep, dK(sBk) + koff(kk, 16), idesc_sm, kk);
+    }
+    if (t >= 1) {
+      const uint8_t* sprev = state_tile(t - 1);
+      const uint8_t* sprev2 = state_tile(t - 2);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)  // dq_{t-1} = S_{t-1} u_{t-1}
+        umma_bf16(tmem + kColDq, dK(sprev) + koff(kk, kR), dK(sBu) + koff(kk, 16), idesc_s, kk);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)  // P_{t-1} = S_{t-2} W + k_{t-1} v_{t-1}^T
+        umma_bf16(tmem + kColP, dK(sprev2) + koff(kk, kR), dK(sWt) + koff(kk, kR), idesc_kk,
+                  kk);
+      umma_bf16(tmem + kColP, dAx, dBx, idesc_kk, 1u);
+    }
+    umma_commit(batch);
+  };
+
+  // First batch: dq_{T-1} and P_{T-1} need S_{T-1}, S_{T-2} and step T-1's inputs.
+  bool ok = true;
+  if (tid == 0) {
+    ok = mbar_wait_bounded(&sfull[slot_of(T - 1)], state_parity(T - 1), limit);
+    ok = ok && mbar_wait_bounded(&sfull[slot_of(T - 2)], state_parity(T - 2), limit);
+    if (debug & kDebugForceTimeout) ok = ok && mbar_wait_bounded(never, 0u, kDebugWaitLimitCycles);
+  }
+  cp_async_wait_all();
+  __syncthreads();
+  put_small(T);
+  put_gate(T - 1);
+  tc_fence_before();
+  bool abort = __syncthreads_or(!ok);
+  if (!abort && tid == 0) issue(T);
+  uint32_t batch_ph = 0;
+  bool has_g = false;
+
+  for (int t = T - 1; t >= 0 && !abort; --t) {
+    // The previous batch: G_{t+1}, dW_{t+1}, dk_{t+1}, dv_{t+1}, dq_t, P_t.
+    ok = mbar_wait_bounded(batch, batch_ph & 1u, limit);
+    ++batch_ph;
+    const uint8_t* in0 = in_buf(t);
+    const float u1 = (ch == 1 && t + 1 < T)
+                         ? reinterpret_cast<const float*>(in_buf(t + 1) + kInU)[i] : 0.f;
+    // Joint decision; past this barrier nothing reads in_buf(t + 1) any more, so it takes step
+    // t - 1's inputs, and the slot state t has left takes state t - 3.
+    tc_fence_before();
+    abort = __syncthreads_or(!ok);
+    if (abort) break;
+    tc_fence_after();
+    if (t >= 1) fetch_inputs(t - 1);
+    if (t - 3 >= -1) load_state(t - 3);
+    // dq_t (column-half 0, rows < K); dk_{t+1} (column-half 0) and dv_{t+1} (column-half 1).
+    {
+      if (ch == 0) {
+        const float dq0 = tmem_ld1(t_lane + kColDq), dq1 = tmem_ld1(t_lane + kColDq + 1);
+        float dk1 = 0.f;
+        if (t + 1 < T) dk1 = tmem_ld1(t_lane + kColDk);
+        if (i < K) {
+          const size_t r0 = ((size_t)b * T + t) * (shared_qk ? N : Nqk) + (shared_qk ? n : nq);
+          float* dqo = shared_qk ? dqk_heads : dq;
+          float* dko = shared_qk ? dqk_heads + (size_t)gridDim.x * T * K : dk;
+          dqo[r0 * K + i] = dq0 + dq1;
+          if (t + 1 < T) dko[(r0 + (shared_qk ? N : Nqk)) * K + i] = dk1;
+        }
+      } else if (t + 1 < T) {
+        const float dv1 = tmem_ld1(t_lane + kColDv);
+        dv[(((size_t)b * T + t + 1) * N + n) * kV + i] = fmaf(wr_j, u1, dv1);
+      }
+    }
+
+    // ---- elementwise step t
+    const float4 gt = gates[t & 1];
+    const float2 ff = make_float2(gt.x, gt.x), gg = make_float2(gt.y, gt.y);
+    const float qi = i < K ? bf16_bits_to_float(reinterpret_cast<const uint16_t*>(in0 + kInQ)[i])
+                           : 0.f;
+    const float2 q2 = make_float2(qi, qi);
+    const float2* u2 = reinterpret_cast<const float2*>(in0 + kInU) + c0 / 2;
+    const uint8_t* sprev = state_tile(t - 1);
+    // The state tile S_{t-1} was waited for by thread 0 before P_t; every thread observes its
+    // load's completion before reading it.
+    ok = ok && mbar_wait_bounded(&sfull[slot_of(t - 1)], state_parity(t - 1), limit);
+    float2 dfp = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int piece = 0; piece < 4; ++piece) {
+      float pv[16], gv[16];
+      tmem_ld16_nowait(t_lane + kColP + c0 + 16 * piece, pv);
+      if (has_g) tmem_ld16_nowait(t_lane + kColG + c0 + 16 * piece, gv);
+      const uint4 hp0 = *reinterpret_cast<const uint4*>(sprev + sw128_off(i, c0 + 16 * piece, kR));
+      const uint4 hp1 =
+          *reinterpret_cast<const uint4*>(sprev + sw128_off(i, c0 + 16 * piece + 8, kR));
+      tmem_wait_ld();
+      const uint32_t hw[8] = {hp0.x, hp0.y, hp0.z, hp0.w, hp1.x, hp1.y, hp1.z, hp1.w};
+      uint32_t dpk[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int u = 8 * piece + e;  // float2 index within the thread's 64 columns
+        const float2 z = make_float2(tanh_mufu(pv[2 * e]), tanh_mufu(pv[2 * e + 1]));
+        const float2 c = has_g ? add2(cf[u], make_float2(gv[2 * e], gv[2 * e + 1])) : cf[u];
+        const float2 r = fma2(q2, u2[u], c);                        // R = C + q u^T
+        const float2 om = fma2(make_float2(-z.x, -z.y), z, make_float2(1.f, 1.f));
+        const float2 d = mul2(mul2(gg, r), om);                     // D = (1 - f) R (1 - Z^2)
+        const float2 hpv = bf16x2_to_float2(hw[e]);
+        dfp = fma2(r, sub2(hpv, z), dfp);                           // <R, S_{t-1} - Z>
+        cf[u] = mul2(ff, r);                                        // f R, for C_{t-1}
+        dpk[e] = pack_bf16x2(d.x, d.y);
+      }
+      *reinterpret_cast<uint4*>(sD + sw128_off(i, c0 + 16 * piece, kR)) =
+          make_uint4(dpk[0], dpk[1], dpk[2], dpk[3]);
+      *reinterpret_cast<uint4*>(sD + sw128_off(i, c0 + 16 * piece + 8, kR)) =
+          make_uint4(dpk[4], dpk[5], dpk[6], dpk[7]);
+    }
+    has_g = true;
+    // dL/df_t partial of the warp; dw_r += u_t ⊙ v_t (column-half 1: column j = i).
+    float dsum = dfp.x + dfp.y;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, o);
+    if (lane == 0) dfpart[(t & 1) * 8 + warp] = dsum;
+    if (ch == 1)
+      dwr_acc = fmaf(reinterpret_cast<const float*>(in0 + kInU)[i],
+                     bf16_bits_to_float(reinterpret_cast<const uint16_t*>(in0 + kInV)[i]),
+                     dwr_acc);
+    // Step t - 1's inputs (for the rank-1 and u rows) and the small operand tiles.
+    cp_async_wait_all();
+    __syncthreads();
+    put_small(t);
+    if (t >= 1) put_gate(t - 1);
+    if (tid == 0 && t >= 1)
+      ok = ok && mbar_wait_bounded(&sfull[slot_of(t - 2)], state_parity(t - 2), limit);
+    fence_proxy_async_smem();
+    tc_fence_before();
+    abort = __syncthreads_or(!ok);
+    if (abort) break;
+    if (tid == 0) issue(t);
+    if (tid == 32) {  // da_t and the dalpha, dbeta sums
+      float df = 0.f;
+#pragma unroll
+      for (int w = 0; w < 8; ++w) df += dfpart[(t & 1) * 8 + w];
+      const float d_a = df * (-al * gt.x * gt.z);
+      da[((size_t)b * T + t) * N + n] = d_a;
+      dal_acc = fmaf(df, -gt.x * gt.w, dal_acc);
+      dbe_acc += d_a;
+    }
+  }
+
+  if (!abort) {
+    // The last batch: G_0, dW_0, dk_0, dv_0.
+    const bool ok2 = mbar_wait_bounded(batch, batch_ph & 1u, limit);
+    tc_fence_before();
+    abort = __syncthreads_or(!ok2);
+    tc_fence_after();
+    if (!abort) {
+      const uint8_t* in0 = in_buf(0);
+      if (ch == 0) {
+        const float dk0 = tmem_ld1(t_lane + kColDk);
+        if (i < K) {
+          const size_t r0 = ((size_t)b * T) * (shared_qk ? N : Nqk) + (shared_qk ? n : nq);
+          float* dko = shared_qk ? dqk_heads + (size_t)gridDim.x * T * K : dk;
+          dko[r0 * K + i] = dk0;
+        }
+      } else {
+        const float dv0 = tmem_ld1(t_lane + kColDv);
+        const float u0 = reinterpret_cast<const float*>(in0 + kInU)[i];
+        dv[(((size_t)b * T) * N + n) * kV + i] = fmaf(wr_j, u0, dv0);
+      }
+      // dH_0 = C_{-1} = f_0 R_0 + G_0.
+      if (dH0) {
+        float* hp = dH0 + ((size_t)pair * K + i) * kV + c0;
+#pragma unroll
+        for (int piece = 0; piece < 4; ++piece) {
+          float gv[16];
+          tmem_ld16_nowait(t_lane + kColG + c0 + 16 * piece, gv);
+          tmem_wait_ld();
+          if (i < K) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const int u = 8 * piece + e;
+              *reinterpret_cast<float2*>(hp + 2 * u) =
+                  add2(cf[u], make_float2(gv[2 * e], gv[2 * e + 1]));
+            }
+          }
+        }
+      }
+      // This pair's dW (TMEM lane j, columns j'), dw_r, dalpha and dbeta partials.
+      float* wsp = ws + (size_t)pair * backward_pair_floats(K, kV);
+      float* dWp = wsp + (size_t)K * kV;
+      float* dwr_p = dWp + kV * kV;
+      float* ab_p = dwr_p + kV;
+#pragma unroll
+      for (int piece = 0; piece < 4; ++piece) {
+        float wv[16];
+        tmem_ld16_nowait(t_lane + kColW + c0 + 16 * piece, wv);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 16; e += 4)
+          *reinterpret_cast<float4*>(dWp + (size_t)i * kV + c0 + 16 * piece + e) =
+              make_float4(wv[e], wv[e + 1], wv[e + 2], wv[e + 3]);
+      }
+      if (ch == 1) dwr_p[i] = dwr_acc;
+      if (tid == 32) {
+        ab_p[0] = dal_acc;
+        ab_p[1] = dbe_acc;
+      }
+    }
+  }
+  if (abort && tid == 0) {
+    atomicExch(status, kStatusTimeout);
+    // Give a tensor-core batch or TMA copy still in flight a bounded chance to finish.
+    mbar_wait_bounded(batch, 0u, kDebugWaitLimitCycles);
+    mbar_wait_bounded(batch, 1u, kDebugWaitLimitCycles);
+    for (int s = 0; s < kSlots; ++s) {
+      mbar_wait_bounded(&sfull[s], 0u, kDebugWaitLimitCycles);
+      mbar_wait_bounded(&sfull[s], 1u, kDebugWaitLimitCycles);
+    }
+  }
+  cp_async_wait_all();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+}
+
+}  // namespace
+
+bool bwd_tc128_supports(int K, int V) { return V == kV && K >= 16 && K <= kR && K % 16 == 0; }
+
+cudaError_t launch_bwd_bf16_tc128(const BackwardProblem& p, EncodeTiledFn enc, int debug,
+                                  int* status, cudaStream_t stream) {
+  if (!bwd_tc128_supports(p.K, p.V) || p.T < 1) return cudaErrorInvalidValue;
+  // Kept states [B N, T, K, V] bf16: a box of 64 columns x K rows of one step (128-byte
+  // swizzle, the K-major operand layout).
+  CUtensorMap mh;
+  const cuuint64_t dims[4] = {(cuuint64_t)kV, (cuuint64_t)p.K, (cuuint64_t)p.T,
+                              (cuuint64_t)p.B * p.N};
+  const cuuint64_t strides[3] = {(cuuint64_t)kV * 2, (cuuint64_t)kV * 2 * p.K,
+                                 (cuuint64_t)kV * 2 * p.K * p.T};
+  const cuuint32_t box[4] = {64u, (cuuint32_t)p.K, 1u, 1u};
+  const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  if (enc(&mh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(p.Hs), dims, strides, box,
+          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  cudaError_t err =
+      cudaFuncSetAttribute(bwd_bf16_tc128, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (err != cudaSuccess) return err;
+  float* heads = p.ws + (size_t)p.B * p.N * backward_pair_floats(p.K, p.V);
+  bwd_bf16_tc128<<<(unsigned)(p.B * p.N), kThreads, kSmemBytes, stream>>>(
+      mh, (const uint16_t*)p.q, (const uint16_t*)p.k, (const uint16_t*)p.v, (const uint16_t*)p.a,
+      p.alpha, p.beta, (const uint16_t*)p.W, p.w_r, p.H0, p.dy, p.dH_T, p.dq, p.dk, p.dv, p.da,
+      p.dH0, p.ws, heads, p.T, p.N, p.Nqk, p.K, debug, status);
+  err = cudaGetLastError();
+  return err == cudaSuccess ? launch_bwd_reduce(p, stream) : err;
+}
+
+}  // namespace m2rnn

@@ -168,6 +168,12 @@ cudaError_t launch_bwd_bf16_tc(const BackwardProblem& p, EncodeTiledFn enc, int 
 cudaError_t launch_bwd_bf16_tcc(const BackwardProblem& p, EncodeTiledFn enc, int debug,
                                 int* status, cudaStream_t stream);
 
+// Backward for V = 128 (K a multiple of 16 up to 128, rows padded to 128) with every product
+// on tcgen05 (tensor-memory accumulators, TMA-streamed bf16 states), then the reduction.
+bool bwd_tc128_supports(int K, int V);
+cudaError_t launch_bwd_bf16_tc128(const BackwardProblem& p, EncodeTiledFn enc, int debug,
+                                  int* status, cudaStream_t stream);
+
 // One decode step (T = 1) on the warp MMA: K % 16 == 0, K <= 128, V in {16, 32, 64, 128}.
 // Uses q, k, v, a, alpha, beta, W, w_r, H0 (state in, may be null), H_T (state out, may
 // equal H0), y, B, N, K, V, Nqk and status of the problem.  K = V = 64 with at least 2048

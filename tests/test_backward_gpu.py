@@ -131,13 +131,22 @@ BF16_SHAPES = [(1, 1, 1, 16, 16), (2, 65, 3, 64, 64), (1, 130, 2, 32, 32), (2, 4
                # exactly two, and a two-step sequence
                (1, 8, 2, 64, 64), (1, 9, 1, 64, 64), (1, 16, 2, 64, 64), (2, 2, 1, 64, 64),
                # ragged K, V of 48 / 80 (row-warp state-keeping forward, SIMT backward)
-               (1, 20, 2, 24, 48), (2, 15, 1, 1, 80)]
+               (1, 20, 2, 24, 48), (2, 15, 1, 1, 80),
+               # V = 128 on the tensor-core backward: one, two, three and four steps (the state
+               # ring's start), rows padded from K = 16, 32, 48, 64, 96 to 128
+               (1, 1, 1, 16, 128), (1, 2, 1, 32, 128), (2, 3, 1, 128, 128), (1, 4, 1, 64, 128),
+               (2, 37, 2, 48, 128), (1, 70, 1, 128, 128)]
 
 
 def bwd_variants(K, V):
     # 1: SIMT (any shape); 2: warp-MMA kernel; 3, 4: tcgen05 kernels with 4 or 8 compute
-    # warps; 5: every product on tcgen05, the chain included (K = V = 64)
-    return [1, 2, 3, 4, 5] if (K, V) == (64, 64) else [1]
+    # warps; 5: every product on tcgen05, the chain included (K = V = 64); 6: every product
+    # on tcgen05 for V = 128 (K a multiple of 16)
+    if (K, V) == (64, 64):
+        return [1, 2, 3, 4, 5]
+    if V == 128 and K % 16 == 0:
+        return [1, 6]
+    return [1]
 
 
 @pytest.mark.parametrize("shape", BF16_SHAPES)
@@ -148,39 +157,45 @@ def test_backward_bf16_matches_oracle(shape, h0):
         assert max(errs.values()) <= TOL["bf16"], (variant, errs)
 
 
-@pytest.mark.parametrize("variant", [1, 2, 3, 4, 5])
+def kv_of(variant):
+    return (64, 128) if variant == 6 else (64, 64)
+
+
+@pytest.mark.parametrize("variant", [1, 2, 3, 4, 5, 6])
 def test_backward_bf16_shared_qk(variant):
-    _, _, g, errs = run_case("bf16", 2, 50, 4, 64, 64, shared=True, variant=variant)
+    _, _, g, errs = run_case("bf16", 2, 50, 4, *kv_of(variant), shared=True, variant=variant)
     assert g["dq"].shape[2] == 1
     assert max(errs.values()) <= TOL["bf16"], errs
 
 
-@pytest.mark.parametrize("variant", [2, 3, 4, 5])
+@pytest.mark.parametrize("variant", [2, 3, 4, 5, 6])
 def test_backward_mma_without_dHT(variant):
-    _, _, _, errs = run_case("bf16", 2, 37, 2, 64, 64, with_dHT=False, variant=variant)
+    _, _, _, errs = run_case("bf16", 2, 37, 2, *kv_of(variant), with_dHT=False, variant=variant)
     assert max(errs.values()) <= TOL["bf16"], errs
 
 
-@pytest.mark.parametrize("variant", [2, 3, 4, 5])
+@pytest.mark.parametrize("variant", [2, 3, 4, 5, 6])
 def test_backward_mma_close_to_simt(variant):
     """The kernels differentiate the same kept states; they differ only by rounding
     (bf16 D in the MMA products vs fp32 SIMT sums)."""
-    wl = Workload("cmp", 2, 90, 3, 64, 64, h0="uniform")
+    K, V = kv_of(variant)
+    wl = Workload("cmp", 2, 90, 3, K, V, h0="uniform")
     inp = make_inputs(wl, DEV, 8)
     _, _, Hs = pkg.m2rnn_forward_train(inp)
-    dy, dHT = upstream(2, 90, 3, 64, 64, 9)
+    dy, dHT = upstream(2, 90, 3, K, V, 9)
     g1 = pkg.m2rnn_backward(inp, Hs, dy, dHT, variant=1)
     g2 = pkg.m2rnn_backward(inp, Hs, dy, dHT, variant=variant)
     for n in GRADS:
         assert rel_err(g2[n], g1[n].double().cpu().numpy()) <= 1e-2, n
 
 
-@pytest.mark.parametrize("variant", [2, 3, 4, 5])
+@pytest.mark.parametrize("variant", [2, 3, 4, 5, 6])
 def test_backward_mma_forced_timeout_is_reported(variant):
-    wl = Workload("to", 2, 20, 2, 64, 64, h0="uniform")
+    K, V = kv_of(variant)
+    wl = Workload("to", 2, 20, 2, K, V, h0="uniform")
     inp = make_inputs(wl, DEV, 3)
     _, _, Hs = pkg.m2rnn_forward_train(inp)
-    dy, dHT = upstream(2, 20, 2, 64, 64, 4)
+    dy, dHT = upstream(2, 20, 2, K, V, 4)
     pkg.m2rnn_backward(inp, Hs, dy, dHT, variant=variant | (1 << 8))
     assert pkg.stream_status() == binding.ERR_TIMEOUT
     assert pkg.stream_status() == binding.OK
@@ -225,8 +240,9 @@ def abs_err(got, want):
     # the training workload's length and head shape on the tensor-core backward (auto = 5)
     ((1, 16384, 4, 64, 64), False, 0),
     ((1, 16384, 4, 64, 64), True, 0),
-    # V = 128 at a long T on the SIMT backward (the kernel that differentiates V = 128)
+    # V = 128 at long T on its tensor-core backward (auto = 6), per-head and shared q, k
     ((1, 4096, 2, 64, 128), False, 0),
+    ((1, 2048, 2, 128, 128), True, 0),
 ])
 def test_backward_bf16_at_training_length(shape, shared, variant):
     """Every gradient tensor against the fp64 backward oracle over the whole sequence:
