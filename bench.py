@@ -47,6 +47,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--batch", type=int, default=None,
                     help="override B of the workload (smaller cases for profiling)")
+    ap.add_argument("--seq", type=int, default=None,
+                    help="override T of the workload (smaller cases for profiling)")
     ap.add_argument("--pass", dest="which", default="forward",
                     choices=["forward", "train", "decode", "block"],
                     help="forward: the forward pass (default); train: the state-keeping "
@@ -1023,6 +1025,8 @@ def main():
     wl = WORKLOADS[args.workload or HEADLINE]
     if args.batch:
         wl = wl.with_(B=args.batch, name=f"{wl.name}_b{args.batch}")
+    if args.seq:
+        wl = wl.with_(T=args.seq, name=f"{wl.name}_t{args.seq}")
     if args.impl == "reference":
         return reference_arm(args, wl)
     if args.which == "train":

@@ -7,27 +7,32 @@
 //   R_t = C_t + q_t u_t^T,  D_t = ((1 - f_t) R_t) ⊙ (1 - Z_t^2),
 //   C_{t-1} = f_t R_t + D_t W^T,  dW += S_{t-1}^T D_t,  dL/df_t = <R_t, S_{t-1} - Z_t>,
 //   dk_t = D_t v_t,  dv_t = D_t^T k_t + w_r ⊙ u_t,  dq_t = S_t u_t.
-// One thread block per (batch, head) pair, 256 threads: thread (row i = 32 (warp & 3) + lane,
-// column half warp >> 2) keeps its 64 entries of f R in fp32 registers and does the step's
-// elementwise work; thread 0 issues the TMA loads and the tensor-core products.  Rows are
-// padded to 128 (state rows K .. 127 stay zero, so they add nothing anywhere).
+// One thread block per (batch, head) pair.  Eight compute warps (256 threads): thread (row
+// i = 32 (warp & 3) + lane, column half warp >> 2) keeps its 64 entries of f R in fp32 registers
+// and does the step's elementwise work.  A ninth warp issues the tensor-core products and the
+// TMA loads of the kept states, so that the compute warps never wait for an issue sequence.
+// Rows are padded to 128 (state rows K .. 127 stay zero, so they add nothing anywhere).
 //
-// Products of one step, issued together after the block has written the bf16 D_t tile (128-byte
-// swizzle, K-major) and committed to one mbarrier, in this order:
+// Products of one step, issued once the compute warps have written the bf16 D_t tile (128-byte
+// swizzle, K-major; two tiles, by t & 1) and signalled, in two commits:
 //   G_t = D_t W^T            (A = D K-major, B = the W^T tile read N-major; M = N = 128)
+//   P_{t-1} = S_{t-2} W + k_{t-1} v_{t-1}^T   (8 K = 16 steps, then the rank-1 step whose A
+//                                               column 0 is k and B column 0 is v)
+//   -- first commit: all that step t - 1 starts with --
 //   dW += S_{t-1}^T D_t      (A = the state tile read M-major, B = D read N-major; one
 //                             accumulator over the whole sequence)
 //   dk_t = D_t v_t, dv_t = D_t^T k_t   (N = 16 products whose B row 0 holds v_t / k_t)
 //   dq_{t-1} = S_{t-1} u_{t-1}         (B rows 0 and 1 hold the bf16 high and low parts of u,
 //                                       so u keeps fp32 accuracy)
-//   P_{t-1} = S_{t-2} W + k_{t-1} v_{t-1}^T   (8 K = 16 steps, then the rank-1 step whose A
-//                                               column 0 is k and B column 0 is v)
-// The next step waits for that one commit: G and P are then ready, and D, the small tiles and
-// the state slot of S_t are free again.  The state tiles (32 KB each) stream through a ring of
-// three slots, one TMA load per step, three steps ahead of their first use; the per-step
-// inputs (q, k, v, dy) are copied one step ahead with cp.async.  Every wait is bounded; a
-// timeout is decided jointly by the block (OR-reduction barrier), in-flight work gets a bounded
-// chance to finish, and the block releases tensor memory and exits.
+//   -- second commit --
+// Step t - 1 waits for the first commit, computes its elementwise part while the tensor core
+// runs the second group, then waits for the second commit: its outputs are read, and the
+// operand tiles it read are free again.  The state tiles (32 KB each) stream through a ring of
+// three slots, one TMA load per step, a step ahead of their first use; the per-step inputs
+// (q, k, v, dy) are copied a step ahead with cp.async into a ring of three buffers.  Every
+// wait is bounded and gives up early once another warp has raised the block's abort flag; a
+// timeout is decided jointly (OR-reduction barriers), in-flight work gets a bounded chance to
+// finish, and the block releases tensor memory and exits.
 #include <cuda_bf16.h>
 
 #include "m2rnn_internal.h"
@@ -38,7 +43,9 @@ namespace {
 
 constexpr int kV = 128;         // value width (the products are M = N = 128)
 constexpr int kR = 128;         // rows of the padded state
-constexpr int kThreads = 256;   // 8 warps: lane quadrant (warp & 3) x column half (warp >> 2)
+constexpr int kCompute = 256;   // 8 compute warps: lane quadrant (warp & 3) x column half (warp >> 2)
+constexpr int kThreads = kCompute + 32;  // + the issuer warp
+constexpr int kBarCompute = 1;  // named barrier of the compute warps
 constexpr int kTile = kR * kV * 2;         // one bf16 128 x 128 tile: [2 column halves][128][128 B]
 constexpr int kSmallTile = 16 * kV * 2;    // an N = 16 B operand: [2 K-blocks][16 rows][128 B]
 constexpr int kSlots = 3;                  // state ring
@@ -49,19 +56,19 @@ constexpr uint32_t kColP = 0, kColG = 128, kColW = 256, kColDk = 384, kColDv = 4
 
 // Shared memory layout (bytes from a 1024-aligned base).
 constexpr int kOffWt = 0;                          // W^T: row j, column l holds W[l][j]
-constexpr int kOffD = kOffWt + kTile;              // D_t (bf16), row i, column j
-constexpr int kOffS = kOffD + kTile;               // state slots [kSlots]
+constexpr int kOffD = kOffWt + kTile;              // D_t (bf16), row i, column j; [2] by t & 1
+constexpr int kOffS = kOffD + 2 * kTile;           // state slots [kSlots]
 constexpr int kOffBv = kOffS + kSlots * kTile;     // dk's B: row 0 = v_t
 constexpr int kOffBk = kOffBv + kSmallTile;        // dv's B: row 0 = k_t (K index = row i)
 constexpr int kOffBu = kOffBk + kSmallTile;        // dq's B: rows 0, 1 = bf16 hi, lo of u_{t-1}
 constexpr int kOffAx = kOffBu + kSmallTile;        // rank-1 A: [128 rows x 16] core matrices
 constexpr int kOffBx = kOffAx + 4096;              // rank-1 B: same layout
 constexpr int kInBytes = kV * 4 + kV * 2 + 2 * kR * 2;  // u (f32), v, q, k (bf16)
-constexpr int kOffIn = kOffBx + 4096;              // per-step inputs [2]
+constexpr int kOffIn = kOffBx + 4096;              // per-step inputs [3] by t % 3
 constexpr int kInU = 0, kInV = kV * 4, kInQ = kInV + kV * 2, kInK = kInQ + kR * 2;
-constexpr int kOffGate = kOffIn + 2 * kInBytes;    // float4 [2]: f, 1 - f, sigmoid(x), softplus(x)
-constexpr int kOffDf = kOffGate + 2 * 16;          // float [2][8]: dL/df partials per warp
-constexpr int kOffBar = kOffDf + 2 * 8 * 4;        // batch, state_full[kSlots], never; tmem slot
+constexpr int kOffGate = kOffIn + 3 * kInBytes;    // float4 [3]: f, 1 - f, sigmoid(x), softplus(x)
+constexpr int kOffDf = kOffGate + 3 * 16;          // float [2][8]: dL/df partials per warp
+constexpr int kOffBar = kOffDf + 2 * 8 * 4;        // gp, rest, dready, full[kSlots], never; abort; slot
 constexpr int kSmemBytes = kOffBar + 64 + 1024;    // + slack to align the base to 1024
 
 __device__ __forceinline__ uint32_t sw128_off(int r, int k, int rows) {
@@ -105,7 +112,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int qd = warp & 3, ch = warp >> 2;
+  const bool issuer = warp == kCompute / 32;
+  const int qd = warp & 3, ch = (warp >> 2) & 1;
   const int i = 32 * qd + lane;  // row of the state owned by this thread (and TMEM lane)
   const int c0 = 64 * ch;        // first of its 64 columns
   const int pair = blockIdx.x, b = pair / N, n = pair - (pair / N) * N;
@@ -123,15 +131,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sBx = smem + kOffBx;
   float4* gates = reinterpret_cast<float4*>(smem + kOffGate);
   float* dfpart = reinterpret_cast<float*>(smem + kOffDf);
-  uint64_t* batch = reinterpret_cast<uint64_t*>(smem + kOffBar);
-  uint64_t* sfull = batch + 1;  // [kSlots]
-  uint64_t* never = batch + 1 + kSlots;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(batch + 2 + kSlots);
+  uint64_t* gp_bar = reinterpret_cast<uint64_t*>(smem + kOffBar);  // G_t and P_{t-1} done
+  uint64_t* rest_bar = gp_bar + 1;  // the whole batch done (dW, dk, dv, dq too)
+  uint64_t* dready = gp_bar + 2;    // the compute warps' operands of a batch are written
+  uint64_t* sfull = gp_bar + 3;     // [kSlots]
+  uint64_t* never = gp_bar + 3 + kSlots;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gp_bar + 4 + kSlots);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gp_bar + 4 + kSlots) + 1;
   auto slot_of = [](int s) { return (s + 1) % kSlots; };  // state s >= -1
   auto state_tile = [&](int s) { return smem + kOffS + slot_of(s) * kTile; };
   // Parity of the load of state s into its slot (loads go in decreasing s).
   auto state_parity = [&](int s) { return (uint32_t)((T - 1 - s) / kSlots) & 1u; };
-  auto in_buf = [&](int t) { return smem + kOffIn + (t & 1) * kInBytes; };
+  auto in_buf = [&](int t) { return smem + kOffIn + (t % 3) * kInBytes; };
   const long long limit = kWaitLimitCycles;
 
   // Copies of step t's inputs into in_buf(t) (threads 0 .. 63); thread 64 loads a_t, whose
@@ -157,10 +168,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     cp_async_commit();
   };
   auto put_gate = [&](int t) {
-    if (tid == 64) gates[t & 1] = gate4(a_pref, al, be);
+    if (tid == 64) gates[t % 3] = gate4(a_pref, al, be);
   };
-  // Writes the bf16 of H_0 (or zeros) as state -1 (all threads; rows < K).
-  auto put_h0 = [&](uint8_t* tile) {
+  // The bf16 of H_0 (or zeros) as state -1 (compute threads, rows < K); thread 0 completes the
+  // slot's phase.
+  auto put_h0 = [&]() {
+    uint8_t* tile = state_tile(-1);
     if (i < K) {
       const float* hp = H0 ? H0 + ((size_t)pair * K + i) * kV + c0 : nullptr;
 #pragma unroll 4
@@ -174,29 +187,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     fence_proxy_async_smem();
+    if (tid == 0) mbar_arrive(&sfull[slot_of(-1)]);
   };
-  // Starts the load of state s >= -1 into its slot: TMA for s >= 0 (thread 0); the bf16 of
-  // H_0 for s = -1 (every thread writes its row; thread 0 completes the slot's phase).
+  // TMA of state s >= 0 into its slot (one lane).
   auto load_state = [&](int s) {
     uint64_t* bar = &sfull[slot_of(s)];
-    if (s >= 0) {
-      if (tid == 0) {
-        mbar_arrive_expect_tx(bar, (uint32_t)(2 * 64 * K * 2));
-        tma_load_4d(state_tile(s), &tm_h, bar, 0, 0, s, pair);
-        tma_load_4d(state_tile(s) + kR * 128, &tm_h, bar, 64, 0, s, pair);
-      }
-    } else {
-      put_h0(state_tile(s));
-      if (tid == 0) mbar_arrive(bar);
-    }
+    mbar_arrive_expect_tx(bar, (uint32_t)(2 * 64 * K * 2));
+    tma_load_4d(state_tile(s), &tm_h, bar, 0, 0, s, pair);
+    tma_load_4d(state_tile(s) + kR * 128, &tm_h, bar, 64, 0, s, pair);
   };
 
   // ---------------------------------------------------------------- set-up
   if (tid == 0) {
     prefetch_tensormap(&tm_h);
-    mbar_init(batch, 1);
+    mbar_init(gp_bar, 1);
+    mbar_init(rest_bar, 1);
+    mbar_init(dready, kCompute / 32);
     for (int s = 0; s < kSlots; ++s) mbar_init(&sfull[s], 1);
     mbar_init(never, 1);
+    *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 0) tmem_alloc(tmem_slot, kTmemCols);
@@ -210,307 +219,365 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int l = e >> 7, j = e & 127;
     *reinterpret_cast<uint16_t*>(sWt + sw128_off(j, l, kR)) = Wn[e];
   }
-  // The running f R of this thread's row: C_{T-1} = dH_T (or 0), no G yet.
-  float2 cf[32];
-  {
-    const float* gp = (dH_T && i < K) ? dH_T + ((size_t)pair * K + i) * kV + c0 : nullptr;
-#pragma unroll
-    for (int u = 0; u < 32; ++u)
-      cf[u] = gp ? *reinterpret_cast<const float2*>(gp + 2 * u) : make_float2(0.f, 0.f);
-  }
-  float dwr_acc = 0.f, dal_acc = 0.f, dbe_acc = 0.f;
-  const float wr_j = w_r[(size_t)n * kV + i];  // w_r of column j = i (column-half 1 threads)
-  __syncthreads();  // the zeroed slots before any load lands in them
-  for (int s = T - 1; s >= T - 3 && s >= -1; --s) load_state(s);
-  fetch_inputs(T - 1);
   fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t t_lane = tmem + ((uint32_t)(32 * qd) << 16);
 
   const uint32_t idesc_kk = umma_idesc_bf16(kR, kV, false);              // K-major A and B
   const uint32_t idesc_g = umma_idesc_bf16_ab(kR, kV, false, true);      // B read N-major
   const uint32_t idesc_w = umma_idesc_bf16_ab(kV, kV, true, true);       // both M/N-major
   const uint32_t idesc_s = umma_idesc_bf16(kR, 16, false);               // N = 16, A K-major
   const uint32_t idesc_sm = umma_idesc_bf16(kV, 16, true);               // N = 16, A M-major
-  auto dK = [&](const uint8_t* tile) { return umma_desc(smem_u32(tile), 16, 1024, 2); };
-  auto dMN = [&](const uint8_t* tile) { return umma_desc(smem_u32(tile), 16384, 1024, 2); };
-  // K-step kk (16 columns) of a K-major 128-column tile with `rows` rows, in 16-byte units.
-  auto koff = [](int kk, int rows) {
-    return (uint64_t)(((kk >> 2) * rows * 128 + (kk & 3) * 32) >> 4);
-  };
-  const uint64_t mnstep = 2048 >> 4;  // 16 rows of an M/N-major read
+  // Descriptor bases: a tile at byte offset `off` from the 1024-aligned base has the base's
+  // start-address field plus off / 16 (shared-memory offsets stay below 256 KB, so the 14-bit
+  // field does not overflow).  K-major tiles step 32 bytes per K = 16 inside a 64-column
+  // block (the next block is 16 KB on, 2 KB in a 16-row tile); M/N-major reads step 16 rows
+  // (2 KB).
+  const uint64_t kbase = umma_desc(smem_u32(smem), 16, 1024, 2);
+  const uint64_t mbase = umma_desc(smem_u32(smem), 16384, 1024, 2);
+  auto at = [](uint64_t base, int off) { return base + (uint64_t)(off >> 4); };
   const uint64_t dAx = umma_desc(smem_u32(sAx), 128, 256, 0);
   const uint64_t dBx = umma_desc(smem_u32(sBx), 128, 256, 0);
 
-  // Small operands of the batch issued at the end of step t (t = T means the first batch):
-  // rank-1 of step t - 1 (k, v), dq_{t-1}'s u rows, and for t < T dk_t's v and dv_t's k rows.
-  auto put_small = [&](int t) {
-    if (t - 1 >= 0) {
-      const uint8_t* in1 = in_buf(t - 1);
-      // Rank-1 A column 0 = k_{t-1} (rows < K), B column 0 = v_{t-1}: column-half 0 / 1.
-      if (ch == 0) {
-        const uint16_t kv = i < K ? reinterpret_cast<const uint16_t*>(in1 + kInK)[i] : 0;
-        *reinterpret_cast<uint16_t*>(sAx + core_off(i, 0)) = kv;
-      } else {
-        *reinterpret_cast<uint16_t*>(sBx + core_off(i, 0)) =
-            reinterpret_cast<const uint16_t*>(in1 + kInV)[i];
+  if (issuer) {
+    // ======================================================= issuer warp
+    // Batch t (t = T first: dq_{T-1} and P_{T-1} only) after the compute warps' signal.  The
+    // first three states load at once; then, before batch t, state t - 3 goes into the slot of
+    // state t, whose last readers were batch t + 1 and the compute warps' step t + 1, a batch
+    // ahead of its first use (batch t - 1).
+    const bool leader = lane == 0;
+    bool ok = true;
+    if (leader) {
+      for (int s = T - 1; s >= T - 3 && s >= 0; --s) load_state(s);
+    }
+    uint32_t dready_ph = 0, rest_ph = 0;
+    for (int t = T; t >= 0 && ok; --t) {
+      if (t < T && t - 3 >= 0) {
+        ok = __all_sync(0xffffffffu,
+                        wait_or_abort(rest_bar, rest_ph & 1u, limit, abort_flag));
+        ++rest_ph;
+        if (!ok) break;
+        if (leader) load_state(t - 3);
       }
-      // u_{t-1} as bf16 hi (row 0) and lo (row 1) parts; thread pairs cover the 128 columns.
-      if (tid < 64) {
-        const float2 x = reinterpret_cast<const float2*>(in1 + kInU)[tid];
-        const uint32_t hi = pack_bf16x2(x.x, x.y);
-        const float2 hf = bf16x2_to_float2(hi);
-        *reinterpret_cast<uint32_t*>(sBu + sw128_off(0, 2 * tid, 16)) = hi;
-        *reinterpret_cast<uint32_t*>(sBu + sw128_off(1, 2 * tid, 16)) =
-            pack_bf16x2(x.x - hf.x, x.y - hf.y);
+      bool w = wait_or_abort(dready, dready_ph & 1u, limit, abort_flag);
+      ++dready_ph;
+      if (t >= 1) w = w && wait_or_abort(&sfull[slot_of(t - 2)], state_parity(t - 2), limit,
+                                         abort_flag);
+      if (t >= 1) w = w && wait_or_abort(&sfull[slot_of(t - 1)], state_parity(t - 1), limit,
+                                         abort_flag);
+      if (t == T && (debug & kDebugForceTimeout))
+        w = w && mbar_wait_bounded(never, 0u, kDebugWaitLimitCycles);
+      ok = __all_sync(0xffffffffu, w);
+      if (!ok) break;
+      tc_fence_after();
+      const int doff = kOffD + (t & 1) * kTile;
+      const int s1 = kOffS + slot_of(t - 1) * kTile;
+      if (t < T) {  // G_t = D_t W^T
+        umma4_if<2, 128>(leader, tmem + kColG, at(kbase, doff), at(mbase, kOffWt), idesc_g, 0u);
+        umma4_if<2, 128>(leader, tmem + kColG, at(kbase, doff + 16384),
+                         at(mbase, kOffWt + 8192), idesc_g, 1u);
       }
-    }
-    if (t < T) {
-      const uint8_t* in0 = in_buf(t);
-      if (ch == 0) {  // dv's B row 0: k_t over the rows (K index = row i)
-        const uint16_t kv = i < K ? reinterpret_cast<const uint16_t*>(in0 + kInK)[i] : 0;
-        *reinterpret_cast<uint16_t*>(sBk + sw128_off(0, i, 16)) = kv;
-      } else {        // dk's B row 0: v_t over the columns
-        *reinterpret_cast<uint16_t*>(sBv + sw128_off(0, i, 16)) =
-            reinterpret_cast<const uint16_t*>(in0 + kInV)[i];
+      if (t >= 1) {  // P_{t-1} = S_{t-2} W + k_{t-1} v_{t-1}^T
+        const int s2 = kOffS + slot_of(t - 2) * kTile;
+        umma4_if<2, 2>(leader, tmem + kColP, at(kbase, s2), at(kbase, kOffWt), idesc_kk, 0u);
+        umma4_if<2, 2>(leader, tmem + kColP, at(kbase, s2 + 16384), at(kbase, kOffWt + 16384),
+                       idesc_kk, 1u);
+        umma_bf16_if(leader, tmem + kColP, dAx, dBx, idesc_kk, 1u);
       }
+      umma_commit_if(leader, gp_bar);
+      if (t < T) {
+        // dW += S_{t-1}^T D_t over the krows 16-row groups (both operands M/N-major).
+        const uint32_t acc0 = t < T - 1 ? 1u : 0u;
+        int kk = 0;
+        for (; kk + 4 <= krows; kk += 4)
+          umma4_if<128, 128>(leader, tmem + kColW, at(mbase, s1 + kk * 2048),
+                             at(mbase, doff + kk * 2048), idesc_w, kk == 0 ? acc0 : 1u);
+        for (; kk < krows; ++kk)
+          umma_bf16_if(leader, tmem + kColW, at(mbase, s1 + kk * 2048),
+                       at(mbase, doff + kk * 2048), idesc_w, kk == 0 ? acc0 : 1u);
+        // dk_t = D_t v_t
+        umma4_if<2, 2>(leader, tmem + kColDk, at(kbase, doff), at(kbase, kOffBv), idesc_s, 0u);
+        umma4_if<2, 2>(leader, tmem + kColDk, at(kbase, doff + 16384), at(kbase, kOffBv + 2048),
+                       idesc_s, 1u);
+        // dv_t = D_t^T k_t (A = D M-major over the row groups, B = k over the same rows)
+        kk = 0;
+        for (; kk + 4 <= krows; kk += 4)
+          umma4_if<128, 2>(leader, tmem + kColDv, at(mbase, doff + kk * 2048),
+                           at(kbase, kOffBk + (kk >> 2) * 2048), idesc_sm, kk == 0 ? 0u : 1u);
+        for (; kk < krows; ++kk)
+          umma_bf16_if(leader, tmem + kColDv, at(mbase, doff + kk * 2048),
+                       at(kbase, kOffBk + (kk >> 2) * 2048 + (kk & 3) * 32), idesc_sm,
+                       kk == 0 ? 0u : 1u);
+      }
+      if (t >= 1) {  // dq_{t-1} = S_{t-1} u_{t-1}
+        umma4_if<2, 2>(leader, tmem + kColDq, at(kbase, s1), at(kbase, kOffBu), idesc_s, 0u);
+        umma4_if<2, 2>(leader, tmem + kColDq, at(kbase, s1 + 16384), at(kbase, kOffBu + 2048),
+                       idesc_s, 1u);
+      }
+      umma_commit_if(leader, rest_bar);
     }
-    fence_proxy_async_smem();
-  };
-  // The batch of products issued at the end of step t (thread 0), see the file comment.
-  // t = T: only dq_{T-1} and P_{T-1}.
-  auto issue = [&](int t) {
-    tc_fence_after();
-    if (t < T) {
-      const uint8_t* sprev = state_tile(t - 1);
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk)  // G_t = D_t W^T
-        umma_bf16(tmem + kColG, dK(sD) + koff(kk, kR), dMN(sWt) + kk * mnstep, idesc_g, kk);
-      for (int kk = 0; kk < krows; ++kk)  // dW += S_{t-1}^T D_t
-        umma_bf16(tmem + kColW, dMN(sprev) + kk * mnstep, dMN(sD) + kk * mnstep, idesc_w,
-                  (t < T - 1 || kk > 0) ? 1u : 0u);
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk)  // dk_t = D_t v_t
-        umma_bf16(tmem + kColDk, dK(sD) + koff(kk, kR), dK(sBv) + koff(kk, 16), idesc_s, kk);
-      for (int kk = 0; kk < krows; ++kk)  // dv_t = D_t^T k_t
-        umma_bf16(tmem + kColDv, dMN(sD) + kk * mnstep, dK(sBk) + koff(kk, 16), idesc_sm, kk);
+    if (!ok && leader) {
+      *abort_flag = 1;
+      atomicExch(status, kStatusTimeout);
     }
-    if (t >= 1) {
-      const uint8_t* sprev = state_tile(t - 1);
-      const uint8_t* sprev2 = state_tile(t - 2);
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk)  // dq_{t-1} = S_{t-1} u_{t-1}
-        umma_bf16(tmem + kColDq, dK(sprev) + koff(kk, kR), dK(sBu) + koff(kk, 16), idesc_s, kk);
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk)  // P_{t-1} = S_{t-2} W + k_{t-1} v_{t-1}^T
-        umma_bf16(tmem + kColP, dK(sprev2) + koff(kk, kR), dK(sWt) + koff(kk, kR), idesc_kk,
-                  kk);
-      umma_bf16(tmem + kColP, dAx, dBx, idesc_kk, 1u);
-    }
-    umma_commit(batch);
-  };
-
-  // First batch: dq_{T-1} and P_{T-1} need S_{T-1}, S_{T-2} and step T-1's inputs.
-  bool ok = true;
-  if (tid == 0) {
-    ok = mbar_wait_bounded(&sfull[slot_of(T - 1)], state_parity(T - 1), limit);
-    ok = ok && mbar_wait_bounded(&sfull[slot_of(T - 2)], state_parity(T - 2), limit);
-    if (debug & kDebugForceTimeout) ok = ok && mbar_wait_bounded(never, 0u, kDebugWaitLimitCycles);
-  }
-  cp_async_wait_all();
-  __syncthreads();
-  put_small(T);
-  put_gate(T - 1);
-  tc_fence_before();
-  bool abort = __syncthreads_or(!ok);
-  if (!abort && tid == 0) issue(T);
-  uint32_t batch_ph = 0;
-  bool has_g = false;
-
-  for (int t = T - 1; t >= 0 && !abort; --t) {
-    // The previous batch: G_{t+1}, dW_{t+1}, dk_{t+1}, dv_{t+1}, dq_t, P_t.
-    ok = mbar_wait_bounded(batch, batch_ph & 1u, limit);
-    ++batch_ph;
-    const uint8_t* in0 = in_buf(t);
-    const float u1 = (ch == 1 && t + 1 < T)
-                         ? reinterpret_cast<const float*>(in_buf(t + 1) + kInU)[i] : 0.f;
-    // Joint decision; past this barrier nothing reads in_buf(t + 1) any more, so it takes step
-    // t - 1's inputs, and the slot state t has left takes state t - 3.
-    tc_fence_before();
-    abort = __syncthreads_or(!ok);
-    if (abort) break;
-    tc_fence_after();
-    if (t >= 1) fetch_inputs(t - 1);
-    if (t - 3 >= -1) load_state(t - 3);
-    // dq_t (column-half 0, rows < K); dk_{t+1} (column-half 0) and dv_{t+1} (column-half 1).
+  } else {
+    // ======================================================= compute warps
+    const uint32_t t_lane = tmem + ((uint32_t)(32 * qd) << 16);
+    // The running f R of this thread's row: C_{T-1} = dH_T (or 0), no G yet.
+    float2 cf[32];
     {
+      const float* gp = (dH_T && i < K) ? dH_T + ((size_t)pair * K + i) * kV + c0 : nullptr;
+#pragma unroll
+      for (int u = 0; u < 32; ++u)
+        cf[u] = gp ? *reinterpret_cast<const float2*>(gp + 2 * u) : make_float2(0.f, 0.f);
+    }
+    float dwr_acc = 0.f, dal_acc = 0.f, dbe_acc = 0.f;
+    const float wr_j = w_r[(size_t)n * kV + i];  // w_r of column j = i (column-half 1 threads)
+    // T <= 2: state -1's slot was never loaded; later it is written at step 2, once state 2
+    // has left it.
+    if (T <= 2) put_h0();
+    fetch_inputs(T - 1);
+
+    // Small operands of the batch issued after step t (t = T means the first batch): rank-1
+    // of step t - 1 (k, v), dq_{t-1}'s u rows, and for t < T dk_t's v and dv_t's k rows.
+    auto put_small = [&](int t) {
+      if (t - 1 >= 0) {
+        const uint8_t* in1 = in_buf(t - 1);
+        // Rank-1 A column 0 = k_{t-1} (rows < K), B column 0 = v_{t-1}: column-half 0 / 1.
+        if (ch == 0) {
+          const uint16_t kv = i < K ? reinterpret_cast<const uint16_t*>(in1 + kInK)[i] : 0;
+          *reinterpret_cast<uint16_t*>(sAx + core_off(i, 0)) = kv;
+        } else {
+          *reinterpret_cast<uint16_t*>(sBx + core_off(i, 0)) =
+              reinterpret_cast<const uint16_t*>(in1 + kInV)[i];
+        }
+        // u_{t-1} as bf16 hi (row 0) and lo (row 1) parts; thread pairs cover the 128 columns.
+        if (tid < 64) {
+          const float2 x = reinterpret_cast<const float2*>(in1 + kInU)[tid];
+          const uint32_t hi = pack_bf16x2(x.x, x.y);
+          const float2 hf = bf16x2_to_float2(hi);
+          *reinterpret_cast<uint32_t*>(sBu + sw128_off(0, 2 * tid, 16)) = hi;
+          *reinterpret_cast<uint32_t*>(sBu + sw128_off(1, 2 * tid, 16)) =
+              pack_bf16x2(x.x - hf.x, x.y - hf.y);
+        }
+      }
+      if (t < T) {
+        const uint8_t* in0 = in_buf(t);
+        if (ch == 0) {  // dv's B row 0: k_t over the rows (K index = row i)
+          const uint16_t kv = i < K ? reinterpret_cast<const uint16_t*>(in0 + kInK)[i] : 0;
+          *reinterpret_cast<uint16_t*>(sBk + sw128_off(0, i, 16)) = kv;
+        } else {        // dk's B row 0: v_t over the columns
+          *reinterpret_cast<uint16_t*>(sBv + sw128_off(0, i, 16)) =
+              reinterpret_cast<const uint16_t*>(in0 + kInV)[i];
+        }
+      }
+      fence_proxy_async_smem();
+    };
+    // Every compute warp has written its operands of the next batch: one arrive per warp.
+    auto signal = [&]() {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(dready);
+    };
+    // dq_t (column-half 0, rows < K) when t >= 0, dk_{t+1} (column-half 0) and dv_{t+1}
+    // (column-half 1) when t + 1 < T: the small products of the batch issued after step t + 1.
+    auto small_outputs = [&](int t) {
+      const int tn = t + 1;
       if (ch == 0) {
-        const float dq0 = tmem_ld1(t_lane + kColDq), dq1 = tmem_ld1(t_lane + kColDq + 1);
-        float dk1 = 0.f;
-        if (t + 1 < T) dk1 = tmem_ld1(t_lane + kColDk);
+        float dq0 = 0.f, dq1 = 0.f, dkn = 0.f;
+        if (t >= 0) {
+          dq0 = tmem_ld1(t_lane + kColDq);
+          dq1 = tmem_ld1(t_lane + kColDq + 1);
+        }
+        if (tn < T) dkn = tmem_ld1(t_lane + kColDk);
         if (i < K) {
-          const size_t r0 = ((size_t)b * T + t) * (shared_qk ? N : Nqk) + (shared_qk ? n : nq);
+          const int hs = shared_qk ? N : Nqk, hq = shared_qk ? n : nq;
           float* dqo = shared_qk ? dqk_heads : dq;
           float* dko = shared_qk ? dqk_heads + (size_t)gridDim.x * T * K : dk;
-          dqo[r0 * K + i] = dq0 + dq1;
-          if (t + 1 < T) dko[(r0 + (shared_qk ? N : Nqk)) * K + i] = dk1;
+          if (t >= 0) dqo[(((size_t)b * T + t) * hs + hq) * K + i] = dq0 + dq1;
+          if (tn < T) dko[(((size_t)b * T + tn) * hs + hq) * K + i] = dkn;
         }
-      } else if (t + 1 < T) {
-        const float dv1 = tmem_ld1(t_lane + kColDv);
-        dv[(((size_t)b * T + t + 1) * N + n) * kV + i] = fmaf(wr_j, u1, dv1);
+      } else if (tn < T) {
+        const float dvn = tmem_ld1(t_lane + kColDv);
+        const float un = reinterpret_cast<const float*>(in_buf(tn) + kInU)[i];
+        dv[(((size_t)b * T + tn) * N + n) * kV + i] = fmaf(wr_j, un, dvn);
       }
-    }
+    };
 
-    // ---- elementwise step t
-    const float4 gt = gates[t & 1];
-    const float2 ff = make_float2(gt.x, gt.x), gg = make_float2(gt.y, gt.y);
-    const float qi = i < K ? bf16_bits_to_float(reinterpret_cast<const uint16_t*>(in0 + kInQ)[i])
-                           : 0.f;
-    const float2 q2 = make_float2(qi, qi);
-    const float2* u2 = reinterpret_cast<const float2*>(in0 + kInU) + c0 / 2;
-    const uint8_t* sprev = state_tile(t - 1);
-    // The state tile S_{t-1} was waited for by thread 0 before P_t; every thread observes its
-    // load's completion before reading it.
-    ok = ok && mbar_wait_bounded(&sfull[slot_of(t - 1)], state_parity(t - 1), limit);
-    float2 dfp = make_float2(0.f, 0.f);
-#pragma unroll
-    for (int piece = 0; piece < 4; ++piece) {
-      float pv[16], gv[16];
-      tmem_ld16_nowait(t_lane + kColP + c0 + 16 * piece, pv);
-      if (has_g) tmem_ld16_nowait(t_lane + kColG + c0 + 16 * piece, gv);
-      const uint4 hp0 = *reinterpret_cast<const uint4*>(sprev + sw128_off(i, c0 + 16 * piece, kR));
-      const uint4 hp1 =
-          *reinterpret_cast<const uint4*>(sprev + sw128_off(i, c0 + 16 * piece + 8, kR));
-      tmem_wait_ld();
-      const uint32_t hw[8] = {hp0.x, hp0.y, hp0.z, hp0.w, hp1.x, hp1.y, hp1.z, hp1.w};
-      uint32_t dpk[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int u = 8 * piece + e;  // float2 index within the thread's 64 columns
-        const float2 z = make_float2(tanh_mufu(pv[2 * e]), tanh_mufu(pv[2 * e + 1]));
-        const float2 c = has_g ? add2(cf[u], make_float2(gv[2 * e], gv[2 * e + 1])) : cf[u];
-        const float2 r = fma2(q2, u2[u], c);                        // R = C + q u^T
-        const float2 om = fma2(make_float2(-z.x, -z.y), z, make_float2(1.f, 1.f));
-        const float2 d = mul2(mul2(gg, r), om);                     // D = (1 - f) R (1 - Z^2)
-        const float2 hpv = bf16x2_to_float2(hw[e]);
-        dfp = fma2(r, sub2(hpv, z), dfp);                           // <R, S_{t-1} - Z>
-        cf[u] = mul2(ff, r);                                        // f R, for C_{t-1}
-        dpk[e] = pack_bf16x2(d.x, d.y);
-      }
-      *reinterpret_cast<uint4*>(sD + sw128_off(i, c0 + 16 * piece, kR)) =
-          make_uint4(dpk[0], dpk[1], dpk[2], dpk[3]);
-      *reinterpret_cast<uint4*>(sD + sw128_off(i, c0 + 16 * piece + 8, kR)) =
-          make_uint4(dpk[4], dpk[5], dpk[6], dpk[7]);
-    }
-    has_g = true;
-    // dL/df_t partial of the warp; dw_r += u_t ⊙ v_t (column-half 1: column j = i).
-    float dsum = dfp.x + dfp.y;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, o);
-    if (lane == 0) dfpart[(t & 1) * 8 + warp] = dsum;
-    if (ch == 1)
-      dwr_acc = fmaf(reinterpret_cast<const float*>(in0 + kInU)[i],
-                     bf16_bits_to_float(reinterpret_cast<const uint16_t*>(in0 + kInV)[i]),
-                     dwr_acc);
-    // Step t - 1's inputs (for the rank-1 and u rows) and the small operand tiles.
+    // First batch's operands (step T - 1's inputs).
     cp_async_wait_all();
-    __syncthreads();
-    put_small(t);
-    if (t >= 1) put_gate(t - 1);
-    if (tid == 0 && t >= 1)
-      ok = ok && mbar_wait_bounded(&sfull[slot_of(t - 2)], state_parity(t - 2), limit);
-    fence_proxy_async_smem();
-    tc_fence_before();
-    abort = __syncthreads_or(!ok);
-    if (abort) break;
-    if (tid == 0) issue(t);
-    if (tid == 32) {  // da_t and the dalpha, dbeta sums
-      float df = 0.f;
-#pragma unroll
-      for (int w = 0; w < 8; ++w) df += dfpart[(t & 1) * 8 + w];
-      const float d_a = df * (-al * gt.x * gt.z);
-      da[((size_t)b * T + t) * N + n] = d_a;
-      dal_acc = fmaf(df, -gt.x * gt.w, dal_acc);
-      dbe_acc += d_a;
-    }
-  }
+    named_bar_sync(kBarCompute, kCompute);
+    put_small(T);
+    put_gate(T - 1);
+    signal();
 
-  if (!abort) {
-    // The last batch: G_0, dW_0, dk_0, dv_0.
-    const bool ok2 = mbar_wait_bounded(batch, batch_ph & 1u, limit);
-    tc_fence_before();
-    abort = __syncthreads_or(!ok2);
-    tc_fence_after();
-    if (!abort) {
-      const uint8_t* in0 = in_buf(0);
-      if (ch == 0) {
-        const float dk0 = tmem_ld1(t_lane + kColDk);
-        if (i < K) {
-          const size_t r0 = ((size_t)b * T) * (shared_qk ? N : Nqk) + (shared_qk ? n : nq);
-          float* dko = shared_qk ? dqk_heads + (size_t)gridDim.x * T * K : dk;
-          dko[r0 * K + i] = dk0;
+    bool abort = false, has_g = false;
+    uint32_t gp_ph = 0, rest_ph = 0;
+    for (int t = T - 1; t >= 0; --t) {
+      // G_{t+1} and P_t (the first commit of the batch issued after step t + 1).
+      bool ok = wait_or_abort(gp_bar, gp_ph & 1u, limit, abort_flag);
+      ++gp_ph;
+      tc_fence_before();
+      abort = named_bar_or(kBarCompute, kCompute, !ok);
+      if (abort) break;
+      tc_fence_after();
+      if (t >= 1) fetch_inputs(t - 1);  // into the buffer step t + 2 used
+
+      // ---- elementwise step t
+      const uint8_t* in0 = in_buf(t);
+      const float4 gt = gates[t % 3];
+      // ff = f_t; ngg = -(1 - f_t), paired with Z^2 - 1 below (no negated operand)
+      const float2 ff = make_float2(gt.x, gt.x), ngg = make_float2(-gt.y, -gt.y);
+      const float qi =
+          i < K ? bf16_bits_to_float(reinterpret_cast<const uint16_t*>(in0 + kInQ)[i]) : 0.f;
+      const float2 q2 = make_float2(qi, qi);
+      const float2* u2 = reinterpret_cast<const float2*>(in0 + kInU) + c0 / 2;
+      const uint8_t* sprev = state_tile(t - 1);
+      uint8_t* dcur = sD + (t & 1) * kTile;
+      // Every thread observes the load of S_{t-1} before reading it.
+      ok = wait_or_abort(&sfull[slot_of(t - 1)], state_parity(t - 1), limit, abort_flag);
+      float2 dfp = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int piece = 0; piece < 4; ++piece) {
+        float pv[16], gv[16];
+        tmem_ld16_nowait(t_lane + kColP + c0 + 16 * piece, pv);
+        if (has_g) tmem_ld16_nowait(t_lane + kColG + c0 + 16 * piece, gv);
+        const uint4 hp0 =
+            *reinterpret_cast<const uint4*>(sprev + sw128_off(i, c0 + 16 * piece, kR));
+        const uint4 hp1 =
+            *reinterpret_cast<const uint4*>(sprev + sw128_off(i, c0 + 16 * piece + 8, kR));
+        tmem_wait_ld();
+        const uint32_t hw[8] = {hp0.x, hp0.y, hp0.z, hp0.w, hp1.x, hp1.y, hp1.z, hp1.w};
+        uint32_t dpk[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int u = 8 * piece + e;  // float2 index within the thread's 64 columns
+          const float2 z = make_float2(tanh_mufu(pv[2 * e]), tanh_mufu(pv[2 * e + 1]));
+          const float2 c = has_g ? add2(cf[u], make_float2(gv[2 * e], gv[2 * e + 1])) : cf[u];
+          const float2 r = fma2(q2, u2[u], c);                        // R = C + q u^T
+          const float2 zz1 = fma2(z, z, make_float2(-1.f, -1.f));     // Z^2 - 1
+          const float2 d = mul2(mul2(ngg, r), zz1);                   // D = (1 - f) R (1 - Z^2)
+          const float2 hpv = bf16x2_to_float2(hw[e]);
+          dfp = fma2(r, sub2(hpv, z), dfp);                           // <R, S_{t-1} - Z>
+          cf[u] = mul2(ff, r);                                        // f R, for C_{t-1}
+          dpk[e] = pack_bf16x2(d.x, d.y);
         }
-      } else {
-        const float dv0 = tmem_ld1(t_lane + kColDv);
-        const float u0 = reinterpret_cast<const float*>(in0 + kInU)[i];
-        dv[(((size_t)b * T) * N + n) * kV + i] = fmaf(wr_j, u0, dv0);
+        *reinterpret_cast<uint4*>(dcur + sw128_off(i, c0 + 16 * piece, kR)) =
+            make_uint4(dpk[0], dpk[1], dpk[2], dpk[3]);
+        *reinterpret_cast<uint4*>(dcur + sw128_off(i, c0 + 16 * piece + 8, kR)) =
+            make_uint4(dpk[4], dpk[5], dpk[6], dpk[7]);
       }
-      // dH_0 = C_{-1} = f_0 R_0 + G_0.
-      if (dH0) {
-        float* hp = dH0 + ((size_t)pair * K + i) * kV + c0;
+      has_g = true;
+      // dL/df_t partial of the warp; dw_r += u_t ⊙ v_t (column-half 1: column j = i).
+      float dsum = dfp.x + dfp.y;
 #pragma unroll
-        for (int piece = 0; piece < 4; ++piece) {
-          float gv[16];
-          tmem_ld16_nowait(t_lane + kColG + c0 + 16 * piece, gv);
-          tmem_wait_ld();
-          if (i < K) {
+      for (int o = 16; o > 0; o >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, o);
+      if (lane == 0) dfpart[(t & 1) * 8 + warp] = dsum;
+      if (ch == 1)
+        dwr_acc = fmaf(reinterpret_cast<const float*>(in0 + kInU)[i],
+                       bf16_bits_to_float(reinterpret_cast<const uint16_t*>(in0 + kInV)[i]),
+                       dwr_acc);
+
+      // The second commit of the batch issued after step t + 1 (dW_{t+1}, dk_{t+1}, dv_{t+1},
+      // dq_t): its outputs, and the operand tiles it read are free again.
+      ok = wait_or_abort(rest_bar, rest_ph & 1u, limit, abort_flag) && ok;
+      ++rest_ph;
+      cp_async_wait_all();  // step t - 1's inputs
+      tc_fence_before();
+      abort = named_bar_or(kBarCompute, kCompute, !ok);
+      if (abort) break;
+      tc_fence_after();
+      small_outputs(t);
+      put_small(t);
+      if (t >= 1) put_gate(t - 1);
+      if (t == 2) put_h0();  // state 2's slot is free: state -1 for batches 1 and 0
+      signal();
+      if (tid == 32) {  // da_t and the dalpha, dbeta sums
+        float df = 0.f;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const int u = 8 * piece + e;
-              *reinterpret_cast<float2*>(hp + 2 * u) =
-                  add2(cf[u], make_float2(gv[2 * e], gv[2 * e + 1]));
+        for (int w = 0; w < 8; ++w) df += dfpart[(t & 1) * 8 + w];
+        const float d_a = df * (-al * gt.x * gt.z);
+        da[((size_t)b * T + t) * N + n] = d_a;
+        dal_acc = fmaf(df, -gt.x * gt.w, dal_acc);
+        dbe_acc += d_a;
+      }
+    }
+
+    if (!abort) {
+      // The last batch: G_0, then dW_0, dk_0, dv_0.
+      bool ok2 = wait_or_abort(gp_bar, gp_ph & 1u, limit, abort_flag);
+      ok2 = wait_or_abort(rest_bar, rest_ph & 1u, limit, abort_flag) && ok2;
+      tc_fence_before();
+      abort = named_bar_or(kBarCompute, kCompute, !ok2);
+      tc_fence_after();
+      if (!abort) {
+        small_outputs(-1);
+        // dH_0 = C_{-1} = f_0 R_0 + G_0.
+        if (dH0) {
+          float* hp = dH0 + ((size_t)pair * K + i) * kV + c0;
+#pragma unroll
+          for (int piece = 0; piece < 4; ++piece) {
+            float gv[16];
+            tmem_ld16_nowait(t_lane + kColG + c0 + 16 * piece, gv);
+            tmem_wait_ld();
+            if (i < K) {
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                const int u = 8 * piece + e;
+                *reinterpret_cast<float2*>(hp + 2 * u) =
+                    add2(cf[u], make_float2(gv[2 * e], gv[2 * e + 1]));
+              }
             }
           }
         }
-      }
-      // This pair's dW (TMEM lane j, columns j'), dw_r, dalpha and dbeta partials.
-      float* wsp = ws + (size_t)pair * backward_pair_floats(K, kV);
-      float* dWp = wsp + (size_t)K * kV;
-      float* dwr_p = dWp + kV * kV;
-      float* ab_p = dwr_p + kV;
+        // This pair's dW (TMEM lane j, columns j'), dw_r, dalpha and dbeta partials.
+        float* wsp = ws + (size_t)pair * backward_pair_floats(K, kV);
+        float* dWp = wsp + (size_t)K * kV;
+        float* dwr_p = dWp + kV * kV;
+        float* ab_p = dwr_p + kV;
 #pragma unroll
-      for (int piece = 0; piece < 4; ++piece) {
-        float wv[16];
-        tmem_ld16_nowait(t_lane + kColW + c0 + 16 * piece, wv);
-        tmem_wait_ld();
+        for (int piece = 0; piece < 4; ++piece) {
+          float wv[16];
+          tmem_ld16_nowait(t_lane + kColW + c0 + 16 * piece, wv);
+          tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 16; e += 4)
-          *reinterpret_cast<float4*>(dWp + (size_t)i * kV + c0 + 16 * piece + e) =
-              make_float4(wv[e], wv[e + 1], wv[e + 2], wv[e + 3]);
-      }
-      if (ch == 1) dwr_p[i] = dwr_acc;
-      if (tid == 32) {
-        ab_p[0] = dal_acc;
-        ab_p[1] = dbe_acc;
+          for (int e = 0; e < 16; e += 4)
+            *reinterpret_cast<float4*>(dWp + (size_t)i * kV + c0 + 16 * piece + e) =
+                make_float4(wv[e], wv[e + 1], wv[e + 2], wv[e + 3]);
+        }
+        if (ch == 1) dwr_p[i] = dwr_acc;
+        if (tid == 32) {
+          ab_p[0] = dal_acc;
+          ab_p[1] = dbe_acc;
+        }
       }
     }
+    if (abort && tid == 0) {
+      *abort_flag = 1;
+      atomicExch(status, kStatusTimeout);
+    }
+    cp_async_wait_all();
   }
-  if (abort && tid == 0) {
-    atomicExch(status, kStatusTimeout);
-    // Give a tensor-core batch or TMA copy still in flight a bounded chance to finish.
-    mbar_wait_bounded(batch, 0u, kDebugWaitLimitCycles);
-    mbar_wait_bounded(batch, 1u, kDebugWaitLimitCycles);
+
+  // Before tensor memory is released every issued product and TMA load must be done: wait
+  // (bounded) for the last phase of each barrier that may still complete.
+  tc_fence_before();
+  __syncthreads();
+  if (tid == 0 && *abort_flag) {
+    mbar_wait_bounded(gp_bar, 0u, kDebugWaitLimitCycles);
+    mbar_wait_bounded(gp_bar, 1u, kDebugWaitLimitCycles);
+    mbar_wait_bounded(rest_bar, 0u, kDebugWaitLimitCycles);
+    mbar_wait_bounded(rest_bar, 1u, kDebugWaitLimitCycles);
     for (int s = 0; s < kSlots; ++s) {
       mbar_wait_bounded(&sfull[s], 0u, kDebugWaitLimitCycles);
       mbar_wait_bounded(&sfull[s], 1u, kDebugWaitLimitCycles);
     }
   }
-  cp_async_wait_all();
   tc_fence_before();
   __syncthreads();
+  tc_fence_after();
   if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
