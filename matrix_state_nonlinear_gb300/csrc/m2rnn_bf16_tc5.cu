@@ -41,6 +41,7 @@
 // not every block were resident at once, and a wait that still runs out is reported as a
 // timeout, never a hang.
 #include <atomic>
+#include <cstring>
 
 #include <cuda_bf16.h>
 
@@ -95,10 +96,15 @@ __device__ __forceinline__ unsigned long long ld_acquire_gpu(const unsigned long
 }
 
 // kBalanced = false: block b runs pair b whole (the stretch logic folds away).
-template <bool kBalanced>
+// kCache: also keep every state, the bf16 A tile of H_t exactly as the next step's product
+// reads it, by one TMA tensor store per step into Hs [B N, T, K, V] (the training forward).
+// The store must have read the tile before the next step rewrites it: thread 0 waits for
+// that, and the block meets once more per step.
+template <bool kBalanced, bool kCache>
 __global__ void __launch_bounds__(kThreads, 2)
     fwd_bf16_tc5(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                 const __grid_constant__ CUtensorMap tm_v, const uint16_t* __restrict__ a,
+                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_h,
+                 const uint16_t* __restrict__ a,
                  const float* __restrict__ alpha, const float* __restrict__ beta,
                  const uint16_t* __restrict__ W, const float* __restrict__ w_r, const float* H0,
                  float* y, float* H_T, int T, int N, int qk_hs, long long pairs,
@@ -144,6 +150,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     prefetch_tensormap(&tm_q);
     prefetch_tensormap(&tm_k);
     prefetch_tensormap(&tm_v);
+    if (kCache) prefetch_tensormap(&tm_h);
     mbar_init(mma_bar, 1);
     mbar_init(&full[0], 1);
     mbar_init(&full[1], 1);
@@ -312,6 +319,11 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       ok = mbar_wait_bounded(mma_bar, mma_ph & 1u, kWaitLimitCycles);
       ++mma_ph;
+      if (kCache && t > t0) {
+        // The A tile is rewritten below: the store of H_{t-1} must have read it.
+        if (tid == 0) bulk_wait_group_read<0>();
+        __syncthreads();
+      }
       tc_fence_after();
       const float2 fg = fgs[st * kTc + s];
       const float2 ff = make_float2(fg.x, fg.x), gg = make_float2(fg.y, fg.y);
@@ -361,7 +373,14 @@ __global__ void __launch_bounds__(kThreads, 2)
       fence_proxy_async_smem();
       tc_fence_before();
       abort = __syncthreads_or(!ok);
-      if (!abort && tid == 0) issue_mma(has_next, true);
+      if (!abort && tid == 0) {
+        issue_mma(has_next, true);
+        if (kCache) {  // H_t (bf16, the A tile) into Hs[pair][t]: two 64-column boxes
+          tma_store_4d_if(true, &tm_h, smem_u32(sA), 0, 0, t, (int)p);
+          tma_store_4d_if(true, &tm_h, smem_u32(sA) + 16384, 64, 0, t, (int)p);
+          bulk_commit_group();
+        }
+      }
     }
     if (abort) break;
 
@@ -393,6 +412,9 @@ __global__ void __launch_bounds__(kThreads, 2)
       for (int u = 0; u < 32; ++u) *reinterpret_cast<float2*>(hp + 2 * u) = h[u];
     }
     chunk_base += (uint32_t)nchunks;
+    // The next segment rewrites the A tile: the store of this segment's last state must
+    // have read it.
+    if (kCache && tid == 0) bulk_wait_group_read<0>();
     abort = __syncthreads_or(!ok2);
   }
 
@@ -410,6 +432,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
     }
   }
+  if (kCache && tid == 0) bulk_wait_group<0>();  // the kept states are written
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, kTmemCols);
@@ -432,40 +455,53 @@ bool tc5_supports(int K, int V) { return K == kD && V == kD; }
 
 cudaError_t launch_fwd_bf16_tc5(const Problem& p, EncodeTiledFn enc, cudaStream_t stream,
                                bool balanced) {
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mh;
   if (!make_map_tc5(enc, &mq, p.q, p.Nqk, p.T, p.B) ||
       !make_map_tc5(enc, &mk, p.k, p.Nqk, p.T, p.B) ||
       !make_map_tc5(enc, &mv, p.v, p.N, p.T, p.B))
     return cudaErrorInvalidValue;
-  cudaError_t err = cudaFuncSetAttribute(fwd_bf16_tc5<false>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-  if (err == cudaSuccess)
-    err = cudaFuncSetAttribute(fwd_bf16_tc5<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               kSmemBytes);
-  if (err != cudaSuccess) return err;
+  const bool cache = p.Hs != nullptr;
+  std::memset(&mh, 0, sizeof(mh));
+  if (cache) {
+    // Kept states [B N, T, K, V] bf16: a box of 64 columns x 128 rows of one step, with the
+    // 128-byte swizzle of the A tile.
+    const cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)kD, (cuuint64_t)p.T,
+                                (cuuint64_t)p.B * p.N};
+    const cuuint64_t strides[3] = {(cuuint64_t)kD * 2, (cuuint64_t)kD * kD * 2,
+                                   (cuuint64_t)kD * kD * 2 * p.T};
+    const cuuint32_t box[4] = {64u, (cuuint32_t)kD, 1u, 1u};
+    const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    if (enc(&mh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, p.Hs, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
   const long long pairs = (long long)p.B * p.N;
   const int qk_hs = p.Nqk == 1 ? 0 : 1;
   long long workers = pairs;
   if (balanced) {
     // Two blocks per SM: what the tensor memory (256 columns each) and shared memory allow.
     int dev = 0, sms = 0;
+    cudaError_t err;
     if ((err = cudaGetDevice(&dev)) != cudaSuccess ||
         (err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
       return err;
     workers = tc5_balanced_workers(pairs, 2LL * sms);
   }
-  if (workers >= pairs) {  // one block per pair
-    fwd_bf16_tc5<false><<<(unsigned)pairs, kThreads, kSmemBytes, stream>>>(
-        mq, mk, mv, (const uint16_t*)p.a, p.alpha, p.beta, (const uint16_t*)p.W, p.w_r, p.H0, p.y,
-        p.H_T, p.T, p.N, qk_hs, pairs, (long long)p.T, 0u, p.debug, p.status);
-    return cudaGetLastError();
-  }
+  const bool bal = workers < pairs;
   static std::atomic<uint32_t> epochs{0};
-  const uint32_t epoch = epochs.fetch_add(1, std::memory_order_relaxed) + 1;
-  fwd_bf16_tc5<true><<<(unsigned)workers, kThreads, kSmemBytes, stream>>>(
-      mq, mk, mv, (const uint16_t*)p.a, p.alpha, p.beta, (const uint16_t*)p.W, p.w_r, p.H0, p.y,
-      p.H_T, p.T, p.N, qk_hs, pairs, tc5_line_per_block(pairs, p.T, workers), epoch, p.debug,
-      p.status);
+  const uint32_t epoch = bal ? epochs.fetch_add(1, std::memory_order_relaxed) + 1 : 0u;
+  const long long line = bal ? tc5_line_per_block(pairs, p.T, workers) : (long long)p.T;
+  auto kern = bal ? (cache ? fwd_bf16_tc5<true, true> : fwd_bf16_tc5<true, false>)
+                  : (cache ? fwd_bf16_tc5<false, true> : fwd_bf16_tc5<false, false>);
+  cudaError_t err =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (err != cudaSuccess) return err;
+  // Balanced: one block per stretch (blocks numbered backwards over the stretches, see the
+  // kernel); otherwise one block per pair.
+  kern<<<(unsigned)workers, kThreads, kSmemBytes, stream>>>(
+      mq, mk, mv, mh, (const uint16_t*)p.a, p.alpha, p.beta, (const uint16_t*)p.W, p.w_r, p.H0,
+      p.y, p.H_T, p.T, p.N, qk_hs, pairs, line, epoch, p.debug, p.status);
   return cudaGetLastError();
 }
 

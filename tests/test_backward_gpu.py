@@ -103,11 +103,13 @@ def test_backward_without_dHT_and_without_dH0():
 
 def test_forward_train_keeps_states_and_matches_plain_forward():
     # The bf16 state-keeping forward runs the pipelined kernel's arithmetic (forward variant
-    # 2) for K, V <= 64 with K % 16 == 0 and the row-warp kernel's (variant 1) otherwise.
+    # 2) for K, V <= 64 with K % 16 == 0, the tcgen05 kernel's (variant 3, or its balanced
+    # form 7 above two pairs per SM) for K = V = 128, and the row-warp kernel's (variant 1)
+    # otherwise.
     for dtype, shape, fwd_variant in [("f32", (2, 37, 3, 8, 24), 0), ("bf16", (2, 150, 3, 64, 64), 2),
                                       ("bf16", (1, 70, 2, 32, 16), 2),
                                       ("bf16", (2, 45, 2, 64, 128), 1),
-                                      ("bf16", (1, 33, 2, 128, 128), 1),
+                                      ("bf16", (1, 33, 2, 128, 128), 3),   # tcgen05
                                       # ragged K and V off the power-of-two grid (row-warp)
                                       ("bf16", (2, 40, 2, 24, 48), 1),
                                       ("bf16", (1, 30, 1, 100, 112), 1),
@@ -122,6 +124,32 @@ def test_forward_train_keeps_states_and_matches_plain_forward():
         _, _, states = m2rnn_forward_inputs(all_f64(inp), return_states=True)
         err = float(np.abs(Hs.double().cpu().numpy() - np.moveaxis(states, 1, 2)).max())
         assert err <= TOL[dtype], err
+
+
+def test_forward_train_balanced_keeps_states():
+    """K = V = 128 with more pairs than two per SM: the state-keeping forward runs the balanced
+    schedule (pairs cut between blocks, the state handed over mid-sequence); its y and H_T are
+    the plain forward's bits, and the kept states of cut pairs, on both sides of the cut,
+    match the oracle's."""
+    B, T, N, K, V = 2, 300, 170, 128, 128
+    wl = Workload("trb", B, T, N, K, V, h0="uniform")
+    inp = make_inputs(wl, DEV, 12)
+    y, HT, Hs = pkg.m2rnn_forward_train(inp)
+    assert pkg.stream_status() == binding.OK
+    y3, HT3 = pkg.m2rnn_forward(inp, variant=3)
+    assert torch.equal(y, y3) and torch.equal(HT, HT3)
+    assert torch.equal(Hs[:, :, T - 1], HT.to(Hs.dtype))
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    workers = min(B * N, 2 * sms)
+    cut = [e // T for e in (binding.balanced_stretch(B * N, T, workers, w)[1]
+                            for w in range(workers)) if e % T]
+    assert cut
+    from matrix_state_nonlinear_gb300.inputs import slice_pair
+    for p in cut[:2]:
+        b, n = divmod(p, N)
+        _, _, states = m2rnn_forward_inputs(slice_pair(inp, b, n), return_states=True)
+        err = float(np.abs(Hs[b, n].double().cpu().numpy() - states[0, :, 0]).max())
+        assert err <= TOL["bf16"], (p, err)
 
 
 BF16_SHAPES = [(1, 1, 1, 16, 16), (2, 65, 3, 64, 64), (1, 130, 2, 32, 32), (2, 40, 2, 48, 16),
