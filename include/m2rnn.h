@@ -301,6 +301,31 @@ m2rnn_status m2rnn_gate_rmsnorm_bf16(const float* y, const uint16_t* g_pre, cons
                                      float eps, uint16_t* out, long long rows, int D,
                                      void* stream);
 
+/*
+ * The block prologue fused into the bf16 forward (the notes' Sec. 2.3, Eq. (14)-(16)): the
+ * recurrence of m2rnn_forward_bf16_qk on
+ *   q = SiLU(conv(xq)), k = SiLU(conv(xk)), v = SiLU(conv(xv)),
+ * each a causal depthwise conv of kernel 4 along t exactly as m2rnn_conv_silu_bf16 computes
+ * it (same fp32 operations, the result rounded to bf16), so y and H_T are bit-identical to
+ * m2rnn_conv_silu_bf16 on each projection followed by m2rnn_forward_bf16_qk.  The convolved
+ * q, k, v are never written to memory.
+ *   xq, xk  [B, T, Nqk, K] bf16, raw projections; conv taps wq, wk [Nqk*K][4] float32
+ *   xv      [B, T, N, V] bf16; taps wv [N*V][4]
+ *   bq, bk, bv: biases [Nqk*K] / [N*V] float32, or NULL for zero
+ * Other arguments and errors as m2rnn_forward_bf16_qk, plus INVALID_ARG for a null tap
+ * pointer (T > 0) or taps not 16-byte aligned.  Runs on the eight-row kernels, so it takes
+ * K in {32, 64} and V in {16, 32, 48, 64} (UNSUPPORTED otherwise).  It saves the memory and
+ * traffic of the convolved q, k, v but not time: on GB300 it runs slower than the separate
+ * prologue plus forward (6.49 ms against 0.37 + 4.26 ms at B=8, T=16384, N=16, K=V=64).
+ */
+m2rnn_status m2rnn_forward_conv_bf16(const uint16_t* xq, const uint16_t* xk, const uint16_t* xv,
+                                     const float* wq, const float* bq, const float* wk,
+                                     const float* bk, const float* wv, const float* bv,
+                                     const uint16_t* a, const float* alpha, const float* beta,
+                                     const uint16_t* W, const float* w_r, const float* H0,
+                                     float* y, float* H_T, int B, int T, int N, int Nqk, int K,
+                                     int V, void* stream);
+
 /* Name of a bf16 kernel variant (NULL for an unknown id).  Id 0 is "auto". */
 const char* m2rnn_variant_name(int variant);
 

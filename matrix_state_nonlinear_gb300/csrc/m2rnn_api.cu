@@ -283,6 +283,37 @@ m2rnn_status m2rnn_forward_bf16_qk(const uint16_t* q, const uint16_t* k, const u
   return err == cudaSuccess ? M2RNN_OK : M2RNN_ERR_CUDA;
 }
 
+m2rnn_status m2rnn_forward_conv_bf16(const uint16_t* xq, const uint16_t* xk, const uint16_t* xv,
+                                     const float* wq, const float* bq, const float* wk,
+                                     const float* bk, const float* wv, const float* bv,
+                                     const uint16_t* a, const float* alpha, const float* beta,
+                                     const uint16_t* W, const float* w_r, const float* H0,
+                                     float* y, float* H_T, int B, int T, int N, int Nqk, int K,
+                                     int V, void* stream) {
+  m2rnn_status st = common_checks(xq, xk, xv, a, alpha, beta, W, w_r, y, B, T, N, K, V);
+  if (st != M2RNN_OK) return st;
+  if (Nqk != 1 && Nqk != N) return M2RNN_ERR_INVALID_ARG;
+  if (T > 0 && (!wq || !wk || !wv)) return M2RNN_ERR_INVALID_ARG;
+  if (!mma_r8_supports(K, V)) return M2RNN_ERR_UNSUPPORTED;
+  if (!aligned(xq, 16) || !aligned(xk, 16) || !aligned(xv, 16) || !aligned(W, 16) ||
+      !aligned(y, 16) || !aligned(H0, 16) || !aligned(H_T, 16) || !aligned(a, 2) ||
+      !aligned(wq, 16) || !aligned(wk, 16) || !aligned(wv, 16))
+    return M2RNN_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (T == 0) return empty_sequence(H0, H_T, B, N, K, V, s);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return M2RNN_ERR_CUDA;
+  int* status = status_address(dev);
+  EncodeTiledFn enc = encode_fn();
+  if (!status || !enc) return M2RNN_ERR_CUDA;
+  Problem p{xq, xk, xv, a, alpha, beta, W, w_r, H0, y, H_T, B, T, N, K, V, Nqk, 0, status};
+  p.conv.wq = wq, p.conv.bq = bq, p.conv.wk = wk, p.conv.bk = bk, p.conv.wv = wv, p.conv.bv = bv;
+  const int base = pick((long long)B * N, K, V, sm_count());
+  const cudaError_t err = base == kMmaR8Cluster ? launch_fwd_bf16_mma_r8_cluster(p, enc, s)
+                                                : launch_fwd_bf16_mma_r8(p, enc, s);
+  return err == cudaSuccess ? M2RNN_OK : M2RNN_ERR_CUDA;
+}
+
 m2rnn_status m2rnn_forward_bf16_variant(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                                         const uint16_t* a, const float* alpha, const float* beta,
                                         const uint16_t* W, const float* w_r, const float* H0,

@@ -87,6 +87,9 @@ struct R8Layout {
                           //   columns, `xbuf` apart
   int fgr;                // float2 [2][G Tc] gates of two batches of G chunks
   int wr;                 // float [V]
+  int cw;                 // fused prologue: float [2K + V][4] conv taps, then [2K + V] biases
+  int halo;               //   bf16 [2][3][2K + V] last three raw rows of a chunk, by parity
+  int mid;                //   bf16 [3][2K + V] raw rows Tc/2 - 3 .. Tc/2 - 1 of the chunk
   int bar;                // uint64 full[3], pdone[2], ydone[2], cready, never, xready[2],
                           //   xfree[2]; int abort
   int total;
@@ -94,7 +97,7 @@ struct R8Layout {
 
 __host__ __device__ inline int r8_al128(int x) { return (x + 127) & ~127; }
 
-__host__ __device__ inline R8Layout r8_layout(int K, int V, int CS) {
+__host__ __device__ inline R8Layout r8_layout(int K, int V, int CS, bool conv = false) {
   constexpr int Tc = kR8Tc;
   R8Layout L;
   const int MT = V / 16;
@@ -112,25 +115,51 @@ __host__ __device__ inline R8Layout r8_layout(int K, int V, int CS) {
   L.xbuf = CS > 1 ? r8_al128(CS * Tc * (V / CS) * 4) : 0;
   L.fgr = L.xpart + 2 * L.xbuf;
   L.wr = L.fgr + r8_al128(2 * kR8GateChunks * Tc * 8);
-  L.bar = L.wr + r8_al128(V * 4);
+  const int C = 2 * K + V;
+  L.cw = L.wr + r8_al128(V * 4);
+  L.halo = L.cw + (conv ? r8_al128(C * 5 * 4) : 0);
+  L.mid = L.halo + (conv ? r8_al128(2 * 3 * C * 2) : 0);
+  L.bar = L.mid + (conv ? r8_al128(3 * C * 2) : 0);
   L.total = L.bar + 160;
   return L;
 }
 
-template <int MT, int CS>
+// The block prologue's causal depthwise conv (kernel 4) and SiLU, for one channel: the same
+// fp32 operations in the same order as the separate prologue kernel (m2rnn_block.cu), so the
+// fused forward's operands are those bits.
+__device__ __forceinline__ float r8_conv_silu(const float* tap, float bias, float x3, float x2,
+                                              float x1, float x0) {
+  float acc = bias;
+  acc = fmaf(tap[0], x3, acc);
+  acc = fmaf(tap[1], x2, acc);
+  acc = fmaf(tap[2], x1, acc);
+  acc = fmaf(tap[3], x0, acc);
+  return __fdividef(acc, 1.f + __expf(-acc));
+}
+__device__ __forceinline__ uint16_t r8_bf16_bits(float x) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+
+// kConv: the block prologue is fused in.  The TMA stages then hold the raw projections x_q,
+// x_k, x_v; the helpers put each chunk through the conv and SiLU (bf16 results: q and v back
+// into the stage in place, k and v also into the fp32 operand buffers) before the compute warps
+// read it.  Conv taps and biases come as [C][4] and [C] per tensor (C = heads x width).
+template <int MT, int CS, bool kConv>
 __global__ void __launch_bounds__(384, 1)
     fwd_bf16_r8(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const uint16_t* __restrict__ a,
                 const float* __restrict__ alpha, const float* __restrict__ beta,
                 const uint16_t* __restrict__ W, const float* __restrict__ w_r, const float* H0,
                 float* __restrict__ y, float* H_T, int T, int N, int K, int qk_hs, int debug,
-                int* status) {
+                int* status, const float* __restrict__ cw_q, const float* __restrict__ cb_q,
+                const float* __restrict__ cw_k, const float* __restrict__ cb_k,
+                const float* __restrict__ cw_v, const float* __restrict__ cb_v) {
   constexpr int V = 16 * MT;
   constexpr int VL = V / CS;  // y columns this block owns: rank VL .. rank VL + VL - 1
   constexpr int Tc = kR8Tc;
   constexpr int G = kR8GateChunks, GB = G * Tc;  // chunks and steps per gate batch
   extern __shared__ __align__(128) uint8_t smem[];
-  const R8Layout L = r8_layout(K, V, CS);
+  const R8Layout L = r8_layout(K, V, CS, kConv);
   const int wt = K / 8;       // compute warps of the pair
   const int nw = wt / CS;     // compute warps of this block; warps nw .. nw + 3 are the helpers
   const int rank = CS > 1 ? (int)cluster_ctarank() : 0;
@@ -172,6 +201,29 @@ __global__ void __launch_bounds__(384, 1)
     fence_mbar_init();
   }
   for (int j = tid; j < V; j += nthreads) wrs[j] = w_r[(size_t)n * V + j];
+  // Fused prologue: this pair's conv taps and biases (q, k channels of head n * qk_hs, v of
+  // head n) in channel order q, k, v; the halo of chunk 0 (steps -3 .. -1) is zero.
+  float* cws = reinterpret_cast<float*>(smem + L.cw);
+  uint16_t* halo = reinterpret_cast<uint16_t*>(smem + L.halo);
+  uint16_t* mid = reinterpret_cast<uint16_t*>(smem + L.mid);
+  const int CC = 2 * K + V;  // conv channels of the pair
+  if constexpr (kConv) {
+    for (int c = tid; c < CC; c += nthreads) {
+      const float* wsrc;
+      const float* bsrc;
+      int gc;
+      if (c < K) {
+        wsrc = cw_q, bsrc = cb_q, gc = n * qk_hs * K + c;
+      } else if (c < 2 * K) {
+        wsrc = cw_k, bsrc = cb_k, gc = n * qk_hs * K + c - K;
+      } else {
+        wsrc = cw_v, bsrc = cb_v, gc = n * V + c - 2 * K;
+      }
+      *reinterpret_cast<float4*>(cws + 4 * c) = *reinterpret_cast<const float4*>(wsrc + 4 * gc);
+      cws[4 * CC + c] = bsrc ? bsrc[gc] : 0.f;
+      for (int r = 0; r < 3; ++r) halo[r * CC + c] = 0;
+    }
+  }
   __syncthreads();
   if constexpr (CS > 1) cluster_sync_all();  // every block's barriers exist before remote arrives
 
@@ -254,6 +306,60 @@ __global__ void __launch_bounds__(384, 1)
       kf[2 * e] = make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
       kf[2 * e + 1] = make_float4(bf16_lo(u.z), bf16_hi(u.z), bf16_lo(u.w), bf16_hi(u.w));
     }
+  };
+  // Fused prologue for chunk cc (its TMA stage has landed): units (channel c of the 2K + V,
+  // half hf of the chunk's steps), participants i0, i0 + count, ...; `sync` is a barrier over
+  // the participants.  Phase A saves the raw rows other units still need (the first half's
+  // last three, for the second half; the chunk's last three, for the next chunk), phase B
+  // runs each unit's 16 steps in order with a three-step window, writing q and v back in
+  // place and k, v into the operand buffer cc & 1 as fp32.
+  auto convert_conv = [&](int cc, int i0, int count, auto sync) {
+    constexpr int kHalf = Tc / 2;
+    uint8_t* raw = smem + (cc % 3) * L.stage;
+    uint16_t* qs = reinterpret_cast<uint16_t*>(raw + L.qs);
+    uint16_t* ks = reinterpret_cast<uint16_t*>(raw + L.ks);
+    uint16_t* vs = reinterpret_cast<uint16_t*>(raw + L.vs);
+    const uint16_t* hal_in = halo + (cc & 1) * 3 * CC;
+    uint16_t* hal_out = halo + ((cc + 1) & 1) * 3 * CC;
+    uint8_t* cbase = smem + L.cb + (cc & 1) * L.cbuf;
+    float4* vd = reinterpret_cast<float4*>(cbase + L.vd);
+    float* kf = reinterpret_cast<float*>(cbase + L.kf);
+    auto xat = [&](int c, int r) -> uint16_t {  // raw row r of channel c in the stage
+      return c < K ? qs[r * K + c] : c < 2 * K ? ks[r * K + c - K] : vs[r * V + c - 2 * K];
+    };
+    for (int e = i0; e < 3 * CC; e += count) {
+      const int r = e / CC, c = e - r * CC;
+      mid[r * CC + c] = xat(c, kHalf - 3 + r);
+      hal_out[r * CC + c] = xat(c, Tc - 3 + r);
+    }
+    sync();
+    for (int e = i0; e < 2 * CC; e += count) {
+      const int hf = e / CC, c = e - hf * CC;
+      const uint16_t* win = hf == 0 ? hal_in : mid;
+      float x3 = bf16_bits_to_float(win[c]), x2 = bf16_bits_to_float(win[CC + c]),
+            x1 = bf16_bits_to_float(win[2 * CC + c]);
+      const float* tap = cws + 4 * c;
+      const float bias = cws[4 * CC + c];
+      for (int r = hf * kHalf; r < (hf + 1) * kHalf; ++r) {
+        const float x0 = bf16_bits_to_float(xat(c, r));
+        const uint16_t o = r8_bf16_bits(r8_conv_silu(tap, bias, x3, x2, x1, x0));
+        const float of = bf16_bits_to_float(o);
+        if (c < K) {
+          qs[r * K + c] = o;
+        } else if (c < 2 * K) {
+          kf[r * K + c - K] = of;
+        } else {
+          const int j = c - 2 * K;
+          vs[r * V + j] = o;
+          reinterpret_cast<float2*>(vd + (size_t)(r * 8 + (j & 7)) * MT + (j >> 4))[(j >> 3) & 1] =
+              make_float2(of, of);
+        }
+        x3 = x2;
+        x2 = x1;
+        x1 = x0;
+      }
+    }
+    sync();
   };
   // y of chunk cc (CS == 1): w_r ⊙ v plus the compute warps' partials in warp order, float4
   // rows; outputs i0, i0 + count, ...  The loop over warps is unrolled so that an output's
@@ -356,8 +462,14 @@ __global__ void __launch_bounds__(384, 1)
       if (tid == tma_tid) drain();
       if constexpr (CS == 1) return;  // (a cluster's blocks leave together, below)
     } else {
-      convert(0, tid, nthreads);
-      if (nchunks > 1) convert(1, tid, nthreads);
+      if constexpr (kConv) {
+        auto block_sync = [] { __syncthreads(); };
+        convert_conv(0, tid, nthreads, block_sync);
+        if (nchunks > 1) convert_conv(1, tid, nthreads, block_sync);
+      } else {
+        convert(0, tid, nthreads);
+        if (nchunks > 1) convert(1, tid, nthreads);
+      }
       gate(0, tid, a0);
     }
   }
@@ -393,7 +505,10 @@ __global__ void __launch_bounds__(384, 1)
         const int nc = cc + 2;  // into operand buffer cc & 1, which chunk cc has released
         ok = wait(&full[nc % 3], (uint32_t)(nc / 3) & 1u, false, true);
         if (named_bar_or(3, 32 * kR8Helpers, !ok)) break;
-        convert(nc, hid, 32 * kR8Helpers);
+        if constexpr (kConv)
+          convert_conv(nc, hid, 32 * kR8Helpers, [] { named_bar_sync(5, 32 * kR8Helpers); });
+        else
+          convert(nc, hid, 32 * kR8Helpers);
         if (nc % G == 0) {  // the gate batch that starts with chunk nc
           gate(nc / G, hid, a_nx);
           a_nx = load_a(nc / G + 1, hid);
@@ -636,16 +751,16 @@ bool make_map_r8(EncodeTiledFn enc, CUtensorMap* map, const void* base, int inne
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int MT, int CS>
+template <int MT, int CS, bool kConv>
 cudaError_t launch_r8(const Problem& p, EncodeTiledFn enc, cudaStream_t stream) {
   constexpr int V = 16 * MT;
-  const R8Layout L = r8_layout(p.K, V, CS);
+  const R8Layout L = r8_layout(p.K, V, CS, kConv);
   CUtensorMap mq, mk, mv;
   if (!make_map_r8(enc, &mq, p.q, p.K, p.Nqk, p.T, p.B, kR8Tc) ||
       !make_map_r8(enc, &mk, p.k, p.K, p.Nqk, p.T, p.B, kR8Tc) ||
       !make_map_r8(enc, &mv, p.v, V, p.N, p.T, p.B, kR8Tc))
     return cudaErrorInvalidValue;
-  auto kern = fwd_bf16_r8<MT, CS>;
+  auto kern = fwd_bf16_r8<MT, CS, kConv>;
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
   if (err != cudaSuccess) return err;
@@ -663,16 +778,17 @@ cudaError_t launch_r8(const Problem& p, EncodeTiledFn enc, cudaStream_t stream) 
   cfg.numAttrs = CS > 1 ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, (const uint16_t*)p.a, p.alpha, p.beta,
                             (const uint16_t*)p.W, p.w_r, p.H0, p.y, p.H_T, p.T, p.N, p.K,
-                            p.Nqk == 1 ? 0 : 1, p.debug, p.status);
+                            p.Nqk == 1 ? 0 : 1, p.debug, p.status, p.conv.wq, p.conv.bq,
+                            p.conv.wk, p.conv.bk, p.conv.wv, p.conv.bv);
 }
 
-template <int CS>
+template <int CS, bool kConv>
 cudaError_t launch_r8_cs(const Problem& p, EncodeTiledFn enc, cudaStream_t stream) {
   switch (p.V) {
-    case 16: return launch_r8<1, CS>(p, enc, stream);
-    case 32: return launch_r8<2, CS>(p, enc, stream);
-    case 48: return launch_r8<3, CS>(p, enc, stream);
-    case 64: return launch_r8<4, CS>(p, enc, stream);
+    case 16: return launch_r8<1, CS, kConv>(p, enc, stream);
+    case 32: return launch_r8<2, CS, kConv>(p, enc, stream);
+    case 48: return launch_r8<3, CS, kConv>(p, enc, stream);
+    case 64: return launch_r8<4, CS, kConv>(p, enc, stream);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -686,12 +802,12 @@ bool mma_r8_supports(int K, int V) {
 bool mma_r8_cluster_supports(int K, int V) { return K == 64 && mma_r8_supports(K, V); }
 
 cudaError_t launch_fwd_bf16_mma_r8(const Problem& p, EncodeTiledFn enc, cudaStream_t stream) {
-  return launch_r8_cs<1>(p, enc, stream);
+  return p.conv.wq ? launch_r8_cs<1, true>(p, enc, stream) : launch_r8_cs<1, false>(p, enc, stream);
 }
 
 cudaError_t launch_fwd_bf16_mma_r8_cluster(const Problem& p, EncodeTiledFn enc,
                                            cudaStream_t stream) {
-  return launch_r8_cs<2>(p, enc, stream);
+  return p.conv.wq ? launch_r8_cs<2, true>(p, enc, stream) : launch_r8_cs<2, false>(p, enc, stream);
 }
 
 }  // namespace m2rnn

@@ -43,6 +43,12 @@ struct Problem {
   int* status;      // device address of this device's status word
   void* Hs = nullptr;  // optional: every step's state [B, N, T, K, V] (fp32 path: float;
                       // bf16 path: the bf16-rounded state, uint16_t bits)
+  // Optional fused block prologue (eight-row kernels): q, k, v are then the raw projections
+  // and these the causal conv's taps [C][4] and biases [C] (biases may be null).
+  struct Conv {
+    const float *wq = nullptr, *bq = nullptr, *wk = nullptr, *bk = nullptr, *wv = nullptr,
+                *bv = nullptr;
+  } conv;
 };
 
 // Backward pass (reverse scan of the notes' Sec. 2.7).  Pointers as in the C ABI;

@@ -44,6 +44,7 @@ SYMBOLS = {
     "m2rnn_decode_step_bf16": (_I, [_P] * 11 + [_I] * 5 + [_P]),
     "m2rnn_decode_step_bf16_variant": (_I, [_P] * 11 + [_I] * 6 + [_P]),
     "m2rnn_conv_silu_bf16": (_I, [_P] * 4 + [_I] * 3 + [_P]),
+    "m2rnn_forward_conv_bf16": (_I, [_P] * 17 + [_I] * 6 + [_P]),
     "m2rnn_gate_rmsnorm_bf16": (_I, [_P] * 3 + [ctypes.c_float, _P, ctypes.c_longlong, _I, _P]),
 }
 
@@ -223,6 +224,31 @@ def m2rnn_forward(inputs: dict, y=None, H_T=None, variant=0, stream=None):
         return m2rnn_forward_f32(*args, inputs.get("H0"), y, H_T, stream=stream)
     return m2rnn_forward_bf16_variant(*args, inputs.get("H0"), y, H_T, variant=variant,
                                       stream=stream)
+
+
+def m2rnn_forward_conv(inputs: dict, conv: dict, y=None, H_T=None, stream=None):
+    """The block prologue fused into the bf16 forward: inputs["q"], ["k"], ["v"] are the raw
+    projections (bf16, shaped like q, k, v); conv holds the causal conv's taps "wq", "wk", "wv"
+    ([C, 4] float32, C = heads x width) and biases "bq", "bk", "bv" ([C] float32 or None).
+    Returns (y, H_T), the bits of conv_silu on each projection followed by m2rnn_forward."""
+    lib = load_library()
+    args = [inputs[x] for x in ("q", "k", "v", "a", "alpha", "beta", "W", "w_r")]
+    ptrs, (B, T, N, K, V), y, Nqk = _marshal(*args, inputs.get("H0"), y, H_T, torch.bfloat16)
+    if H_T is None:
+        H_T = torch.empty((B, N, K, V), dtype=torch.float32, device=y.device)
+        ptrs[10] = _ptr(H_T)
+    dev = y.device
+    taps = []
+    for name, C in (("q", Nqk * K), ("k", Nqk * K), ("v", N * V)):
+        w, b = conv["w" + name], conv.get("b" + name)
+        _check(w, "w" + name, torch.float32, (C, 4), dev)
+        _check(b, "b" + name, torch.float32, (C,), dev)
+        taps += [_ptr(w), _ptr(b)]
+    st = lib.m2rnn_forward_conv_bf16(*ptrs[:3], *taps, *ptrs[3:], B, T, N, Nqk, K, V,
+                                     ctypes.c_void_p(_stream_ptr(stream)))
+    if st != OK:
+        raise M2RNNError(st, "m2rnn_forward_conv_bf16")
+    return y, H_T
 
 
 # ---------------------------------------------------------------- training support

@@ -230,3 +230,22 @@ def test_block_argument_checks(lib):
     assert lib.m2rnn_gate_rmsnorm_bf16(q[0], q[1], q[2], 1e-6, q[3], 4, 12, None) == binding.ERR_UNSUPPORTED
     assert lib.m2rnn_gate_rmsnorm_bf16(q[0], q[1], q[2], -1.0, q[3], 4, 16, None) == binding.ERR_INVALID_ARG
     assert lib.m2rnn_gate_rmsnorm_bf16(q[0], None, q[2], 1e-6, q[3], 4, 16, None) == binding.ERR_INVALID_ARG
+
+
+def test_fused_prologue_argument_checks(lib):
+    p = fake_ptrs(17)
+    dims = (2, 8, 3, 3, 64, 64)   # B, T, N, Nqk, K, V
+    taps = p[3:9]
+    rest = p[9:]
+    assert lib.m2rnn_forward_conv_bf16(*p[:3], *taps, *rest, 2, 8, 3, 3, 128, 128, None) \
+        == binding.ERR_UNSUPPORTED                                   # not an eight-row shape
+    no_tap = list(taps)
+    no_tap[0] = None
+    assert lib.m2rnn_forward_conv_bf16(*p[:3], *no_tap, *rest, *dims, None) \
+        == binding.ERR_INVALID_ARG                                   # null q taps
+    assert lib.m2rnn_forward_conv_bf16(*p[:3], *taps, *rest, 2, 8, 3, 2, 64, 64, None) \
+        == binding.ERR_INVALID_ARG                                   # Nqk neither 1 nor N
+    bad = list(taps)
+    bad[2] = bad[2] + 4
+    assert lib.m2rnn_forward_conv_bf16(*p[:3], *bad, *rest, *dims, None) \
+        == binding.ERR_INVALID_ARG                                   # taps not 16-byte aligned

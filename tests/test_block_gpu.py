@@ -101,3 +101,75 @@ def test_block_chain_matches_oracle():
     ref = gate_rmsnorm(y.view(B, T, N * V).double().cpu().numpy(), gpre.double().cpu().numpy(),
                        wn.double().cpu().numpy(), 1e-6)
     assert close_bf16(out, ref) <= 0.0
+
+
+def fused_case(B, T, N, K, V, shared=False, with_bias=True, seed=0, scale=1.5, tap=0.6):
+    Nqk = 1 if shared else N
+    wl = Workload("fz", B, T, N, K, V, h0="uniform", shared_qk=shared)
+    inp = make_inputs(wl, DEV, seed)
+    pre = {"q": rand_bf16((B, T, Nqk * K), seed + 1, scale),
+           "k": rand_bf16((B, T, Nqk * K), seed + 2, scale),
+           "v": rand_bf16((B, T, N * V), seed + 3, scale)}
+    g = torch.Generator().manual_seed(seed + 4)
+    conv = {}
+    for n in ("q", "k", "v"):
+        C = pre[n].shape[2]
+        conv["w" + n] = (torch.randn((C, 4), generator=g) * tap).to(DEV)
+        conv["b" + n] = (torch.randn(C, generator=g) * 0.1).to(DEV) if with_bias else None
+    return inp, pre, conv, Nqk
+
+
+@pytest.mark.parametrize("B,T,N,K,V,shared", [
+    (2, 100, 3, 64, 64, False),   # ragged last chunk
+    (1, 33, 2, 32, 16, False),
+    (2, 2, 2, 64, 48, False),     # fewer steps than the conv window
+    (2, 70, 4, 64, 64, True),     # q, k shared by the heads
+    (8, 300, 16, 64, 64, False),  # 128 pairs: one block per pair
+    (4, 200, 8, 64, 32, False),   # 32 pairs: two-block clusters
+])
+@pytest.mark.parametrize("with_bias", [True, False])
+def test_fused_prologue_forward_is_bitwise_the_chain(B, T, N, K, V, shared, with_bias):
+    """m2rnn_forward_conv gives the bits of conv_silu on each projection followed by the
+    forward: the fused prologue runs the same fp32 operations and rounds to bf16 the same way."""
+    inp, pre, conv, Nqk = fused_case(B, T, N, K, V, shared, with_bias, seed=B + T + K + V)
+    run = dict(inp)
+    for n in ("q", "k", "v"):
+        run[n] = pkg.conv_silu(pre[n], conv["w" + n], conv["b" + n]).view(B, T, -1, V if n == "v" else K)
+    y_ref, HT_ref = pkg.m2rnn_forward(run)
+    fused_in = dict(inp)
+    for n in ("q", "k", "v"):
+        fused_in[n] = pre[n].view(B, T, -1, V if n == "v" else K)
+    y, HT = pkg.m2rnn_forward_conv(fused_in, conv)
+    assert pkg.stream_status() == binding.OK
+    assert torch.equal(y, y_ref) and torch.equal(HT, HT_ref)
+
+
+def test_fused_prologue_matches_oracle():
+    """Against the fp64 oracle (conv outputs rounded to bf16 as the GPU's are), with the
+    chained-block test's input scale (unit projections, taps of scale 0.5), at the
+    recurrence's bf16 bar."""
+    B, T, N, K, V = 2, 90, 3, 64, 64
+    inp, pre, conv, _ = fused_case(B, T, N, K, V, seed=7, scale=1.0, tap=0.5)
+    fused_in = dict(inp)
+    for n in ("q", "k", "v"):
+        fused_in[n] = pre[n].view(B, T, N, -1)
+    y, HT = pkg.m2rnn_forward_conv(fused_in, conv)
+    assert pkg.stream_status() == binding.OK
+    ref_in = all_f64(inp)
+    for n in ("q", "k", "v"):
+        c = conv_silu(pre[n].double().cpu().numpy(), conv["w" + n].double().cpu().numpy(),
+                      conv["b" + n].double().cpu().numpy())
+        ref_in[n] = torch.from_numpy(c).to(torch.bfloat16).double().numpy().reshape(B, T, N, -1)
+    yo, HTo = m2rnn_forward_inputs(ref_in)
+    assert float(np.abs(y.double().cpu().numpy() - yo).max()) <= 3e-2
+    assert float(np.abs(HT.double().cpu().numpy() - HTo).max()) <= 3e-2
+
+
+def test_fused_prologue_unsupported_shape():
+    inp, pre, conv, _ = fused_case(1, 10, 2, 128, 128, seed=3)
+    fused_in = dict(inp)
+    for n in ("q", "k", "v"):
+        fused_in[n] = pre[n].view(1, 10, 2, -1)
+    with pytest.raises(binding.M2RNNError) as e:
+        pkg.m2rnn_forward_conv(fused_in, conv)
+    assert e.value.status == binding.ERR_UNSUPPORTED
