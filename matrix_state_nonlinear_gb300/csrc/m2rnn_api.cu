@@ -358,7 +358,8 @@ m2rnn_status m2rnn_forward_train_bf16(const uint16_t* q, const uint16_t* k, cons
   if (T > 0 && !Hs) return M2RNN_ERR_INVALID_ARG;
   const bool pipe = mma_pipe_supports(K, V);
   const bool tc5 = tc5_supports(K, V);
-  if (!pipe && !tc5 && !mma_rowwarp_supports(K, V)) return M2RNN_ERR_UNSUPPORTED;
+  const bool cluster = mma_cluster_supports(K, V);
+  if (!pipe && !tc5 && !cluster && !mma_rowwarp_supports(K, V)) return M2RNN_ERR_UNSUPPORTED;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(W, 16) ||
       !aligned(y, 16) || !aligned(H0, 16) || !aligned(H_T, 16) || !aligned(Hs, 16) ||
       !aligned(a, 2))
@@ -372,11 +373,13 @@ m2rnn_status m2rnn_forward_train_bf16(const uint16_t* q, const uint16_t* k, cons
   if (!status || !enc) return M2RNN_ERR_CUDA;
   Problem p{q, k, v, a, alpha, beta, W, w_r, H0, y, H_T, B, T, N, K, V, Nqk, 0, status, Hs};
   // K, V <= 64: the pipelined kernel; K = V = 128: the tcgen05 kernel (balanced above two
-  // pairs per SM); other shapes (V = 128, K up to 128): the row-warp kernel.
+  // pairs per SM); K = 64, V = 128: the 4-CTA cluster kernel; other shapes (V = 128, K up to
+  // 128): the row-warp kernel.
   const cudaError_t err =
-      pipe  ? launch_fwd_bf16_mma_pipe(p, enc, s)
-      : tc5 ? launch_fwd_bf16_tc5(p, enc, s, (long long)B * N > 2LL * sm_count())
-            : launch_fwd_bf16_mma_rowwarp(p, enc, s);
+      pipe      ? launch_fwd_bf16_mma_pipe(p, enc, s)
+      : tc5     ? launch_fwd_bf16_tc5(p, enc, s, (long long)B * N > 2LL * sm_count())
+      : cluster ? launch_fwd_bf16_mma_cluster(p, enc, s)
+                : launch_fwd_bf16_mma_rowwarp(p, enc, s);
   return err == cudaSuccess ? M2RNN_OK : M2RNN_ERR_CUDA;
 }
 

@@ -22,6 +22,8 @@
 //     CTA c (the owner of column quarter c) through distributed shared memory.
 //     CTA c's producer warp adds the 4 row blocks' partials and w_r ⊙ v_t and
 //     stores its 32-column slice of y.
+// With kCache (the training forward) every warp also stores the bf16 H_t it packs each step
+// into the kept-state history Hs, so the backward reads exactly the product's operand.
 // Cross-CTA handoffs are mbarriers with remote release arrives and bounded acquire
 // waits: `ready` (a chunk's partials for my quarter arrived from all ranks) and
 // `free` (every owner has consumed the partials I sent, so the buffer can be reused).
@@ -75,6 +77,9 @@ __host__ __device__ inline ClusterLayout cluster_layout(int Tc) {
   return L;
 }
 
+// kCache: also keep every state H_t in Hs [B N, T, K, V] as bf16, the A fragments each warp
+// packs for the next step's product (streaming stores of its 16 rows x 32 columns).
+template <bool kCache>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_bf16_mma_cluster(const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k,
@@ -82,7 +87,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                          const uint16_t* __restrict__ a, const float* __restrict__ alpha,
                          const float* __restrict__ beta, const uint16_t* __restrict__ W,
                          const float* __restrict__ w_r, const float* H0, float* __restrict__ y,
-                         float* H_T, int T, int N, int Tc, int qk_hs, int debug, int* status) {
+                         float* H_T, uint16_t* __restrict__ Hs, int T, int N, int Tc, int qk_hs,
+                         int debug, int* status) {
   extern __shared__ __align__(128) uint8_t smem[];
   const ClusterLayout L = cluster_layout(Tc);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -233,7 +239,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // two k-tiles (columns 32 cq .. 32 cq + 31 of H), issue them, meet the other three
     // compute warps, then issue their six k-tiles.  `slot` alternates between calls;
     // prep(u) runs just before own k-tile u is packed (it brings h up to date).
-    auto hw_accumulate = [&](float2 (&nx)[4][2], int slot, auto&& prep) {
+    // `hs` (kCache): the kept state of this step, or null (the initial state is not kept).
+    auto hw_accumulate = [&](float2 (&nx)[4][2], int slot, uint16_t* hs, auto&& prep) {
       uint4* xslot = xbuf + (size_t)slot * kCompute * 2 * 32;
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
@@ -244,6 +251,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         af[2] = pack_bf16x2(h[2 * u + 1][0].x, h[2 * u + 1][0].y);
         af[3] = pack_bf16x2(h[2 * u + 1][1].x, h[2 * u + 1][1].y);
         xslot[(cq * 2 + u) * 32 + lane] = make_uint4(af[0], af[1], af[2], af[3]);
+        if (kCache && hs) {  // (row, column pair) of each fragment register
+          const int cl = col0 + 16 * u + 2 * c;
+          __stcs(reinterpret_cast<unsigned int*>(hs + (size_t)gr0 * kV + cl), af[0]);
+          __stcs(reinterpret_cast<unsigned int*>(hs + (size_t)gr1 * kV + cl), af[1]);
+          __stcs(reinterpret_cast<unsigned int*>(hs + (size_t)gr0 * kV + cl + 8), af[2]);
+          __stcs(reinterpret_cast<unsigned int*>(hs + (size_t)gr1 * kV + cl + 8), af[3]);
+        }
 #pragma unroll
         for (int j = 0; j < 4; ++j) mma2(nx[j], af, wbo[u][j][0], wbo[u][j][1]);
       }
@@ -279,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float2 acc[4][2], nxt[4][2];
     if (!aborted) {  // P_0 = k_0 v_0^T + H_0 W (exchange slot 1; step 0 uses slot 0)
       rank1(acc, smem, 0);
-      hw_accumulate(acc, 1, [](int) {});
+      hw_accumulate(acc, 1, nullptr, [](int) {});
     }
 
     // One time step t.  On entry `cur` = P_t (this quarter), h = H_{t-1}; on exit
@@ -295,7 +309,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       rank1(nx, nbase, sn);  // P_{t+1} starts as k_{t+1} v_{t+1}^T
       // Z_t = tanh(P_t), H_t = f H_{t-1} + (1 - f) Z_t (Eq. (10)-(11)), one own k-tile
       // (n-tiles 2u, 2u + 1) at a time, then P_{t+1} += H_t W.
-      hw_accumulate(nx, px, [&](int u) {
+      uint16_t* hs = kCache ? Hs + ((size_t)pair * T + (size_t)cc * Tc + s) * kK * kV : nullptr;
+      hw_accumulate(nx, px, hs, [&](int u) {
 #pragma unroll
         for (int j = 2 * u; j < 2 * u + 2; ++j)
 #pragma unroll
@@ -413,8 +428,9 @@ cudaError_t launch_fwd_bf16_mma_cluster(const Problem& p, EncodeTiledFn enc, cud
       !make_map_cluster(enc, &mk, p.k, kK, 16, p.Nqk, p.T, p.B, Tc) ||
       !make_map_cluster(enc, &mv, p.v, kV, kV, p.N, p.T, p.B, Tc))
     return cudaErrorInvalidValue;
-  cudaError_t err = cudaFuncSetAttribute(fwd_bf16_mma_cluster,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
+  auto kern = p.Hs ? fwd_bf16_mma_cluster<true> : fwd_bf16_mma_cluster<false>;
+  cudaError_t err =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)kR * (unsigned)p.B * (unsigned)p.N, 1, 1);
@@ -428,9 +444,10 @@ cudaError_t launch_fwd_bf16_mma_cluster(const Problem& p, EncodeTiledFn enc, cud
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, fwd_bf16_mma_cluster, mq, mk, mv, (const uint16_t*)p.a, p.alpha,
-                            p.beta, (const uint16_t*)p.W, p.w_r, p.H0, p.y, p.H_T, p.T, p.N, Tc,
-                            p.Nqk == 1 ? 0 : 1, p.debug, p.status);
+  return cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, (const uint16_t*)p.a, p.alpha, p.beta,
+                            (const uint16_t*)p.W, p.w_r, p.H0, p.y, p.H_T,
+                            static_cast<uint16_t*>(p.Hs), p.T, p.N, Tc, p.Nqk == 1 ? 0 : 1,
+                            p.debug, p.status);
 }
 
 }  // namespace m2rnn
