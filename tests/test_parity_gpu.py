@@ -368,3 +368,29 @@ def test_balanced_forced_timeout_with_cut_pairs():
     y3, H3 = run_gpu(inp, variant=3)
     y7, H7 = run_gpu(inp, variant=7)
     assert torch.equal(y7, y3) and torch.equal(H7, H3)
+
+
+@pytest.mark.parametrize("variant", [3, 7])
+def test_tcgen05_forward_cuda_graph_replay(variant):
+    """The K = V = 128 forward captured in a CUDA graph and replayed: every replay gives the
+    eager bits, also for the balanced schedule, whose handoff tags carry the epoch of the
+    captured launch (each replay's taking block overwrites them with y before the next)."""
+    wl = Workload("gr", 2, 300, 160, 128, 128, h0="uniform")
+    inp = make_inputs(wl, DEV, 31)
+    y_ref, HT_ref = run_gpu(inp, variant=variant)
+    y = torch.full_like(y_ref, float("nan"))
+    HT = torch.full_like(HT_ref, float("nan"))
+    pkg.m2rnn_forward(inp, y=y, H_T=HT, variant=variant)    # first call outside capture
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            pkg.m2rnn_forward(inp, y=y, H_T=HT, variant=variant, stream=s)
+    for _ in range(3):
+        y.fill_(float("nan"))
+        HT.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert pkg.stream_status() == binding.OK
+        assert torch.equal(y, y_ref) and torch.equal(HT, HT_ref)
