@@ -49,6 +49,8 @@ def parse():
                     help="override B of the workload (smaller cases for profiling)")
     ap.add_argument("--seq", type=int, default=None,
                     help="override T of the workload (smaller cases for profiling)")
+    ap.add_argument("--heads", type=int, default=None,
+                    help="override N of the workload (fewer pairs)")
     ap.add_argument("--pass", dest="which", default="forward",
                     choices=["forward", "train", "decode", "block"],
                     help="forward: the forward pass (default); train: the state-keeping "
@@ -70,6 +72,7 @@ KERNEL_SOURCES = {
     "tcgen05_k128_v128": ["m2rnn_bf16_tc5.cu"],
     "tcgen05_k128_v128_balanced": ["m2rnn_bf16_tc5.cu"],
     "mma_sync_cluster4_k64_v128": ["m2rnn_bf16_cluster.cu"],
+    "mma_sync_rows8_cluster8_k64_v128": ["m2rnn_bf16_c8.cu"],
     "mma_sync_rows8": ["m2rnn_bf16_r8.cu"],
     "mma_sync_rows8_cluster2": ["m2rnn_bf16_r8.cu"],
     "backward_mma_k64_v64": ["m2rnn_bwd_bf16_mma.cu"],
@@ -1083,6 +1086,8 @@ def main():
         wl = wl.with_(B=args.batch, name=f"{wl.name}_b{args.batch}")
     if args.seq:
         wl = wl.with_(T=args.seq, name=f"{wl.name}_t{args.seq}")
+    if args.heads:
+        wl = wl.with_(N=args.heads, name=f"{wl.name}_n{args.heads}")
     if args.impl == "reference":
         return reference_arm(args, wl)
     if args.which == "train":

@@ -73,8 +73,9 @@ m2rnn_status m2rnn_forward_f32(const float* q, const float* k, const float* v, c
  * bf16-operand / fp32-state path.  q, k, v, a and W are bfloat16 (passed as
  * their uint16_t bit patterns); alpha, beta, w_r, H0, y and H_T are float32.
  * The state H is carried in fp32 and rounded to bf16 only as the tensor-core
- * operand of each step's H W; the rank-1 term, tanh, gate lerp and readout are
- * fp32.  Supports any 1 <= K <= 128 and V a multiple of 16 with 16 <= V <= 128.
+ * operand of each step's H W; the rank-1 term, tanh and gate lerp are fp32, and
+ * the readout H_t^T q_t accumulates in fp32 (the eight-row kernels take it on the
+ * tensor cores from the same bf16 rounding of H_t that the next step's H W reads).  Supports any 1 <= K <= 128 and V a multiple of 16 with 16 <= V <= 128.
  * K that is not a multiple of 16 runs with its rows padded to the next multiple
  * of 16 inside the kernel (padding rows hold zero state, k and q, stay zero for
  * every t and are never stored), so the results are those of the K-row problem.

@@ -160,6 +160,12 @@ __host__ __device__ inline long long tc5_cut(long long c, long long total, int T
 // SMs, readout partials exchanged through distributed shared memory): K = 64, V = 128.
 bool mma_cluster_supports(int K, int V);
 cudaError_t launch_fwd_bf16_mma_cluster(const Problem& p, EncodeTiledFn enc, cudaStream_t stream);
+// The same shape with an 8-CTA cluster per pair (eight rows per CTA, product transposed,
+// each compute warp owning 32 value columns), K = 64, V = 128.  mma_c8_max_clusters: the
+// clusters of that kernel the current device runs at once (0 when it cannot say).
+bool mma_c8_supports(int K, int V);
+int mma_c8_max_clusters();
+cudaError_t launch_fwd_bf16_mma_c8(const Problem& p, EncodeTiledFn enc, cudaStream_t stream);
 
 // Tensor-core backward (warp-level MMA, TMA-staged bf16 states), K = V = 64, then the
 // reduction.  `debug` takes the kDebug* bits; `status` is the device status word.

@@ -68,7 +68,11 @@ def test_variant_support_table(lib):
     assert binding.variant_name(7) == "tcgen05_k128_v128_balanced"
     assert binding.variant_supports(4, 1, 8, 1, 64, 128)       # 4-CTA cluster: K = 64, V = 128
     assert not binding.variant_supports(4, 1, 8, 1, 64, 64)
-    assert binding.pick_variant(1, 65536, 16, 64, 128) == 4
+    assert binding.variant_supports(8, 1, 8, 1, 64, 128)       # 8-CTA cluster: K = 64, V = 128
+    assert not binding.variant_supports(8, 1, 8, 1, 128, 128)
+    assert binding.pick_variant(1, 65536, 15, 64, 128) == 8    # 15 clusters of 8 resident at once
+    assert binding.pick_variant(1, 65536, 16, 64, 128) == 4    # the 16th would wait: 4 SMs per pair
+    assert binding.pick_variant(8, 8192, 16, 64, 128) == 4
     assert binding.variant_name(2) is not None
 
 
