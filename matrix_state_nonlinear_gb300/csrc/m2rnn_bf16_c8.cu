@@ -47,6 +47,8 @@
 // operand.
 #include <cuda_bf16.h>
 
+#include <mutex>
+
 #include "m2rnn_internal.h"
 #include "ptx_util.cuh"
 
@@ -574,12 +576,14 @@ cudaError_t c8_prepare() {
 bool mma_c8_supports(int K, int V) { return K == kK && V == kV; }
 
 // Clusters of this kernel the current device runs at once (0 when it cannot say), cached per
-// device: the kernel pays only when every pair's cluster is resident.
+// device (under a mutex): the kernel pays only when every pair's cluster is resident.
 int mma_c8_max_clusters() {
   static int cache[64];
   static bool known[64];
+  static std::mutex mu;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::lock_guard<std::mutex> lock(mu);
   if (known[dev]) return cache[dev];
   int n = 0;
   cudaLaunchAttribute attr[1];
