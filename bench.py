@@ -1236,6 +1236,10 @@ def main():
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     mhz = clk.get("sm_mhz") or 1950.0
     roof["t_mufu_tanh_floor_ms"] = K * V * wl.units / (16.0 * sms * mhz * 1e6) * 1e3
+    # The FP32 ALU floor: about four FP32 operations per state element and step (the rank-1
+    # product, the gate lerp's multiply and fused multiply-add, the bf16 pack) at 128 lanes
+    # per clock per SM.
+    roof["t_fp32_alu_floor_ms"] = 4.0 * K * V * wl.units / (128.0 * sms * mhz * 1e6) * 1e3
     roof.update(serial_bound(pkg, inp, wl, args.variant, stream, dev, ms_per_step, mhz))
 
     cpu = None
