@@ -418,7 +418,9 @@ def reference_arm(args, wl):
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
-    per = max(2.0, min(args.cpu_seconds, 120.0 / max(1, args.steps + args.warmup)))
+    # Each step is a sample of about `per` seconds of oracle wall time, so that the whole run
+    # (warm-up included) stays near two minutes; the sizing below may overshoot by up to 2x.
+    per = max(0.25, min(args.cpu_seconds, 60.0 / max(1, args.steps + args.warmup)))
     vals = []
     pool = OraclePool()
     try:
@@ -432,7 +434,10 @@ def reference_arm(args, wl):
     value = statistics.median(vals)
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": None,
+        "steps": args.steps, "warmup": args.warmup,
+        # The oracle's rate on the sample, carried to the whole workload: the time one full
+        # step of this workload would take at that rate.
+        "ms_per_step": wl.units / value * 1e3, "ms_per_step_basis": "projected from the sample",
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": workload_config(wl),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
