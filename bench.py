@@ -73,6 +73,7 @@ KERNEL_SOURCES = {
     "tcgen05_k128_v128_balanced": ["m2rnn_bf16_tc5.cu"],
     "mma_sync_cluster4_k64_v128": ["m2rnn_bf16_cluster.cu"],
     "mma_sync_rows8_cluster8_k64_v128": ["m2rnn_bf16_c8.cu"],
+    "mma_sync_rows8_cluster4x2_k64_v128": ["m2rnn_bf16_c8.cu"],
     "mma_sync_rows8": ["m2rnn_bf16_r8.cu"],
     "mma_sync_rows8_cluster2": ["m2rnn_bf16_r8.cu"],
     "backward_mma_k64_v64": ["m2rnn_bwd_bf16_mma.cu"],

@@ -61,7 +61,8 @@ enum Variant : int {
   kMmaR8Cluster = 6,
   kTc5Balanced = 7,
   kMmaC8 = 8,
-  kNumVariants = 9
+  kMmaC4x2 = 9,
+  kNumVariants = 10
 };
 
 m2rnn_status common_checks(const void* q, const void* k, const void* v, const void* a,
@@ -113,12 +114,21 @@ int sm_count() {
   return sms;
 }
 
-// 8-CTA clusters of the K = 64, V = 128 kernel that the device runs at once: the occupancy
-// calculator's answer, or, without a device to ask, the count it gives on a 152-SM GB300
-// (15: its graphics processing clusters are of unequal size) scaled to the SM count.
-int c8_capacity(int sms) {
-  const int n = mma_c8_max_clusters();
-  return n > 0 ? n : sms * 15 / 152;
+// Clusters of R CTAs (R = 8 or 4) of the eight-SMs-per-pair K = 64, V = 128 kernel that the
+// device runs at once: the occupancy calculator's answer, or, without a device to ask, the
+// count it gives on a 152-SM GB300 (15 of eight: its graphics processing clusters are of
+// unequal size; 36 of four) scaled to the SM count.
+int c8_capacity(int R, int sms) {
+  const int n = mma_c8_max_clusters(R);
+  return n > 0 ? n : sms * (R == 8 ? 15 : 36) / 152;
+}
+// Eight SMs per pair for K = 64, V = 128, while every cluster of the launch is resident at
+// once: one 8-CTA cluster per pair (kMmaC8), else two 4-CTA clusters (kMmaC4x2); 0 when
+// neither fits (the 4-CTA kernel then runs, four SMs per pair).
+int c8_form(long long pairs, int sms) {
+  if (pairs <= c8_capacity(8, sms)) return kMmaC8;
+  if (2 * pairs <= c8_capacity(4, sms)) return kMmaC4x2;
+  return 0;
 }
 
 // The automatic variant: a function of the shape and of how many (batch, head) pairs there
@@ -128,7 +138,10 @@ int c8_capacity(int sms) {
 // at once, else four.
 int pick(long long pairs, int K, int V, int sms) {
   if (tc5_supports(K, V)) return pairs > 2LL * sms ? kTc5Balanced : kTc5;
-  if (mma_c8_supports(K, V) && pairs <= c8_capacity(sms)) return kMmaC8;
+  if (mma_c8_supports(K, V)) {
+    const int form = c8_form(pairs, sms);
+    if (form) return form;
+  }
   if (mma_cluster_supports(K, V)) return kMmaCluster;
   if (mma_r8_cluster_supports(K, V) && 2 * pairs <= sms) return kMmaR8Cluster;
   if (mma_r8_supports(K, V)) return kMmaR8;
@@ -146,7 +159,8 @@ bool supports(int variant, int K, int V) {
     case kMmaCluster: return mma_cluster_supports(K, V);
     case kMmaR8: return mma_r8_supports(K, V);
     case kMmaR8Cluster: return mma_r8_cluster_supports(K, V);
-    case kMmaC8: return mma_c8_supports(K, V);
+    case kMmaC8:
+    case kMmaC4x2: return mma_c8_supports(K, V);
   }
   return false;
 }
@@ -207,6 +221,7 @@ const char* m2rnn_variant_name(int variant) {
     case kMmaR8: return "mma_sync_rows8";
     case kMmaR8Cluster: return "mma_sync_rows8_cluster2";
     case kMmaC8: return "mma_sync_rows8_cluster8_k64_v128";
+    case kMmaC4x2: return "mma_sync_rows8_cluster4x2_k64_v128";
   }
   return nullptr;
 }
@@ -290,7 +305,8 @@ m2rnn_status m2rnn_forward_bf16_qk(const uint16_t* q, const uint16_t* k, const u
     case kTc5: err = launch_fwd_bf16_tc5(p, enc, s, false); break;
     case kTc5Balanced: err = launch_fwd_bf16_tc5(p, enc, s, true); break;
     case kMmaCluster: err = launch_fwd_bf16_mma_cluster(p, enc, s); break;
-    case kMmaC8: err = launch_fwd_bf16_mma_c8(p, enc, s); break;
+    case kMmaC8: err = launch_fwd_bf16_mma_c8(p, enc, s, 8); break;
+    case kMmaC4x2: err = launch_fwd_bf16_mma_c8(p, enc, s, 4); break;
     case kMmaR8: err = launch_fwd_bf16_mma_r8(p, enc, s); break;
     case kMmaR8Cluster: err = launch_fwd_bf16_mma_r8_cluster(p, enc, s); break;
   }
@@ -387,14 +403,15 @@ m2rnn_status m2rnn_forward_train_bf16(const uint16_t* q, const uint16_t* k, cons
   if (!status || !enc) return M2RNN_ERR_CUDA;
   Problem p{q, k, v, a, alpha, beta, W, w_r, H0, y, H_T, B, T, N, K, V, Nqk, 0, status, Hs};
   // K, V <= 64: the pipelined kernel; K = V = 128: the tcgen05 kernel (balanced above two
-  // pairs per SM); K = 64, V = 128: the 8-CTA cluster kernel while every pair's cluster is
-  // resident at once, else the 4-CTA one; other shapes (V = 128, K up to 128): the row-warp
-  // kernel.
-  const bool c8 = cluster && (long long)B * N <= c8_capacity(sm_count());
+  // pairs per SM); K = 64, V = 128: eight SMs per pair while every cluster is resident at once
+  // (one 8-CTA or two 4-CTA clusters per pair), else the 4-CTA kernel; other shapes (V = 128,
+  // K up to 128): the row-warp kernel.
+  const int form = cluster ? c8_form((long long)B * N, sm_count()) : 0;
+  const bool c8 = form != 0;
   const cudaError_t err =
       pipe      ? launch_fwd_bf16_mma_pipe(p, enc, s)
       : tc5     ? launch_fwd_bf16_tc5(p, enc, s, (long long)B * N > 2LL * sm_count())
-      : c8      ? launch_fwd_bf16_mma_c8(p, enc, s)
+      : c8      ? launch_fwd_bf16_mma_c8(p, enc, s, form == kMmaC8 ? 8 : 4)
       : cluster ? launch_fwd_bf16_mma_cluster(p, enc, s)
                 : launch_fwd_bf16_mma_rowwarp(p, enc, s);
   return err == cudaSuccess ? M2RNN_OK : M2RNN_ERR_CUDA;

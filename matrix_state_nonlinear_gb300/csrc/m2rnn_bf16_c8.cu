@@ -1,6 +1,9 @@
-// m2rnn_bf16_c8.cu — bf16-operand / fp32-state forward recurrence for K = 64, V = 128, one
-// 8-CTA thread-block cluster per (batch, head) pair: eight state rows per CTA, the step
-// product taken transposed on the warp-level tensor-core MMA (mma.sync).
+// m2rnn_bf16_c8.cu — bf16-operand / fp32-state forward recurrence for K = 64, V = 128 on eight
+// SMs per (batch, head) pair: eight state rows per CTA, the step product taken transposed on
+// the warp-level tensor-core MMA (mma.sync).  Two forms: one 8-CTA thread-block cluster per
+// pair (R = 8), or two independent 4-CTA clusters per pair (R = 4, rows 0..31 and 32..63),
+// which fit where eight-CTA clusters do not (a GB300 runs 15 clusters of eight at once, but
+// 36 of four).
 //
 // The recurrence is Eq. (10)-(12) with the gate of Eq. (13)/(17) of the M²RNN study notes
 // (Sec. 2.1-2.2):
@@ -20,6 +23,12 @@
 // Each step a warp finishes its own two column tiles (tanh, lerp, pack, transpose), writes
 // their B fragments into a double-buffered shared-memory slot and issues their MMAs, meets
 // the other compute warps at a named barrier, then issues the other six k-tiles.
+//
+// With R = 4, CTA r of cluster h owns rows 8 (4h + r) .. and y columns 32r .. 32r + 31 of its
+// half; each cluster sums its four row blocks and adds the sum into y (red.global.add) after
+// the launcher has zeroed y.  With two addends onto an exact zero the bits do not depend on
+// which cluster adds first (0 + a = a, a + b = b + a), so y stays deterministic; the two
+// clusters never wait for each other.
 //
 // Readout, two steps per MMA.  The untransposed bf16 pack of a column tile is half of an
 // m16n8k16 A fragment over the CTA's eight rows; with A = [H_t^T | H_{t+1}^T] (16 columns x
@@ -57,12 +66,10 @@ namespace {
 
 constexpr int kV = 128;
 constexpr int kK = 64;
-constexpr int kR = 8;             // CTAs per pair: CTA r owns rows 8r .. 8r + 7
 constexpr int kCW = 4;            // compute warps: warp w owns columns 32w .. 32w + 31
 constexpr int kThreads = 32 * (kCW + 1);
 constexpr int kBar = 1;           // named barrier of the compute warps
 constexpr int kTc = 32;           // steps per chunk
-constexpr int kOwn = kV / kR;     // y columns a CTA owns (16r .. 16r + 15)
 constexpr int kMinSmem = 120 * 1024;  // one CTA per SM
 
 struct C8Layout {
@@ -71,8 +78,8 @@ struct C8Layout {
   int kf;                 // float  [2][Tc][8]
   int fg;                 // float2 [2][Tc] (f, 1 - f)
   int xbuf;               // uint4  [2][kCW][32] B fragments of each warp's two k-tiles
-  int ypart;              // float2 [2][kR][Tc / 2][kOwn] partials for my columns, (t, t+1)
-  int wr;                 // float  [kOwn]
+  int ypart;              // float2 [2][R][Tc / 2][V / R] partials for my columns, (t, t+1)
+  int wr;                 // float  [V / R]
   int bar;                // full[2], conv[2], done[2], ready[2], fre[2], never; int abort
   int total;
 };
@@ -112,16 +119,16 @@ __host__ __device__ inline C8Layout c8_layout() {
   L.xbuf = o;
   o += 2 * kCW * 32 * 16;
   L.ypart = o;
-  o += 2 * kR * (kTc / 2) * kOwn * 8;
+  o += 2 * (kTc / 2) * kV * 8;
   L.wr = o;
-  o += c8_al128(kOwn * 4);
+  o += c8_al128(kV * 4);
   L.bar = o;
   o += 128;
   L.total = o < kMinSmem ? kMinSmem : o;
   return L;
 }
 
-template <bool kCache>
+template <bool kCache, int R>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_bf16_c8(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const uint16_t* __restrict__ a,
@@ -130,11 +137,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float* __restrict__ y, float* H_T, uint16_t* __restrict__ Hs, int T, int N,
                 int qk_hs, int debug, int* status) {
   constexpr int Tc = kTc;
+  constexpr int kOwn = kV / R;          // y columns a CTA owns: kOwn rank .. kOwn (rank + 1) - 1
+  constexpr int kHalves = 8 / R;        // clusters per pair (rows 8 R h .. of cluster h)
+  constexpr int kTilesPerOwner = kOwn / 16;
   extern __shared__ __align__(128) uint8_t smem[];
   const C8Layout L = c8_layout();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int rb = (int)cluster_ctarank();  // row block (and y column block) of this CTA
-  const int pair = (int)cluster_id_x();
+  const int rank = (int)cluster_ctarank();  // y column block of this CTA within its cluster
+  const int cid = (int)cluster_id_x();
+  const int pair = cid / kHalves, half = cid - (cid / kHalves) * kHalves;
+  const int rb = half * R + rank;           // row block: rows 8 rb .. 8 rb + 7
   const int b = pair / N, n = pair - (pair / N) * N;
   const int nchunks = (T + Tc - 1) / Tc;
   const size_t row_base = (size_t)b * T;
@@ -159,14 +171,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&full[i], 1);
       mbar_init(&conv[i], 32);
       mbar_init(&done[i], 32 * kCW);
-      mbar_init(&ready[i], 32 * kR);  // lanes of warp rb / 2 of every CTA
-      mbar_init(&fre[i], 32 * kR);    // producer lanes of every owner
+      mbar_init(&ready[i], 32 * R);  // lanes of the warp(s) of every CTA whose tiles I own
+      mbar_init(&fre[i], 32 * R);    // producer lanes of every owner
     }
     mbar_init(never, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (tid < kOwn) wrs[tid] = w_r[(size_t)n * kV + kOwn * rb + tid];
+  if (tid < kOwn) wrs[tid] = w_r[(size_t)n * kV + kOwn * rank + tid];
   __syncthreads();
   cluster_sync_all();  // every CTA's barriers exist before any remote arrive
 
@@ -229,30 +241,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = false;
         break;
       }
-      // y_t[16 rb + jj] = w_r ⊙ v_t plus the eight row blocks' partials, in CTA order.
+      // y_t[kOwn rank + jj]: the cluster's R row blocks' partials in CTA order, plus w_r ⊙ v_t
+      // (cluster 0 of the pair).  One cluster per pair stores y; with two (R = 4) each adds
+      // its sum into y, which the host zeroed: two addends onto an exact zero give the same
+      // bits in either order (0 + a = a, a + b = b + a).
       const int steps = min(Tc, T - cc * Tc);
       const uint16_t* vs = reinterpret_cast<const uint16_t*>(smem + st * L.stage + L.vs);
-      const float2* yp = ypart + (size_t)st * kR * (Tc / 2) * kOwn;
+      const float2* yp = ypart + (size_t)st * R * (Tc / 2) * kOwn;
       for (int idx = lane; idx < ((steps + 1) >> 1) * kOwn; idx += 32) {
         const int s2 = idx / kOwn, jj = idx - s2 * kOwn, s = 2 * s2;
-        const int col = kOwn * rb + jj;
-        float2 u[kR];
+        const int col = kOwn * rank + jj;
+        float2 u[R];
 #pragma unroll
-        for (int r = 0; r < kR; ++r) u[r] = yp[((size_t)r * (Tc / 2) + s2) * kOwn + jj];
-        float o0 = wrs[jj] * bf16_bits_to_float(vs[s * kV + col]);
+        for (int r = 0; r < R; ++r) u[r] = yp[((size_t)r * (Tc / 2) + s2) * kOwn + jj];
+        float* y0 = y + ((row_base + (size_t)cc * Tc + s) * N + n) * kV + col;
+        float o0 = half == 0 ? wrs[jj] * bf16_bits_to_float(vs[s * kV + col]) : 0.f;
 #pragma unroll
-        for (int r = 0; r < kR; ++r) o0 += u[r].x;
-        y[((row_base + (size_t)cc * Tc + s) * N + n) * kV + col] = o0;
+        for (int r = 0; r < R; ++r) o0 += u[r].x;
+        if (kHalves == 1)
+          *y0 = o0;
+        else
+          atomicAdd(y0, o0);
         if (s + 1 < steps) {
-          float o1 = wrs[jj] * bf16_bits_to_float(vs[(s + 1) * kV + col]);
+          float* y1 = y0 + (size_t)N * kV;
+          float o1 = half == 0 ? wrs[jj] * bf16_bits_to_float(vs[(s + 1) * kV + col]) : 0.f;
 #pragma unroll
-          for (int r = 0; r < kR; ++r) o1 += u[r].y;
-          y[((row_base + (size_t)cc * Tc + s + 1) * N + n) * kV + col] = o1;
+          for (int r = 0; r < R; ++r) o1 += u[r].y;
+          if (kHalves == 1)
+            *y1 = o1;
+          else
+            atomicAdd(y1, o1);
         }
       }
       // This chunk's partials are consumed: tell every CTA (each lane's own reads are done).
 #pragma unroll
-      for (int r = 0; r < kR; ++r) mbar_arrive_cluster(mapa_shared(smem_u32(&fre[st]), (uint32_t)r));
+      for (int r = 0; r < R; ++r) mbar_arrive_cluster(mapa_shared(smem_u32(&fre[st]), (uint32_t)r));
       if (issued < nchunks) {
         arm(issued);
         ok = land_and_convert(issued);
@@ -307,8 +330,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                          : make_float2(0.f, 0.f);
         }
     }
-    // Remote base address of the partial buffers of the owner of tile 2w + c (lanes c < 2).
-    const uint32_t yremote = mapa_shared(smem_u32(ypart), (uint32_t)(2 * w + (c & 1)));
+    // Lanes c < 2 send the readout of tile 2w + c: its owner within the cluster, the remote
+    // base address of the owner's partial buffers, and the tile's first local column there.
+    const int my_tile = 2 * w + (c & 1);
+    const int owner = my_tile / kTilesPerOwner;
+    const uint32_t yremote = mapa_shared(smem_u32(ypart), (uint32_t)owner);
+    const int ycol0 = 16 * (my_tile - owner * kTilesPerOwner);
 
     // A step's shared-memory operands, loaded during the step before: the gate and q of step
     // t, v and k of step t + 1 (its rank-1 term).
@@ -457,7 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float2 lo = add2(make_float2(d[0][0], d[0][1]), make_float2(d[1][0], d[1][1]));
         const float2 hi = add2(make_float2(d[0][2], d[0][3]), make_float2(d[1][2], d[1][3]));
         const uint32_t off =
-            (uint32_t)((((size_t)buf * kR + rb) * (Tc / 2) + (s >> 1)) * kOwn + g) * 8u;
+            (uint32_t)((((size_t)buf * R + rank) * (Tc / 2) + (s >> 1)) * kOwn + ycol0 + g) * 8u;
         c8_st_cluster_v2(yremote + off, lo);
         c8_st_cluster_v2(yremote + off + 64u, hi);
       }
@@ -511,9 +538,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         readout2(st, apA, apB, qA, 0u, s);
       }
-      // This chunk's partials are sent: signal both owners of my tiles, release the stage.
-      mbar_arrive_cluster(mapa_shared(smem_u32(&ready[st]), (uint32_t)(2 * w)));
-      mbar_arrive_cluster(mapa_shared(smem_u32(&ready[st]), (uint32_t)(2 * w + 1)));
+      // This chunk's partials are sent: signal the owner(s) of my two tiles, release the stage.
+      if (kTilesPerOwner == 1) {
+        mbar_arrive_cluster(mapa_shared(smem_u32(&ready[st]), (uint32_t)(2 * w)));
+        mbar_arrive_cluster(mapa_shared(smem_u32(&ready[st]), (uint32_t)(2 * w + 1)));
+      } else {
+        mbar_arrive_cluster(mapa_shared(smem_u32(&ready[st]), (uint32_t)(2 * w / kTilesPerOwner)));
+      }
       mbar_arrive(&done[st]);
     }
     if (aborted) {
@@ -548,16 +579,18 @@ bool make_map_c8(EncodeTiledFn enc, CUtensorMap* map, const void* base, int inne
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool kCache>
+// Grid of 8 CTAs per pair (8 / R clusters of R), one CTA per SM (dynamic shared memory above
+// half an SM).
+template <int R>
 cudaLaunchConfig_t c8_config(int pairs, cudaStream_t stream, cudaLaunchAttribute* attr) {
   const C8Layout L = c8_layout();
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)kR * (unsigned)pairs, 1, 1);
+  cfg.gridDim = dim3(8u * (unsigned)pairs, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = (size_t)L.total;
   cfg.stream = stream;
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = kR;
+  attr[0].val.clusterDim.x = R;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
@@ -565,19 +598,14 @@ cudaLaunchConfig_t c8_config(int pairs, cudaStream_t stream, cudaLaunchAttribute
   return cfg;
 }
 
-template <bool kCache>
+template <bool kCache, int R>
 cudaError_t c8_prepare() {
-  return cudaFuncSetAttribute(fwd_bf16_c8<kCache>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  return cudaFuncSetAttribute(fwd_bf16_c8<kCache, R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               c8_layout().total);
 }
 
-}  // namespace
-
-bool mma_c8_supports(int K, int V) { return K == kK && V == kV; }
-
-// Clusters of this kernel the current device runs at once (0 when it cannot say), cached per
-// device (under a mutex): the kernel pays only when every pair's cluster is resident.
-int mma_c8_max_clusters() {
+template <int R>
+int c8_max_clusters() {
   static int cache[64];
   static bool known[64];
   static std::mutex mu;
@@ -587,16 +615,17 @@ int mma_c8_max_clusters() {
   if (known[dev]) return cache[dev];
   int n = 0;
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = c8_config<false>(1, nullptr, attr);
-  if (c8_prepare<false>() != cudaSuccess ||
-      cudaOccupancyMaxActiveClusters(&n, fwd_bf16_c8<false>, &cfg) != cudaSuccess)
+  cudaLaunchConfig_t cfg = c8_config<R>(1, nullptr, attr);
+  if (c8_prepare<false, R>() != cudaSuccess ||
+      cudaOccupancyMaxActiveClusters(&n, fwd_bf16_c8<false, R>, &cfg) != cudaSuccess)
     n = 0;
   cache[dev] = n;
   known[dev] = true;
   return n;
 }
 
-cudaError_t launch_fwd_bf16_mma_c8(const Problem& p, EncodeTiledFn enc, cudaStream_t stream) {
+template <int R>
+cudaError_t launch_c8(const Problem& p, EncodeTiledFn enc, cudaStream_t stream) {
   CUtensorMap mq, mk, mv;
   if (!make_map_c8(enc, &mq, p.q, kK, 8, p.Nqk, p.T, p.B) ||
       !make_map_c8(enc, &mk, p.k, kK, 8, p.Nqk, p.T, p.B) ||
@@ -605,20 +634,38 @@ cudaError_t launch_fwd_bf16_mma_c8(const Problem& p, EncodeTiledFn enc, cudaStre
   cudaLaunchAttribute attr[1];
   const int pairs = p.B * p.N;
   const int qk_hs = p.Nqk == 1 ? 0 : 1;
-  if (p.Hs) {
-    cudaError_t err = c8_prepare<true>();
+  if (R < 8) {  // two clusters per pair add their sums into y
+    cudaError_t err =
+        cudaMemsetAsync(p.y, 0, sizeof(float) * (size_t)p.B * p.T * p.N * kV, stream);
     if (err != cudaSuccess) return err;
-    cudaLaunchConfig_t cfg = c8_config<true>(pairs, stream, attr);
-    return cudaLaunchKernelEx(&cfg, fwd_bf16_c8<true>, mq, mk, mv, (const uint16_t*)p.a, p.alpha,
-                              p.beta, (const uint16_t*)p.W, p.w_r, p.H0, p.y, p.H_T,
+  }
+  if (p.Hs) {
+    cudaError_t err = c8_prepare<true, R>();
+    if (err != cudaSuccess) return err;
+    cudaLaunchConfig_t cfg = c8_config<R>(pairs, stream, attr);
+    return cudaLaunchKernelEx(&cfg, fwd_bf16_c8<true, R>, mq, mk, mv, (const uint16_t*)p.a,
+                              p.alpha, p.beta, (const uint16_t*)p.W, p.w_r, p.H0, p.y, p.H_T,
                               static_cast<uint16_t*>(p.Hs), p.T, p.N, qk_hs, p.debug, p.status);
   }
-  cudaError_t err = c8_prepare<false>();
+  cudaError_t err = c8_prepare<false, R>();
   if (err != cudaSuccess) return err;
-  cudaLaunchConfig_t cfg = c8_config<false>(pairs, stream, attr);
-  return cudaLaunchKernelEx(&cfg, fwd_bf16_c8<false>, mq, mk, mv, (const uint16_t*)p.a, p.alpha,
-                            p.beta, (const uint16_t*)p.W, p.w_r, p.H0, p.y, p.H_T,
+  cudaLaunchConfig_t cfg = c8_config<R>(pairs, stream, attr);
+  return cudaLaunchKernelEx(&cfg, fwd_bf16_c8<false, R>, mq, mk, mv, (const uint16_t*)p.a,
+                            p.alpha, p.beta, (const uint16_t*)p.W, p.w_r, p.H0, p.y, p.H_T,
                             static_cast<uint16_t*>(nullptr), p.T, p.N, qk_hs, p.debug, p.status);
+}
+
+}  // namespace
+
+bool mma_c8_supports(int K, int V) { return K == kK && V == kV; }
+
+// Clusters of the R-CTA form the current device runs at once (0 when it cannot say), cached
+// per device (under a mutex): a form pays only when all its clusters are resident at once.
+int mma_c8_max_clusters(int R) { return R == 8 ? c8_max_clusters<8>() : c8_max_clusters<4>(); }
+
+cudaError_t launch_fwd_bf16_mma_c8(const Problem& p, EncodeTiledFn enc, cudaStream_t stream,
+                                   int R) {
+  return R == 8 ? launch_c8<8>(p, enc, stream) : launch_c8<4>(p, enc, stream);
 }
 
 }  // namespace m2rnn

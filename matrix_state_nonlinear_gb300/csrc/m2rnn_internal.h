@@ -160,12 +160,15 @@ __host__ __device__ inline long long tc5_cut(long long c, long long total, int T
 // SMs, readout partials exchanged through distributed shared memory): K = 64, V = 128.
 bool mma_cluster_supports(int K, int V);
 cudaError_t launch_fwd_bf16_mma_cluster(const Problem& p, EncodeTiledFn enc, cudaStream_t stream);
-// The same shape with an 8-CTA cluster per pair (eight rows per CTA, product transposed,
-// each compute warp owning 32 value columns), K = 64, V = 128.  mma_c8_max_clusters: the
-// clusters of that kernel the current device runs at once (0 when it cannot say).
+// The same shape on eight SMs per pair (eight rows per CTA, product transposed, each compute
+// warp owning 32 value columns), K = 64, V = 128: one 8-CTA cluster per pair (R = 8), or two
+// independent 4-CTA clusters per pair (R = 4) that add their halves of y into a y the
+// launcher zeroes.  mma_c8_max_clusters(R): the R-CTA clusters the current device runs at
+// once (0 when it cannot say).
 bool mma_c8_supports(int K, int V);
-int mma_c8_max_clusters();
-cudaError_t launch_fwd_bf16_mma_c8(const Problem& p, EncodeTiledFn enc, cudaStream_t stream);
+int mma_c8_max_clusters(int R);
+cudaError_t launch_fwd_bf16_mma_c8(const Problem& p, EncodeTiledFn enc, cudaStream_t stream,
+                                   int R);
 
 // Tensor-core backward (warp-level MMA, TMA-staged bf16 states), K = V = 64, then the
 // reduction.  `debug` takes the kDebug* bits; `status` is the device status word.

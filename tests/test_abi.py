@@ -70,9 +70,11 @@ def test_variant_support_table(lib):
     assert not binding.variant_supports(4, 1, 8, 1, 64, 64)
     assert binding.variant_supports(8, 1, 8, 1, 64, 128)       # 8-CTA cluster: K = 64, V = 128
     assert not binding.variant_supports(8, 1, 8, 1, 128, 128)
+    assert binding.variant_supports(9, 1, 8, 1, 64, 128)       # two 4-CTA clusters per pair
+    assert binding.variant_name(9) == "mma_sync_rows8_cluster4x2_k64_v128"
     assert binding.pick_variant(1, 65536, 15, 64, 128) == 8    # 15 clusters of 8 resident at once
-    assert binding.pick_variant(1, 65536, 16, 64, 128) == 4    # the 16th would wait: 4 SMs per pair
-    assert binding.pick_variant(8, 8192, 16, 64, 128) == 4
+    assert binding.pick_variant(1, 65536, 16, 64, 128) == 9    # the 16th cluster of 8 would wait
+    assert binding.pick_variant(8, 8192, 16, 64, 128) == 4     # 128 pairs: four SMs per pair
     assert binding.variant_name(2) is not None
 
 

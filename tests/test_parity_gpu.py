@@ -107,7 +107,7 @@ BF16_SHAPES = [(1, 1, 1, 16, 16), (1, 2, 1, 16, 32), (3, 17, 1, 16, 64), (1, 63,
 
 
 def bf16_variants():
-    return [1, 2, 3, 4, 5, 6, 7, 8]
+    return [1, 2, 3, 4, 5, 6, 7, 8, 9]
 
 
 @pytest.mark.parametrize("B,T,N,K,V", BF16_SHAPES)
@@ -291,7 +291,8 @@ def test_unsupported_and_invalid_from_binding(K, V):
 
 
 @pytest.mark.parametrize("variant,K,V", [(1, 64, 64), (2, 64, 64), (3, 128, 128), (4, 64, 128),
-                                         (5, 64, 64), (6, 64, 64), (7, 128, 128), (8, 64, 128)])
+                                         (5, 64, 64), (6, 64, 64), (7, 128, 128), (8, 64, 128),
+                                         (9, 64, 128)])
 def test_forced_wait_timeout_is_reported_and_context_survives(variant, K, V):
     inp = bf16_inputs(T=70, K=K, V=V)
     y = torch.empty((2, 70, 2, V), device=DEV)
@@ -371,12 +372,13 @@ def test_balanced_forced_timeout_with_cut_pairs():
 
 
 @pytest.mark.parametrize("variant,N,K,V", [(3, 160, 128, 128), (7, 160, 128, 128),
-                                           (8, 3, 64, 128)])
+                                           (8, 3, 64, 128), (9, 3, 64, 128)])
 def test_tcgen05_forward_cuda_graph_replay(variant, N, K, V):
     """The forward captured in a CUDA graph and replayed: every replay gives the eager bits,
     also for the balanced schedule, whose handoff tags carry the epoch of the captured launch
-    (each replay's taking block overwrites them with y before the next), and for the 8-CTA
-    cluster kernel (whose launcher queries the occupancy calculator)."""
+    (each replay's taking block overwrites them with y before the next), and for the 8-SM-per-
+    pair kernels (whose launcher queries the occupancy calculator; the two-cluster form also
+    zeroes y before its clusters add into it)."""
     wl = Workload("gr", 2, 300, N, K, V, h0="uniform")
     inp = make_inputs(wl, DEV, 31)
     y_ref, HT_ref = run_gpu(inp, variant=variant)
@@ -398,25 +400,32 @@ def test_tcgen05_forward_cuda_graph_replay(variant, N, K, V):
         assert torch.equal(y, y_ref) and torch.equal(HT, HT_ref)
 
 
+@pytest.mark.parametrize("variant", [8, 9])
 @pytest.mark.parametrize("B,T,N", [(1, 96, 2), (2, 33, 1), (1, 257, 3)])
-def test_cluster8_in_place_state_no_final_state_and_chunks(B, T, N):
-    """The 8-CTA cluster kernel (K = 64, V = 128): in-place state (H0 == H_T), no final state,
-    and a sequence run as two calls (the state carried through H_T) give the bits of one
-    call; chunk-boundary lengths (32-step chunks) included."""
+def test_cluster8_in_place_state_no_final_state_and_chunks(B, T, N, variant):
+    """The eight-SMs-per-pair kernels (K = 64, V = 128; one 8-CTA cluster, or two 4-CTA
+    clusters adding into y): in-place state (H0 == H_T), no final state, and a sequence run as
+    two calls (the state carried through H_T) give the bits of one call; chunk-boundary
+    lengths (32-step chunks) included.  The two forms differ only in the order of the readout
+    sums over rows."""
     inp = bf16_inputs(B=B, T=T, N=N, K=64, V=128)
-    y_ref, HT_ref = run_gpu(inp, variant=8)
+    y_ref, HT_ref = run_gpu(inp, variant=variant)
     state = inp["H0"].clone()
     inp2 = dict(inp)
     inp2["H0"] = state
     y = torch.empty_like(y_ref)
-    pkg.m2rnn_forward(inp2, y=y, H_T=state, variant=8)       # H0 == H_T
+    pkg.m2rnn_forward(inp2, y=y, H_T=state, variant=variant)       # H0 == H_T
     assert pkg.stream_status() == binding.OK
     assert torch.equal(state, HT_ref) and torch.equal(y, y_ref)
-    y3, _ = run_gpu(inp, variant=8, H_T=False)               # H_T = NULL
+    y3, _ = run_gpu(inp, variant=variant, H_T=False)               # H_T = NULL
     assert torch.equal(y3, y_ref)
     cut = 64 if T > 64 else T // 2
-    ya, Ha = run_gpu(sub_t(inp, 0, cut), variant=8)
+    ya, Ha = run_gpu(sub_t(inp, 0, cut), variant=variant)
     rest = sub_t(inp, cut, T)
     rest["H0"] = Ha
-    yb, Hb = run_gpu(rest, variant=8)
+    yb, Hb = run_gpu(rest, variant=variant)
     assert torch.equal(torch.cat([ya, yb], dim=1), y_ref) and torch.equal(Hb, HT_ref)
+    if variant == 9:   # the same state arithmetic as one 8-CTA cluster per pair
+        y8, H8 = run_gpu(inp, variant=8)
+        assert torch.equal(H8, HT_ref)
+        assert float((y8 - y_ref).abs().max()) <= 1e-5

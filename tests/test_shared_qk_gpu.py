@@ -40,7 +40,8 @@ CASES = [("f32", 0, (2, 33, 3, 8, 8)), ("bf16", 1, (2, 70, 3, 32, 32)), ("bf16",
          ("bf16", 2, (2, 97, 3, 64, 64)), ("bf16", 2, (1, 66, 4, 16, 32)), ("bf16", 3, (2, 40, 3, 128, 128)),
          ("bf16", 4, (1, 150, 3, 64, 128)), ("bf16", 5, (2, 97, 3, 64, 64)),
          ("bf16", 5, (1, 66, 4, 32, 48)), ("bf16", 6, (2, 97, 3, 64, 64)),
-         ("bf16", 6, (1, 70, 2, 64, 16)), ("bf16", 8, (1, 150, 3, 64, 128))]
+         ("bf16", 6, (1, 70, 2, 64, 16)), ("bf16", 8, (1, 150, 3, 64, 128)),
+         ("bf16", 9, (1, 150, 3, 64, 128))]
 
 
 @pytest.mark.parametrize("dtype,variant,shape", CASES)
