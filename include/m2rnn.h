@@ -130,10 +130,12 @@ m2rnn_status m2rnn_forward_bf16_qk(const uint16_t* q, const uint16_t* k, const u
  *                           rounding of H_t, i.e. exactly the tensor-core operand
  *                           the next step multiplies by W (B·N·T·K·V·2 bytes).
  *   Hs is required when T > 0 (16-byte aligned on the bf16 entry).  The bf16 entry
- *   takes the pipelined warp-MMA kernel for K a multiple of 16 with K <= 64 and V in
- *   {16, 32, 64}, and the row-warp kernel for every other 1 <= K <= 128 with V a
- *   multiple of 16 up to 128 (UNSUPPORTED otherwise); the fp32 entry supports
- *   1 <= K, V <= 128.
+ *   runs the state-keeping form of a forward kernel, with that kernel's arithmetic:
+ *   the pipelined warp-MMA kernel for K a multiple of 16 up to 64 with V in
+ *   {16, 32, 64}; the tcgen05 kernel for K = V = 128; eight SMs per pair (or the
+ *   4-CTA cluster kernel when their clusters do not all fit) for K = 64, V = 128;
+ *   and the row-warp kernel for every other 1 <= K <= 128 with V a multiple of 16
+ *   up to 128 (UNSUPPORTED otherwise).  The fp32 entry supports 1 <= K, V <= 128.
  */
 m2rnn_status m2rnn_forward_train_f32(const float* q, const float* k, const float* v,
                                      const float* a, const float* alpha, const float* beta,
