@@ -104,12 +104,13 @@ def test_backward_without_dHT_and_without_dH0():
 def test_forward_train_keeps_states_and_matches_plain_forward():
     # The bf16 state-keeping forward runs the pipelined kernel's arithmetic (forward variant
     # 2) for K, V <= 64 with K % 16 == 0, the tcgen05 kernel's (variant 3, or its balanced
-    # form 7 above two pairs per SM) for K = V = 128, the 8-CTA cluster kernel's (variant 8,
-    # while every pair's cluster is resident at once, else the 4-CTA one, 4) for K = 64,
-    # V = 128, and the row-warp kernel's (variant 1) otherwise.
+    # form 7 above two pairs per SM) for K = V = 128, eight SMs per pair for K = 64, V = 128
+    # (one 8-CTA cluster, variant 8, while all fit; else two 4-CTA clusters, variant 9; else the
+    # 4-CTA kernel, 4), and the row-warp kernel's (variant 1) otherwise.
     for dtype, shape, fwd_variant in [("f32", (2, 37, 3, 8, 24), 0), ("bf16", (2, 150, 3, 64, 64), 2),
                                       ("bf16", (1, 70, 2, 32, 16), 2),
                                       ("bf16", (2, 45, 2, 64, 128), 8),   # 8-CTA cluster
+                                      ("bf16", (1, 41, 16, 64, 128), 9),  # 16 pairs: 2 x 4-CTA
                                       ("bf16", (1, 33, 2, 128, 128), 3),   # tcgen05
                                       # ragged K and V off the power-of-two grid (row-warp)
                                       ("bf16", (2, 40, 2, 24, 48), 1),
