@@ -82,6 +82,7 @@ KERNEL_SOURCES = {
     "backward_tcc_k64_v64": ["m2rnn_bwd_bf16_tcc.cu"],
     "backward_simt": ["m2rnn_bwd_f32.cu"],
     "backward_tc_v128": ["m2rnn_bwd_bf16_tc128.cu"],
+    "backward_tc_v128_t": ["m2rnn_bwd_bf16_tc128t.cu"],
     "decode_bf16_mma": ["m2rnn_decode.cu"],
     "decode_bf16_persist": ["m2rnn_decode.cu"],
     "conv_silu": ["m2rnn_block.cu"],
@@ -646,11 +647,13 @@ def main_train(args, wl):
     fwd_bytes = wl.units * (e * K * V + e * (2 * K + V + 1) + 4 * V)
     achieved = flops / (bwd_ms / 1e3) / 1e12
     mma = wl.dtype == "bf16" and K == 64 and V == 64 and args.variant in (0, 2, 3, 4, 5)
-    v128 = wl.dtype == "bf16" and V == 128 and K % 16 == 0 and args.variant in (0, 6)
+    v128 = wl.dtype == "bf16" and V == 128 and K % 16 == 0 and args.variant in (0, 6, 7)
+    # V = 128: the products transposed for K <= 64 (variant 7, the automatic choice there)
+    v128t = v128 and (args.variant == 7 or (args.variant == 0 and K <= 64))
     if mma or v128:   # bf16 tensor-core products: the measured bf16 dense peak
         peak, bound = float(peaks["bf16_tflops"]), "tensor"
         psrc = f"{peak_src} bf16 dense burst (kernel timed alone)"
-        kname = "backward_tc_v128" if v128 else {
+        kname = ("backward_tc_v128_t" if v128t else "backward_tc_v128") if v128 else {
             2: "backward_mma_k64_v64", 4: "backward_tc8_k64_v64",
             3: "backward_tc_k64_v64"}.get(args.variant, "backward_tcc_k64_v64")
     else:     # fp32 SIMT arithmetic: SMs x 128 FMA lanes x 2 flop x max SM clock

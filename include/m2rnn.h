@@ -182,16 +182,19 @@ size_t m2rnn_backward_workspace_bytes(int B, int T, int N, int Nqk, int K, int V
  * Errors: INVALID_ARG for a null required pointer (q, k, v, a, Hs, dy, dq, dk, dv,
  * da are required only when T > 0) or a bad size; UNSUPPORTED for K or V > 128.
  * The bf16 entry takes bf16 q, k, v, a, W; its `variant` is 0 (automatic: 5 when
- * K = V = 64 and T > 0, 6 when V = 128, K is a multiple of 16 and T > 0, else 1),
+ * K = V = 64 and T > 0, 7 when V = 128, K is a multiple of 16 up to 64 and T > 0,
+ * 6 when V = 128, K is a multiple of 16 above 64 and T > 0, else 1),
  * 1 (SIMT kernel, fp32 arithmetic, any K, V <= 128),
  * 2 (H_{t-1} W, D_t W^T and H_{t-1}^T D_t as bf16 warp MMAs with fp32 accumulation) or
  * 3 (H_{t-1} W and H_{t-1}^T D_t on the 5th-generation tensor cores with tensor-memory
  * accumulators, D_t W^T as warp MMAs), 4 (variant 3 with eight compute warps) or 5 (all
  * three products on the 5th-generation tensor cores, the chain product D_t W^T included)
  * or 6 (V = 128: every product on the 5th-generation tensor cores, rows padded to 128;
- * D_t enters the products, dk and dv included, rounded to bf16).
- * Variants 2 to 5 need K = V = 64, variant 6 V = 128 and K a multiple of 16
- * (UNSUPPORTED otherwise); all of them need q, k, v, W, Hs, dy, dv, H0, dH_T, dH0
+ * D_t enters the products, dk and dv included, rounded to bf16) or 7 (variant 6 with the
+ * recurrence's products transposed, so that the tensor-memory lanes run over the 128
+ * columns and no row is padding; K <= 64).
+ * Variants 2 to 5 need K = V = 64, variant 6 V = 128 and K a multiple of 16, variant 7
+ * V = 128 and K a multiple of 16 up to 64 (UNSUPPORTED otherwise); all of them need q, k, v, W, Hs, dy, dv, H0, dH_T, dH0
  * 16-byte aligned.  Bits 8 and up
  * of `variant` are test hooks (0).
  */

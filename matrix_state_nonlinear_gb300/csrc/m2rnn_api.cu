@@ -454,12 +454,14 @@ m2rnn_status m2rnn_backward_bf16(const uint16_t* q, const uint16_t* k, const uin
   if (st != M2RNN_OK) return st;
   const int debug = variant >> 8;
   int base = variant & 0xff;
-  if (base < 0 || base > 6) return M2RNN_ERR_INVALID_ARG;
+  if (base < 0 || base > 7) return M2RNN_ERR_INVALID_ARG;
   const bool mma_ok = bwd_mma_supports(K, V) && T > 0;
   const bool tc128_ok = bwd_tc128_supports(K, V) && T > 0;
-  if (base == 0) base = mma_ok ? 5 : tc128_ok ? 6 : 1;
+  const bool tc128t_ok = bwd_tc128t_supports(K, V) && T > 0;
+  if (base == 0) base = mma_ok ? 5 : tc128t_ok ? 7 : tc128_ok ? 6 : 1;
   if (base >= 2 && base <= 5 && !mma_ok) return M2RNN_ERR_UNSUPPORTED;
   if (base == 6 && !tc128_ok) return M2RNN_ERR_UNSUPPORTED;
+  if (base == 7 && !tc128t_ok) return M2RNN_ERR_UNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (base == 1) return launch_bwd_simt_bf16(p, s) == cudaSuccess ? M2RNN_OK : M2RNN_ERR_CUDA;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(W, 16) ||
@@ -472,7 +474,8 @@ m2rnn_status m2rnn_backward_bf16(const uint16_t* q, const uint16_t* k, const uin
   EncodeTiledFn enc = encode_fn();
   if (!status || !enc) return M2RNN_ERR_CUDA;
   const cudaError_t err =
-      base == 6   ? launch_bwd_bf16_tc128(p, enc, debug, status, s)
+      base == 7   ? launch_bwd_bf16_tc128t(p, enc, debug, status, s)
+      : base == 6 ? launch_bwd_bf16_tc128(p, enc, debug, status, s)
       : base == 5 ? launch_bwd_bf16_tcc(p, enc, debug, status, s)
       : base >= 3 ? launch_bwd_bf16_tc(p, enc, debug, status, base == 4 ? 8 : 4, s)
                   : launch_bwd_bf16_mma(p, enc, debug, status, s);

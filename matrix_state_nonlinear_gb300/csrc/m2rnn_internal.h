@@ -188,6 +188,11 @@ cudaError_t launch_bwd_bf16_tcc(const BackwardProblem& p, EncodeTiledFn enc, int
 bool bwd_tc128_supports(int K, int V);
 cudaError_t launch_bwd_bf16_tc128(const BackwardProblem& p, EncodeTiledFn enc, int debug,
                                   int* status, cudaStream_t stream);
+// The same backward for V = 128 and K <= 64 (a multiple of 16) with the recurrence's products
+// transposed (M over the 128 value columns, N = K), so no state row is padding.
+bool bwd_tc128t_supports(int K, int V);
+cudaError_t launch_bwd_bf16_tc128t(const BackwardProblem& p, EncodeTiledFn enc, int debug,
+                                   int* status, cudaStream_t stream);
 
 // One decode step (T = 1) on the warp MMA: K % 16 == 0, K <= 128, V in {16, 32, 64, 128}.
 // Uses q, k, v, a, alpha, beta, W, w_r, H0 (state in, may be null), H_T (state out, may

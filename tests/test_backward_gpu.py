@@ -171,11 +171,12 @@ BF16_SHAPES = [(1, 1, 1, 16, 16), (2, 65, 3, 64, 64), (1, 130, 2, 32, 32), (2, 4
 def bwd_variants(K, V):
     # 1: SIMT (any shape); 2: warp-MMA kernel; 3, 4: tcgen05 kernels with 4 or 8 compute
     # warps; 5: every product on tcgen05, the chain included (K = V = 64); 6: every product
-    # on tcgen05 for V = 128 (K a multiple of 16)
+    # on tcgen05 for V = 128 (K a multiple of 16, rows padded); 7: the same with the
+    # recurrence's products transposed (V = 128, K <= 64)
     if (K, V) == (64, 64):
         return [1, 2, 3, 4, 5]
     if V == 128 and K % 16 == 0:
-        return [1, 6]
+        return [1, 6, 7] if K <= 64 else [1, 6]
     return [1]
 
 
@@ -188,23 +189,23 @@ def test_backward_bf16_matches_oracle(shape, h0):
 
 
 def kv_of(variant):
-    return (64, 128) if variant == 6 else (64, 64)
+    return (64, 128) if variant in (6, 7) else (64, 64)
 
 
-@pytest.mark.parametrize("variant", [1, 2, 3, 4, 5, 6])
+@pytest.mark.parametrize("variant", [1, 2, 3, 4, 5, 6, 7])
 def test_backward_bf16_shared_qk(variant):
     _, _, g, errs = run_case("bf16", 2, 50, 4, *kv_of(variant), shared=True, variant=variant)
     assert g["dq"].shape[2] == 1
     assert max(errs.values()) <= TOL["bf16"], errs
 
 
-@pytest.mark.parametrize("variant", [2, 3, 4, 5, 6])
+@pytest.mark.parametrize("variant", [2, 3, 4, 5, 6, 7])
 def test_backward_mma_without_dHT(variant):
     _, _, _, errs = run_case("bf16", 2, 37, 2, *kv_of(variant), with_dHT=False, variant=variant)
     assert max(errs.values()) <= TOL["bf16"], errs
 
 
-@pytest.mark.parametrize("variant", [2, 3, 4, 5, 6])
+@pytest.mark.parametrize("variant", [2, 3, 4, 5, 6, 7])
 def test_backward_mma_close_to_simt(variant):
     """The kernels differentiate the same kept states; they differ only by rounding
     (bf16 D in the MMA products vs fp32 SIMT sums)."""
@@ -219,7 +220,7 @@ def test_backward_mma_close_to_simt(variant):
         assert rel_err(g2[n], g1[n].double().cpu().numpy()) <= 1e-2, n
 
 
-@pytest.mark.parametrize("variant", [2, 3, 4, 5, 6])
+@pytest.mark.parametrize("variant", [2, 3, 4, 5, 6, 7])
 def test_backward_mma_forced_timeout_is_reported(variant):
     K, V = kv_of(variant)
     wl = Workload("to", 2, 20, 2, K, V, h0="uniform")
@@ -270,8 +271,11 @@ def abs_err(got, want):
     # the training workload's length and head shape on the tensor-core backward (auto = 5)
     ((1, 16384, 4, 64, 64), False, 0),
     ((1, 16384, 4, 64, 64), True, 0),
-    # V = 128 at long T on its tensor-core backward (auto = 6), per-head and shared q, k
+    # V = 128 at long T on its tensor-core backwards (auto = 7 for K <= 64, else 6; both
+    # forms at K = 64), per-head and shared q, k
     ((1, 4096, 2, 64, 128), False, 0),
+    ((1, 4096, 2, 64, 128), False, 6),
+    ((1, 1024, 3, 32, 128), True, 7),
     ((1, 2048, 2, 128, 128), True, 0),
 ])
 def test_backward_bf16_at_training_length(shape, shared, variant):
